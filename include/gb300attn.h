@@ -1,0 +1,189 @@
+/*
+ * gb300attn — exact packed-THD attention hot path for one GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only.  Unless stated otherwise every
+ * pointer is a DEVICE pointer owned by the caller; the library allocates no
+ * device memory and keeps no state between calls.  Every call validates its
+ * arguments on the host first and returns ATTN_ERR_INVALID_ARG /
+ * ATTN_ERR_UNSUPPORTED without launching anything; otherwise it enqueues its
+ * kernels asynchronously on `stream` and returns ATTN_OK (or ATTN_ERR_CUDA if
+ * a launch failed).  Nothing synchronises implicitly except
+ * attn_read_device_status.
+ *
+ * Notation (pages: "Context parallelism and ring attention", sections "The
+ * attention problem", "Online softmax", "Causal attention", "Load balance";
+ * "JAX: Context-Parallel Attention with TransformerEngine", sections 1
+ * "Packed THD inputs", 3 "Fused attention call", 4 "Striped load balancing
+ * and sharding"; "Implementation:NVIDIA TransformerEngine JAX Cpp
+ * Attention", "I/O Contract"):
+ *
+ *   q            bf16 [b, s_q, h_q, d]   contiguous ("THD" separate-QKV layout)
+ *   k, v         bf16 [b, s_kv, h_kv, d] contiguous
+ *   segment ids  int32 [b, s]   0 = padding slot, >0 = segment id
+ *   segment pos  int32 [b, s]   position of the token inside its segment
+ *   visible(i,j) <=> ids_q[i] == ids_kv[j] != 0 and pos_kv[j] <= pos_q[i]
+ *                    and (window_left < 0 or pos_q[i] - pos_kv[j] <= window_left)
+ *   out          O = softmax(scale * Q K^T + M) V   per head, M = 0 / -inf
+ *   lse          fp32 [b, h_q, s_q], natural log of the softmax denominator
+ *                including the scale; rows with no visible key: O = 0, lse = -inf
+ *   GQA          query head h reads kv head h / (h_q / h_kv)
+ */
+#ifndef GB300ATTN_H
+#define GB300ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GB300ATTN_API __attribute__((visibility("default")))
+#else
+#define GB300ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t; NULL = legacy default stream */
+
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or flag; nothing launched */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64,128}) */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
+  ATTN_ERR_TIMEOUT = 4      /* a device-side bounded wait gave up (see attn_read_device_status) */
+};
+
+enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
+
+/* Forward attention parameters.
+ * Page: "Context parallelism and ring attention", section "The attention
+ * problem" (O = softmax(QK^T/sqrt(H) + M) V); TE tutorial section 3 (packed
+ * THD, PADDING_CAUSAL mask, window (left, 0), scaling_factor); TE Cpp
+ * Attention page, "I/O Contract" (outputs: output, softmax_aux).
+ *
+ *  q, k, v        bf16, layouts above; 16-byte aligned base pointers.
+ *  q_segment_ids, q_segment_pos    int32 [b, s_q]
+ *  kv_segment_ids, kv_segment_pos  int32 [b, s_kv]  (may alias the q ones)
+ *  b, s_q, s_kv, h_q, h_kv, d      sizes; h_q % h_kv == 0; d in {64, 128};
+ *                                  s_q, s_kv >= 1 (ragged lengths allowed)
+ *  window_left    -1 = unlimited, else >= 0 (inclusive, W+1 keys incl. self)
+ *  window_right   must be 0 (causal)
+ *  scale          softmax scale, usually 1/sqrt(d)
+ *  out            bf16 [b, s_q, h_q, d], or fp32 when out_fp32 != 0
+ *  lse            fp32 [b, h_q, s_q]
+ *  workspace      device scratch of at least attn_fwd_workspace_bytes() bytes,
+ *                 256-byte aligned; contents need no initialisation and are
+ *                 overwritten (the tile plan and the device status word).
+ */
+typedef struct attn_fwd_params {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* q_segment_ids;
+  const int32_t* q_segment_pos;
+  const int32_t* kv_segment_ids;
+  const int32_t* kv_segment_pos;
+  int64_t b, s_q, s_kv, h_q, h_kv, d;
+  int32_t window_left;
+  int32_t window_right;
+  float scale;
+  int32_t out_fp32;
+  void* out;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+} attn_fwd_params;
+
+/* Backward parameters: gradient of sum(out * dout) with respect to q, k, v
+ * (TE tutorial section 5 differentiates jnp.vdot(out, dout)).  The forward
+ * fields mean the same as in attn_fwd_params (out_fp32 must be 0), plus:
+ *  out      bf16 [b, s_q, h_q, d]  forward output (as written by attn_fwd)
+ *  lse      fp32 [b, h_q, s_q]     forward LSE (as written by attn_fwd)
+ *  dout     bf16 [b, s_q, h_q, d]
+ *  dq       bf16 [b, s_q, h_q, d]     (written)
+ *  dk, dv   bf16 [b, s_kv, h_kv, d]   (written; summed over the GQA group)
+ *  workspace  >= attn_bwd_workspace_bytes() bytes, 256-byte aligned; holds the
+ *             fp32 dQ accumulator, D = rowsum(dO * O) and the tile plan.
+ */
+typedef struct attn_bwd_params {
+  attn_fwd_params fwd;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+} attn_bwd_params;
+
+/* Scratch sizes (bytes) for the given problem; 0 on invalid sizes. */
+GB300ATTN_API size_t attn_fwd_workspace_bytes(const attn_fwd_params* p);
+GB300ATTN_API size_t attn_bwd_workspace_bytes(const attn_bwd_params* p);
+
+/* Forward attention (tile plan + fused tcgen05 kernel).  See attn_fwd_params. */
+GB300ATTN_API int attn_fwd(const attn_fwd_params* p, attn_stream_t stream);
+
+/* Backward attention: D = rowsum(dO*O), fused dQ/dK/dV kernel, dQ finalise. */
+GB300ATTN_API int attn_bwd(const attn_bwd_params* p, attn_stream_t stream);
+
+/* Online-softmax merge of a partial result into an accumulator, per row-head.
+ * Page: "Context parallelism and ring attention", section "Online softmax"
+ * (m' = max(m, m_b); z' = e^(m-m') z + e^(m_b-m') z_b; u' likewise; output
+ * u'/z'), applied to finished partials (O, LSE) == (u/z, m + ln z):
+ *   M = max(l_acc, l_blk); if M == -inf the row stays (0, -inf); else
+ *   l' = M + ln(e^(l_acc-M) + e^(l_blk-M)),
+ *   O' = e^(l_acc-l') O_acc + e^(l_blk-l') O_blk.
+ *  out_acc   fp32 [b, s, h, d]  accumulator (read; written unless out_final)
+ *  lse_acc   fp32 [b, h, s]     accumulator LSE (read and written)
+ *  out_blk   [b, s, h, d], fp32 or bf16 (blk_is_bf16 != 0)
+ *  lse_blk   fp32 [b, h, s]
+ *  out_final NULL, or bf16 [b, s, h, d]: then O' goes there (as bf16, RNE)
+ *            instead of into out_acc.
+ * A row whose accumulator LSE is -inf takes the block as is (its out_acc
+ * value is not read).  Pointers 16-byte aligned; d % 8 == 0.
+ */
+GB300ATTN_API int attn_merge_partial(float* out_acc, float* lse_acc, const void* out_blk,
+                       const float* lse_blk, int blk_is_bf16, void* out_final,
+                       int64_t b, int64_t s, int64_t h, int64_t d, attn_stream_t stream);
+
+/* Causal load-balancing reorder along the sequence axis of a tensor viewed as
+ * [outer, s, inner_bytes] (q/k/v/out: inner = h*d*2; ids/pos: outer = b,
+ * inner = 4; lse [b, h, s]: outer = b*h, inner = 4).
+ * Page: "Context parallelism and ring attention", section "Load balance"
+ * (pair early and late pieces on each device); TE tutorial section 4.
+ *  strategy DUAL_CHUNK: 2R chunks of s/(2R); shard r = [chunk r, chunk 2R-1-r],
+ *           shards in order r = 0..R-1.  Needs s % (2R) == 0.
+ *  strategy STRIPED: stripes of stripe_size tokens; stripe t -> shard t mod R,
+ *           kept in order.  Needs s % (R*stripe_size) == 0.
+ *  out[o, i, :] = in[o, src(i), :].  in != out (no in-place).
+ */
+GB300ATTN_API int reorder_causal_lb(const void* in, void* out, int64_t outer, int64_t s, int64_t inner_bytes,
+                      int strategy, int cp_size, int stripe_size, attn_stream_t stream);
+
+/* Inverse of reorder_causal_lb with the same arguments: out[o, src(i), :] = in[o, i, :]. */
+GB300ATTN_API int inverse_reorder_causal_lb(const void* in, void* out, int64_t outer, int64_t s,
+                              int64_t inner_bytes, int strategy, int cp_size, int stripe_size,
+                              attn_stream_t stream);
+
+/* Debug hook: the per-tile work classification the forward pass uses.
+ * Page: "Context parallelism and ring attention", section "Causal attention"
+ * (skip future blocks, process fully valid blocks, mask overlapping ones).
+ *  classes  uint8 [b, ceil(s_q/128), ceil(s_kv/128)]: 0 SKIP, 1 PARTIAL, 2 FULL
+ *  ranges   int32 [b, ceil(s_q/128), 2]: first / last non-SKIP kv tile (0, -1 if none)
+ * Uses p->workspace like attn_fwd.
+ */
+GB300ATTN_API int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,
+                   attn_stream_t stream);
+
+/* Synchronises `stream`, then returns the device status word kept at the start
+ * of `workspace` by the last attn_fwd / attn_bwd that used it: ATTN_OK, or
+ * ATTN_ERR_TIMEOUT if a bounded device-side wait gave up (the kernel then
+ * stopped early and its outputs are undefined). */
+GB300ATTN_API int attn_read_device_status(const void* workspace, attn_stream_t stream);
+
+/* Static description of a status code. */
+GB300ATTN_API const char* attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300ATTN_H */

@@ -1,0 +1,273 @@
+"""gb300attn: exact packed-THD attention for one GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI in ``include/gb300attn.h``.  This module
+only marshals arguments (tensor pointers, sizes, the current CUDA stream) and
+allocates result tensors with PyTorch; every step of the computation runs in
+the library's CUDA kernels.  There is no CPU fallback: every call raises if
+the shared library is missing or a tensor is not on a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgb300attn.so")
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+DUAL_CHUNK, STRIPED = 0, 1
+TILE = 128
+
+EXPORTS = (
+    "attn_fwd_workspace_bytes", "attn_bwd_workspace_bytes", "attn_fwd", "attn_bwd",
+    "attn_merge_partial", "reorder_causal_lb", "inverse_reorder_causal_lb", "attn_tile_plan",
+    "attn_read_device_status", "attn_status_string",
+)
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+class FwdParams(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("q_segment_ids", ctypes.c_void_p), ("q_segment_pos", ctypes.c_void_p),
+        ("kv_segment_ids", ctypes.c_void_p), ("kv_segment_pos", ctypes.c_void_p),
+        ("b", ctypes.c_int64), ("s_q", ctypes.c_int64), ("s_kv", ctypes.c_int64),
+        ("h_q", ctypes.c_int64), ("h_kv", ctypes.c_int64), ("d", ctypes.c_int64),
+        ("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("out_fp32", ctypes.c_int32),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class BwdParams(ctypes.Structure):
+    _fields_ = [
+        ("fwd", FwdParams), ("dout", ctypes.c_void_p), ("dq", ctypes.c_void_p),
+        ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+    ]
+
+
+_lib_handle = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        h = ctypes.CDLL(LIB_PATH)
+        vp, i64, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        h.attn_fwd_workspace_bytes.argtypes = [ctypes.POINTER(FwdParams)]
+        h.attn_fwd_workspace_bytes.restype = ctypes.c_size_t
+        h.attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(BwdParams)]
+        h.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        h.attn_fwd.argtypes = [ctypes.POINTER(FwdParams), vp]
+        h.attn_fwd.restype = c_int
+        h.attn_bwd.argtypes = [ctypes.POINTER(BwdParams), vp]
+        h.attn_bwd.restype = c_int
+        h.attn_merge_partial.argtypes = [vp, vp, vp, vp, c_int, vp, i64, i64, i64, i64, vp]
+        h.attn_merge_partial.restype = c_int
+        for name in ("reorder_causal_lb", "inverse_reorder_causal_lb"):
+            f = getattr(h, name)
+            f.argtypes = [vp, vp, i64, i64, i64, c_int, c_int, c_int, vp]
+            f.restype = c_int
+        h.attn_tile_plan.argtypes = [ctypes.POINTER(FwdParams), vp, vp, vp]
+        h.attn_tile_plan.restype = c_int
+        h.attn_read_device_status.argtypes = [vp, vp]
+        h.attn_read_device_status.restype = c_int
+        h.attn_status_string.argtypes = [c_int]
+        h.attn_status_string.restype = ctypes.c_char_p
+        _lib_handle = h
+    return _lib_handle
+
+
+def status_string(code: int) -> str:
+    return lib().attn_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != ATTN_OK:
+        raise AttnError(code, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("gb300attn runs on CUDA tensors only")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("gb300attn expects contiguous tensors")
+
+
+def _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, out_fp32):
+    b, s_q, hq, d = q.shape
+    _, s_kv, hkv, _ = k.shape
+    p = FwdParams()
+    p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    p.q_segment_ids, p.q_segment_pos = q_ids.data_ptr(), q_pos.data_ptr()
+    p.kv_segment_ids, p.kv_segment_pos = kv_ids.data_ptr(), kv_pos.data_ptr()
+    p.b, p.s_q, p.s_kv, p.h_q, p.h_kv, p.d = b, s_q, s_kv, hq, hkv, d
+    p.window_left, p.window_right = int(window_left), 0
+    p.scale = float(d ** -0.5 if scale is None else scale)
+    p.out_fp32 = 1 if out_fp32 else 0
+    p.out = out.data_ptr() if out is not None else None
+    p.lse = lse.data_ptr() if lse is not None else None
+    return p
+
+
+def workspace_bytes_fwd(q, k, q_ids, q_pos, kv_ids=None, kv_pos=None, window_left=-1,
+                        scale=None) -> int:
+    kv_ids = q_ids if kv_ids is None else kv_ids
+    kv_pos = q_pos if kv_pos is None else kv_pos
+    p = _fwd_params(q, k, k, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, q, q, False)
+    return int(lib().attn_fwd_workspace_bytes(ctypes.byref(p)))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: int = -1,
+             scale: Optional[float] = None, out=None, lse=None, out_fp32: bool = False,
+             workspace: Optional[torch.Tensor] = None):
+    """Forward attention.  Returns (out [b,s_q,Hq,d], lse fp32 [b,Hq,s_q]).
+
+    q bf16 [b,s_q,Hq,d]; k, v bf16 [b,s_kv,Hkv,d]; ids/pos int32 [b,s].
+    kv_ids / kv_pos default to the query descriptor (self-attention).
+    """
+    kv_ids = q_ids if kv_ids is None else kv_ids
+    kv_pos = q_pos if kv_pos is None else kv_pos
+    _need_cuda(q, k, v, q_ids, q_pos, kv_ids, kv_pos, out, lse, workspace)
+    b, s_q, hq, d = q.shape
+    if out is None:
+        out = torch.empty(b, s_q, hq, d, device=q.device,
+                          dtype=torch.float32 if out_fp32 else torch.bfloat16)
+    if lse is None:
+        lse = torch.empty(b, hq, s_q, device=q.device, dtype=torch.float32)
+    p = _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, out_fp32)
+    need = lib().attn_fwd_workspace_bytes(ctypes.byref(p))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    _check(lib().attn_fwd(ctypes.byref(p), _stream(q.device)), "attn_fwd")
+    return out, lse
+
+
+def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
+             window_left: int = -1, scale: Optional[float] = None, dq=None, dk=None, dv=None,
+             workspace: Optional[torch.Tensor] = None):
+    """Backward attention.  Returns (dq, dk, dv) in bf16."""
+    kv_ids = q_ids if kv_ids is None else kv_ids
+    kv_pos = q_pos if kv_pos is None else kv_pos
+    _need_cuda(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids, kv_pos, workspace)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    p = BwdParams()
+    p.fwd = _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, False)
+    p.dout, p.dq, p.dk, p.dv = dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    need = lib().attn_bwd_workspace_bytes(ctypes.byref(p))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    p.fwd.workspace, p.fwd.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    _check(lib().attn_bwd(ctypes.byref(p), _stream(q.device)), "attn_bwd")
+    return dq, dk, dv
+
+
+def workspace_bytes_bwd(q, k, q_ids, q_pos, window_left=-1) -> int:
+    p = BwdParams()
+    p.fwd = _fwd_params(q, k, k, q_ids, q_pos, q_ids, q_pos, window_left, None, q, q, False)
+    return int(lib().attn_bwd_workspace_bytes(ctypes.byref(p)))
+
+
+def attn_merge_partial(out_acc, lse_acc, out_blk, lse_blk, out_final=None):
+    """Online-softmax merge of (out_blk, lse_blk) into (out_acc, lse_acc), in place.
+
+    out_acc fp32 [b,s,H,d]; lse_* fp32 [b,H,s]; out_blk fp32 or bf16.
+    With ``out_final`` (bf16 [b,s,H,d]) the merged output goes there instead.
+    """
+    _need_cuda(out_acc, lse_acc, out_blk, lse_blk, out_final)
+    b, s, h, d = out_acc.shape
+    rc = lib().attn_merge_partial(
+        _ptr(out_acc), _ptr(lse_acc), _ptr(out_blk), _ptr(lse_blk),
+        1 if out_blk.dtype == torch.bfloat16 else 0, _ptr(out_final), b, s, h, d,
+        _stream(out_acc.device))
+    _check(rc, "attn_merge_partial")
+    return (out_final if out_final is not None else out_acc), lse_acc
+
+
+def _seq_view(x: torch.Tensor, seq_dim: int):
+    outer = 1
+    for n in x.shape[:seq_dim]:
+        outer *= n
+    inner = x.element_size()
+    for n in x.shape[seq_dim + 1:]:
+        inner *= n
+    return outer, x.shape[seq_dim], inner
+
+
+def reorder_causal_lb(x, strategy: int = DUAL_CHUNK, cp_size: int = 4, stripe_size: int = 1,
+                      seq_dim: int = 1, out=None):
+    """Causal load-balancing reorder along ``seq_dim`` (returns a new tensor)."""
+    _need_cuda(x, out)
+    out = torch.empty_like(x) if out is None else out
+    outer, s, inner = _seq_view(x, seq_dim)
+    rc = lib().reorder_causal_lb(_ptr(x), _ptr(out), outer, s, inner, strategy, cp_size,
+                                 stripe_size, _stream(x.device))
+    _check(rc, "reorder_causal_lb")
+    return out
+
+
+def inverse_reorder_causal_lb(x, strategy: int = DUAL_CHUNK, cp_size: int = 4,
+                              stripe_size: int = 1, seq_dim: int = 1, out=None):
+    """Inverse of :func:`reorder_causal_lb` with the same arguments."""
+    _need_cuda(x, out)
+    out = torch.empty_like(x) if out is None else out
+    outer, s, inner = _seq_view(x, seq_dim)
+    rc = lib().inverse_reorder_causal_lb(_ptr(x), _ptr(out), outer, s, inner, strategy, cp_size,
+                                         stripe_size, _stream(x.device))
+    _check(rc, "inverse_reorder_causal_lb")
+    return out
+
+
+def attn_tile_plan(q, k, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: int = -1,
+                   workspace=None):
+    """Per-tile classes (uint8 [b,nq,nk]: 0 SKIP, 1 PARTIAL, 2 FULL) and q ranges."""
+    kv_ids = q_ids if kv_ids is None else kv_ids
+    kv_pos = q_pos if kv_pos is None else kv_pos
+    _need_cuda(q, k, q_ids, q_pos, kv_ids, kv_pos)
+    b, s_q = q.shape[:2]
+    s_kv = k.shape[1]
+    nq, nk = -(-s_q // TILE), -(-s_kv // TILE)
+    p = _fwd_params(q, k, k, q_ids, q_pos, kv_ids, kv_pos, window_left, None, q, q, False)
+    need = lib().attn_fwd_workspace_bytes(ctypes.byref(p))
+    workspace = _workspace(need, q.device) if workspace is None else workspace
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    cls = torch.empty(b, nq, nk, dtype=torch.uint8, device=q.device)
+    rng = torch.empty(b, nq, 2, dtype=torch.int32, device=q.device)
+    _check(lib().attn_tile_plan(ctypes.byref(p), _ptr(cls), _ptr(rng), _stream(q.device)),
+           "attn_tile_plan")
+    return cls, rng
+
+
+def read_device_status(workspace: torch.Tensor) -> int:
+    """Synchronise the current stream and read the device status word."""
+    return int(lib().attn_read_device_status(_ptr(workspace), _stream(workspace.device)))

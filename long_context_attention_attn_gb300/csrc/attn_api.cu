@@ -1,0 +1,247 @@
+// C ABI of gb300attn: argument validation, tensor-map encoding, launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+
+using namespace gb300;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Shared checks of the forward problem description.
+int check_fwd(const attn_fwd_params* p) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  if (!p->q || !p->k || !p->v || !p->q_segment_ids || !p->q_segment_pos || !p->kv_segment_ids ||
+      !p->kv_segment_pos || !p->out || !p->lse)
+    return ATTN_ERR_INVALID_ARG;
+  if (p->b < 1 || p->s_q < 1 || p->s_kv < 1 || p->h_q < 1 || p->h_kv < 1 || p->d < 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (p->h_q % p->h_kv) return ATTN_ERR_INVALID_ARG;
+  if (p->window_right != 0 || p->window_left < -1) return ATTN_ERR_INVALID_ARG;
+  if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;
+  if (p->s_q > (1ll << 30) || p->s_kv > (1ll << 30) || p->h_q > 65535 || p->b > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(p->q, 16) || !aligned(p->k, 16) || !aligned(p->v, 16) || !aligned(p->out, 16) ||
+      !aligned(p->lse, 4) || !aligned(p->q_segment_ids, 4) || !aligned(p->q_segment_pos, 4) ||
+      !aligned(p->kv_segment_ids, 4) || !aligned(p->kv_segment_pos, 4))
+    return ATTN_ERR_INVALID_ARG;
+  const int64_t g = p->h_q / p->h_kv;
+  const int64_t units = p->b * cdiv(p->s_q, kTile) * p->h_kv * ((g + 1) / 2);
+  if (units > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+PlanLayout fwd_layout(const attn_fwd_params* p) {
+  return plan_layout(p->b, cdiv(p->s_q, kTile), cdiv(p->s_kv, kTile));
+}
+
+int check_workspace(const attn_fwd_params* p, size_t need) {
+  if (!p->workspace || !aligned(p->workspace, 256) || p->workspace_bytes < need)
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+namespace gb300 {
+
+bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  // dims innermost first: (d, head, token, batch); box = 64 d x 1 head x 128 tokens.
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)h, (cuuint64_t)s, (cuuint64_t)b};
+  cuuint64_t strides[3] = {(cuuint64_t)(d * 2), (cuuint64_t)(h * d * 2), (cuuint64_t)(s * h * d * 2)};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gb300
+
+extern "C" {
+
+size_t attn_fwd_workspace_bytes(const attn_fwd_params* p) {
+  if (check_fwd(p) != ATTN_OK) return 0;
+  return fwd_layout(p).end;
+}
+
+int attn_fwd(const attn_fwd_params* p, attn_stream_t stream) {
+  int rc = check_fwd(p);
+  if (rc != ATTN_OK) return rc;
+  const PlanLayout L = fwd_layout(p);
+  rc = check_workspace(p, L.end);
+  if (rc != ATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  FwdLaunch fl;
+  fl.p = p;
+  fl.plan = plan_ptrs(p->workspace, L);
+  fl.nq = cdiv(p->s_q, kTile);
+  fl.nk = cdiv(p->s_kv, kTile);
+  if (!encode_qkv_map(&fl.tm_q, p->q, p->b, p->s_q, p->h_q, p->d) ||
+      !encode_qkv_map(&fl.tm_k, p->k, p->b, p->s_kv, p->h_kv, p->d) ||
+      !encode_qkv_map(&fl.tm_v, p->v, p->b, p->s_kv, p->h_kv, p->d))
+    return ATTN_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(fl.plan.status, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = launch_tile_plan(*p, fl.plan, fl.nq, fl.nk, false, st);
+  if (e == cudaSuccess) e = launch_attn_fwd(fl, st);
+  return cuda_status(e);
+}
+
+int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,
+                   attn_stream_t stream) {
+  int rc = check_fwd(p);
+  if (rc != ATTN_OK) return rc;
+  if (!classes || !ranges || !aligned(ranges, 4)) return ATTN_ERR_INVALID_ARG;
+  const PlanLayout L = fwd_layout(p);
+  rc = check_workspace(p, L.end);
+  if (rc != ATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t nq = cdiv(p->s_q, kTile), nk = cdiv(p->s_kv, kTile);
+  const PlanPtrs pp = plan_ptrs(p->workspace, L);
+  cudaError_t e = launch_tile_plan(*p, pp, nq, nk, false, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(classes, pp.classes, (size_t)(p->b * nq * nk), cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ranges, pp.q_range, (size_t)(p->b * nq) * 8, cudaMemcpyDeviceToDevice, st);
+  return cuda_status(e);
+}
+
+size_t attn_bwd_workspace_bytes(const attn_bwd_params* p) {
+  if (!p || check_fwd(&p->fwd) != ATTN_OK) return 0;
+  const PlanLayout L = fwd_layout(&p->fwd);
+  const size_t d_bytes = align_up((size_t)(p->fwd.b * p->fwd.h_q * p->fwd.s_q) * 4, 256);
+  const size_t dq_bytes = align_up((size_t)(p->fwd.b * p->fwd.s_q * p->fwd.h_q * p->fwd.d) * 4, 256);
+  return L.end + d_bytes + dq_bytes;
+}
+
+int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  int rc = check_fwd(&p->fwd);
+  if (rc != ATTN_OK) return rc;
+  if (p->fwd.out_fp32) return ATTN_ERR_INVALID_ARG;
+  if (!p->dout || !p->dq || !p->dk || !p->dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(p->dout, 16) || !aligned(p->dq, 16) || !aligned(p->dk, 16) || !aligned(p->dv, 16))
+    return ATTN_ERR_INVALID_ARG;
+  const attn_fwd_params* f = &p->fwd;
+  const PlanLayout L = fwd_layout(f);
+  const size_t need = attn_bwd_workspace_bytes(p);
+  rc = check_workspace(f, need);
+  if (rc != ATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  BwdLaunch bl;
+  bl.p = p;
+  bl.plan = plan_ptrs(f->workspace, L);
+  bl.nq = cdiv(f->s_q, kTile);
+  bl.nk = cdiv(f->s_kv, kTile);
+  char* ws = static_cast<char*>(f->workspace);
+  bl.D = reinterpret_cast<float*>(ws + L.end);
+  bl.dq_acc = reinterpret_cast<float*>(
+      ws + L.end + align_up((size_t)(f->b * f->h_q * f->s_q) * 4, 256));
+  if (!encode_qkv_map(&bl.tm_q, f->q, f->b, f->s_q, f->h_q, f->d) ||
+      !encode_qkv_map(&bl.tm_k, f->k, f->b, f->s_kv, f->h_kv, f->d) ||
+      !encode_qkv_map(&bl.tm_v, f->v, f->b, f->s_kv, f->h_kv, f->d) ||
+      !encode_qkv_map(&bl.tm_do, p->dout, f->b, f->s_q, f->h_q, f->d))
+    return ATTN_ERR_CUDA;
+  const size_t n_dq = (size_t)(f->b * f->s_q * f->h_q * f->d);
+  cudaError_t e = cudaMemsetAsync(bl.plan.status, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(bl.dq_acc, 0, n_dq * 4, st);
+  if (e == cudaSuccess) e = launch_tile_plan(*f, bl.plan, bl.nq, bl.nk, true, st);
+  if (e == cudaSuccess)
+    e = launch_bwd_preprocess(f->out, p->dout, bl.D, f->b, f->s_q, f->h_q, f->d, st);
+  if (e == cudaSuccess) e = launch_attn_bwd(bl, st);
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  if (e == cudaSuccess) e = launch_dq_finalize(bl.dq_acc, p->dq, (int64_t)n_dq, st);
+  return cuda_status(e);
+}
+
+int attn_merge_partial(float* out_acc, float* lse_acc, const void* out_blk, const float* lse_blk,
+                       int blk_is_bf16, void* out_final, int64_t b, int64_t s, int64_t h, int64_t d,
+                       attn_stream_t stream) {
+  if (!out_acc || !lse_acc || !out_blk || !lse_blk) return ATTN_ERR_INVALID_ARG;
+  if (b < 1 || s < 1 || h < 1 || d < 8 || d % 8) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(out_acc, 16) || !aligned(out_blk, 16) || !aligned(lse_acc, 4) ||
+      !aligned(lse_blk, 4) || (out_final && !aligned(out_final, 16)))
+    return ATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_merge(out_acc, lse_acc, out_blk, lse_blk, blk_is_bf16 ? 1 : 0,
+                                  out_final, b, s, h, d, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static int reorder_common(const void* in, void* out, int64_t outer, int64_t s, int64_t inner,
+                          int strategy, int cp, int stripe, bool inverse, attn_stream_t stream) {
+  if (!in || !out || in == out) return ATTN_ERR_INVALID_ARG;
+  if (outer < 1 || s < 1 || inner < 1 || cp < 1) return ATTN_ERR_INVALID_ARG;
+  if (strategy == ATTN_REORDER_DUAL_CHUNK) {
+    if (s % (2ll * cp)) return ATTN_ERR_INVALID_ARG;
+  } else if (strategy == ATTN_REORDER_STRIPED) {
+    if (stripe < 1 || s % ((int64_t)cp * stripe)) return ATTN_ERR_INVALID_ARG;
+  } else {
+    return ATTN_ERR_INVALID_ARG;
+  }
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(in), b0 = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t n = (uintptr_t)(outer * s * inner);
+  if (a0 < b0 + n && b0 < a0 + n) return ATTN_ERR_INVALID_ARG;  // overlapping buffers
+  return cuda_status(launch_permute(in, out, outer, s, inner, strategy, cp, stripe, inverse,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int reorder_causal_lb(const void* in, void* out, int64_t outer, int64_t s, int64_t inner_bytes,
+                      int strategy, int cp_size, int stripe_size, attn_stream_t stream) {
+  return reorder_common(in, out, outer, s, inner_bytes, strategy, cp_size, stripe_size, false,
+                        stream);
+}
+
+int inverse_reorder_causal_lb(const void* in, void* out, int64_t outer, int64_t s,
+                              int64_t inner_bytes, int strategy, int cp_size, int stripe_size,
+                              attn_stream_t stream) {
+  return reorder_common(in, out, outer, s, inner_bytes, strategy, cp_size, stripe_size, true,
+                        stream);
+}
+
+int attn_read_device_status(const void* workspace, attn_stream_t stream) {
+  if (!workspace || !aligned(workspace, 256)) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return v;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

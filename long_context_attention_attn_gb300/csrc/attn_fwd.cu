@@ -1,0 +1,495 @@
+// Forward attention over packed THD inputs on sm_103a.
+//
+// Page: "Context parallelism and ring attention", sections "The attention
+// problem" (O = softmax(QK^T/sqrt(H) + M) V), "Online softmax" (running
+// m, z, u with rescaling) and "Causal attention" (skip / full / masked key
+// blocks); TE tutorial sections 1 and 3 (segment ids/pos, GQA, causal window).
+//
+// One CTA computes a 128-row query tile for TWO query heads of one GQA group
+// (both read the same kv head, so every K/V tile loaded into shared memory
+// feeds both).  Roles (384 threads):
+//   warp 0        TMA producer: Q tiles once, then K and V tiles into a ring
+//                 of shared-memory slots, plus the key tile's ids/pos.
+//   warp 1        MMA issuer (one thread): S_h = Q_h K^T and O_h += P_h V on
+//                 tcgen05; also owns the TMEM allocation.
+//   warps 4-7     softmax for head slot 0 (one thread per query row)
+//   warps 8-11    softmax for head slot 1
+// TMEM (512 columns x 128 lanes, lane = query row):
+//   S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D, 256+2D)
+// P (bf16, 2 per column) overwrites the first 64 columns of its S tile and is
+// the A operand of the P.V MMA straight from TMEM.
+//
+// Softmax runs in the base-2 domain: x = s * scale * log2(e).  The running
+// maximum m is only raised (and O rescaled) when a row's new maximum exceeds
+// it by more than 8, so exp2(x - m) <= 256; the final u / z is exact for any
+// reference m.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int NST = 4;  // K/V shared-memory slots (K and V tiles alternate)
+constexpr int NID = 4;  // ids/pos ring entries
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct FwdArgs {
+  const int* q_ids;
+  const int* q_pos;
+  const int* kv_ids;
+  const int* kv_pos;
+  void* out;
+  float* lse;
+  const uint8_t* cls;
+  const int2* qrange;
+  const int* order;
+  int* status;
+  int b, s_q, s_kv, hq, hkv, g, npairs, nq, nk;
+  int window;
+  int out_fp32;
+  float scale_log2;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kChunk = BM * 128;             // one 64-wide bf16 chunk of a 128-row tile
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = BM * D * 2;       // a Q, K or V tile
+  static constexpr int q_off = 0;                     // 2 Q tiles
+  static constexpr int kv_off = q_off + 2 * kTileBytes;
+  static constexpr int id_off = kv_off + NST * kTileBytes;  // NID x (128 ids + 128 pos)
+  static constexpr int bar_off = id_off + NID * 2 * BN * 4;
+  static constexpr int bytes = bar_off + 256;
+  // + slack for 1024-byte alignment; at least 150 KB so that one CTA (which
+  // holds all 512 TMEM columns) is resident per SM.
+  static constexpr int alloc = (bytes + 1024) > 150 * 1024 ? (bytes + 1024) : 150 * 1024;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[NST];
+  uint64_t kv_empty[NST];
+  uint64_t id_full[NID];
+  uint64_t id_empty[NID];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block too large");
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::bar_off);
+  int* s_ids = reinterpret_cast<int*>(smem + L::id_off);  // [NID][2][BN]
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  // A CTA of this launch already timed out: the outputs are undefined, stop.
+  if (a.status && *reinterpret_cast<volatile int*>(a.status) != kStatusOk) return;
+
+  // ---- work unit: (b, q tile) heavy first, then kv head, then head pair
+  const int per_tile = a.hkv * a.npairs;
+  const int rank = blockIdx.x / per_tile;
+  const int rem = blockIdx.x % per_tile;
+  const int kvh = rem / a.npairs;
+  const int pair = rem % a.npairs;
+  const int e = a.order[rank];
+  const int bi = e / a.nq;
+  const int qt = e % a.nq;
+  const int h0 = kvh * a.g + 2 * pair;
+  const int nslots = (2 * pair + 1 < a.g) ? 2 : 1;
+  const int2 rng = a.qrange[e];
+  const uint8_t* cls_row = a.cls + (size_t)e * a.nk;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+    }
+    for (int i = 0; i < NID; ++i) {
+      mbar_init(&bars->id_full[i], 1);
+      mbar_init(&bars->id_empty[i], 128 * nslots);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->o_done[i], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtx ctx{&bars->abort_flag, a.status};
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&bars->q_full, nslots * L::kTileBytes);
+      for (int sl = 0; sl < nslots; ++sl)
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_4d(smem_u32(smem + L::q_off + sl * L::kTileBytes + c * L::kChunk), &tm_q,
+                      c * 64, h0 + sl, qt * BM, bi, &bars->q_full);
+    }
+    int n = 0;
+    int last_use[NST];
+    for (int i = 0; i < NST; ++i) last_use[i] = -1;
+    bool ok = true;
+    for (int j = rng.x; j <= rng.y && ok; ++j) {
+      const uint8_t kind = cls_row[j];
+      if (kind == kSkip) continue;
+      // K tile
+      {
+        const int ld = 2 * n, slot = ld % NST, use = ld / NST;
+        if (lane == 0) {
+          ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars->kv_full[slot], L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kTileBytes + c * L::kChunk), &tm_k,
+                          c * 64, kvh, j * BN, bi, &bars->kv_full[slot]);
+            last_use[slot] = use;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      // ids / pos of the key tile (for the element mask)
+      {
+        const int en = n % NID, use = n / NID;
+        if (lane == 0) ok = mbar_wait(&bars->id_empty[en], (use & 1) ^ 1, ctx);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        int* dst = s_ids + en * 2 * BN;
+        const int64_t base = (int64_t)bi * a.s_kv;
+        for (int t = lane; t < BN; t += 32) {
+          const int tok = j * BN + t;
+          const bool in = tok < a.s_kv;
+          dst[t] = in ? a.kv_ids[base + tok] : 0;
+          dst[BN + t] = in ? a.kv_pos[base + tok] : 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->id_full[en]);
+      }
+      // V tile
+      {
+        const int ld = 2 * n + 1, slot = ld % NST, use = ld / NST;
+        if (lane == 0) {
+          ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars->kv_full[slot], L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kTileBytes + c * L::kChunk), &tm_v,
+                          c * 64, kvh, j * BN, bi, &bars->kv_full[slot]);
+            last_use[slot] = use;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      ++n;
+    }
+    // Drain: every TMA copy this warp issued has landed before the CTA exits
+    // (already true on the normal path; bounded after an abort).
+    if (lane == 0) {
+      mbar_wait_drain(&bars->q_full, 0, a.status);
+      for (int i = 0; i < NST; ++i)
+        if (last_use[i] >= 0) mbar_wait_drain(&bars->kv_full[i], last_use[i] & 1, a.status);
+    }
+  } else if (warp == 1) {
+    // ======================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
+      bool ok = mbar_wait(&bars->q_full, 0, ctx);
+      const uint32_t q_base = smem_u32(smem + L::q_off);
+      const uint32_t kv_base = smem_u32(smem + L::kv_off);
+      int n = 0;
+      for (int j = rng.x; j <= rng.y && ok; ++j) {
+        if (cls_row[j] == kSkip) continue;
+        // S_h = Q_h K^T
+        const int ldk = 2 * n, slot_k = ldk % NST;
+        ok = mbar_wait(&bars->kv_full[slot_k], (ldk / NST) & 1, ctx);
+        if (!ok) break;
+        for (int sl = 0; sl < nslots && ok; ++sl) {
+          if (n > 0) ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qa = q_base + sl * L::kTileBytes;
+          const uint32_t kb = kv_base + slot_k * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * L::kChunk + (kk % 4) * 32;
+            mma_ss(tmem + sl * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                   idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[sl]);
+        }
+        if (!ok) break;
+        mma_commit(&bars->kv_empty[slot_k]);
+        // O_h += P_h V
+        const int ldv = 2 * n + 1, slot_v = ldv % NST;
+        ok = mbar_wait(&bars->kv_full[slot_v], (ldv / NST) & 1, ctx);
+        if (!ok) break;
+        for (int sl = 0; sl < nslots && ok; ++sl) {
+          ok = mbar_wait(&bars->p_full[sl], n & 1, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vb = kv_base + slot_v * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            mma_ts(tmem + 2 * BN + sl * D, tmem + sl * BN + kk * 8,
+                   sdesc_sw128(vb + kk * 16 * 128, L::kChunk, 1024), idesc_o,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->o_done[sl]);
+        }
+        if (!ok) break;
+        mma_commit(&bars->kv_empty[slot_v]);
+        ++n;
+      }
+      // Drain: all MMAs issued by this thread complete before TMEM is freed.
+      mma_commit(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0, a.status);
+    }
+  } else if (warp >= 4) {
+    // ======================================================== softmax
+    const int sl = (warp - 4) / 4;
+    const int wq = warp % 4;  // TMEM lane quarter this warp may access
+    const int row = wq * 32 + lane;
+    if (sl < nslots) {
+      const int h = h0 + sl;
+      const int grow = qt * BM + row;
+      const bool row_in = grow < a.s_q;
+      const int iq = row_in ? a.q_ids[(int64_t)bi * a.s_q + grow] : 0;
+      const int pq = row_in ? a.q_pos[(int64_t)bi * a.s_q + grow] : 0;
+      const uint32_t t_s = tmem + ((uint32_t)(wq * 32) << 16) + sl * BN;
+      const uint32_t t_o = tmem + ((uint32_t)(wq * 32) << 16) + 2 * BN + sl * D;
+      const float sl2 = a.scale_log2;
+      float m = -INFINITY;  // running max (base-2 units)
+      float l = 0.f;        // running denominator relative to m
+      int n = 0;
+      bool ok = true;
+      for (int j = rng.x; j <= rng.y; ++j) {
+        const uint8_t kind = cls_row[j];
+        if (kind == kSkip) continue;
+        const int en = n % NID;
+        ok = mbar_wait(&bars->id_full[en], (n / NID) & 1, ctx);
+        ok = mbar_wait(&bars->s_full[sl], n & 1, ctx) && ok;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[BN];
+        tmem_ld32(t_s + 0, &sr[0]);
+        tmem_ld32(t_s + 32, &sr[32]);
+        tmem_ld32(t_s + 64, &sr[64]);
+        tmem_ld32(t_s + 96, &sr[96]);
+        tmem_wait_ld();
+        if (kind == kPartial) {
+          const int4* ids4 = reinterpret_cast<const int4*>(s_ids + en * 2 * BN);
+          const int4* pos4 = reinterpret_cast<const int4*>(s_ids + en * 2 * BN + BN);
+#pragma unroll
+          for (int c = 0; c < BN / 4; ++c) {
+            const int4 ik = ids4[c];
+            const int4 pk4 = pos4[c];
+            const int ika[4] = {ik.x, ik.y, ik.z, ik.w};
+            const int pka[4] = {pk4.x, pk4.y, pk4.z, pk4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              bool vis = (ika[u] == iq) && (iq != 0) && (pka[u] <= pq);
+              if (a.window >= 0) vis = vis && (pq - pka[u] <= a.window);
+              if (!vis) sr[4 * c + u] = __float_as_uint(-INFINITY);
+            }
+          }
+        }
+        mbar_arrive(&bars->id_empty[en]);
+        // row max of the raw scores (scale > 0 keeps the order)
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int c = 4; c < BN; c += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+        }
+        const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float m_new = fmaxf(m, mt);
+        float alpha = 1.f;
+        bool rescale = false;
+        float m_use = m;
+        if (m == -INFINITY) {
+          m_use = m_new;  // nothing accumulated yet: O row and l are 0
+        } else if (m_new > m + kRescaleThreshold) {
+          m_use = m_new;
+          alpha = ex2(m - m_new);
+          rescale = true;
+        }
+        const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        // packed bf16 P overwrites the front of the score registers
+#pragma unroll
+        for (int c = 0; c < BN; c += 4) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, -msub));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -msub));
+          const float p2 = ex2(fmaf(__uint_as_float(sr[c + 2]), sl2, -msub));
+          const float p3 = ex2(fmaf(__uint_as_float(sr[c + 3]), sl2, -msub));
+          s0 += p0;
+          s1 += p1;
+          s2 += p2;
+          s3 += p3;
+          sr[c / 2] = pack_bf16(p0, p1);
+          sr[c / 2 + 1] = pack_bf16(p2, p3);
+        }
+        l = l * alpha + ((s0 + s1) + (s2 + s3));
+        m = m_use;
+        tmem_st32(t_s + 0, &sr[0]);
+        tmem_st32(t_s + 32, &sr[32]);
+        if (__any_sync(0xffffffffu, rescale) && n > 0) {
+          // O += P V of the previous tile must be complete before O is rescaled.
+          ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+            tmem_st32(t_o + c, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[sl]);
+        ++n;
+      }
+      // ---- epilogue: O = u / z, LSE = ln2 * (m + log2 z)
+      if (ok && n > 0) {
+        ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+      }
+      if (ok) {
+        const bool has = l > 0.f;
+        const float inv = has ? 1.f / l : 0.f;
+        const int64_t orow = ((int64_t)bi * a.s_q + grow) * a.hq + h;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          if (n > 0) {
+            tmem_ld32(t_o + c, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = 0u;
+          }
+          if (!row_in) continue;
+          if (a.out_fp32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * D + c);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              dst[u] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                                   __uint_as_float(o[4 * u + 2]) * inv,
+                                   __uint_as_float(o[4 * u + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + c);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+              w.y = pack_bf16(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+              w.z = pack_bf16(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+              w.w = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+              dst[u] = w;
+            }
+          }
+        }
+        if (row_in)
+          a.lse[((int64_t)bi * a.hq + h) * a.s_q + grow] = has ? (m + log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  // ---- teardown (the producer and MMA threads drained their async work above)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
+  const attn_fwd_params& p = *Lc.p;
+  FwdArgs a;
+  a.q_ids = p.q_segment_ids;
+  a.q_pos = p.q_segment_pos;
+  a.kv_ids = p.kv_segment_ids;
+  a.kv_pos = p.kv_segment_pos;
+  a.out = p.out;
+  a.lse = p.lse;
+  a.cls = Lc.plan.classes;
+  a.qrange = Lc.plan.q_range;
+  a.order = Lc.plan.q_order;
+  a.status = Lc.plan.status;
+  a.b = (int)p.b;
+  a.s_q = (int)p.s_q;
+  a.s_kv = (int)p.s_kv;
+  a.hq = (int)p.h_q;
+  a.hkv = (int)p.h_kv;
+  a.g = (int)(p.h_q / p.h_kv);
+  a.npairs = (a.g + 1) / 2;
+  a.nq = (int)Lc.nq;
+  a.nk = (int)Lc.nk;
+  a.window = p.window_left;
+  a.out_fp32 = p.out_fp32 ? 1 : 0;
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  const int64_t units = p.b * Lc.nq * p.h_kv * a.npairs;
+  if (units == 0) return cudaSuccess;
+  if (p.d == 128) {
+    const int smem = Layout<128>::alloc;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_fwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
+  } else {
+    const int smem = Layout<64>::alloc;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_fwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gb300

@@ -1,0 +1,124 @@
+// Shared host-side declarations of the gb300attn library (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gb300attn.h"
+
+namespace gb300 {
+
+constexpr int kTile = 128;  // query / key tile edge used by the plan and the kernels
+
+// Per-128-token tile summary of a segment descriptor (32 bytes).
+struct TileSummary {
+  int any_valid;  // some token has id != 0
+  int has_pad;    // some slot is padding or past the end of the sequence
+  int id_min;     // min / max nonzero id (valid only if any_valid)
+  int id_max;
+  int pos_min;    // min / max position over valid tokens
+  int pos_max;
+  int reserved0;
+  int reserved1;
+};
+
+enum : uint8_t { kSkip = 0, kPartial = 1, kFull = 2 };
+
+// Byte offsets of the tile plan inside a workspace.
+struct PlanLayout {
+  size_t status;      // int: device status word
+  size_t q_sum;       // TileSummary [b, nq]
+  size_t kv_sum;      // TileSummary [b, nk]
+  size_t q_range;     // int2 [b, nq]  first/last non-SKIP kv tile
+  size_t kv_range;    // int2 [b, nk]  first/last non-SKIP q tile
+  size_t q_weight;    // int  [b, nq]  number of non-SKIP kv tiles
+  size_t kv_weight;   // int  [b, nk]  number of non-SKIP q tiles
+  size_t q_order;     // int  [b, nq]  (b, q tile) heavy first
+  size_t kv_order;    // int  [b, nk]  (b, kv tile) heavy first
+  size_t classes;     // uint8 [b, nq, nk]
+  size_t end;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline PlanLayout plan_layout(int64_t b, int64_t nq, int64_t nk, size_t base = 0) {
+  PlanLayout L;
+  size_t o = base;
+  L.status = o;    o = align_up(o + 256, 256);
+  L.q_sum = o;     o = align_up(o + (size_t)(b * nq) * sizeof(TileSummary), 256);
+  L.kv_sum = o;    o = align_up(o + (size_t)(b * nk) * sizeof(TileSummary), 256);
+  L.q_range = o;   o = align_up(o + (size_t)(b * nq) * 8, 256);
+  L.kv_range = o;  o = align_up(o + (size_t)(b * nk) * 8, 256);
+  L.q_weight = o;  o = align_up(o + (size_t)(b * nq) * 4, 256);
+  L.kv_weight = o; o = align_up(o + (size_t)(b * nk) * 4, 256);
+  L.q_order = o;   o = align_up(o + (size_t)(b * nq) * 4, 256);
+  L.kv_order = o;  o = align_up(o + (size_t)(b * nk) * 4, 256);
+  L.classes = o;   o = align_up(o + (size_t)(b * nq * nk), 256);
+  L.end = o;
+  return L;
+}
+
+struct PlanPtrs {
+  int* status;
+  TileSummary* q_sum;
+  TileSummary* kv_sum;
+  int2* q_range;
+  int2* kv_range;
+  int* q_weight;
+  int* kv_weight;
+  int* q_order;
+  int* kv_order;
+  uint8_t* classes;
+};
+
+inline PlanPtrs plan_ptrs(void* ws, const PlanLayout& L) {
+  char* c = static_cast<char*>(ws);
+  return PlanPtrs{reinterpret_cast<int*>(c + L.status),
+                  reinterpret_cast<TileSummary*>(c + L.q_sum),
+                  reinterpret_cast<TileSummary*>(c + L.kv_sum),
+                  reinterpret_cast<int2*>(c + L.q_range),
+                  reinterpret_cast<int2*>(c + L.kv_range),
+                  reinterpret_cast<int*>(c + L.q_weight),
+                  reinterpret_cast<int*>(c + L.kv_weight),
+                  reinterpret_cast<int*>(c + L.q_order),
+                  reinterpret_cast<int*>(c + L.kv_order),
+                  reinterpret_cast<uint8_t*>(c + L.classes)};
+}
+
+// ---- kernels_misc.cu
+cudaError_t launch_tile_plan(const attn_fwd_params& p, const PlanPtrs& pp, int64_t nq, int64_t nk,
+                             bool need_kv_side, cudaStream_t st);
+cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t s, int64_t inner_bytes,
+                           int strategy, int cp, int stripe, bool inverse, cudaStream_t st);
+cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, const float* lse_blk,
+                         int blk_bf16, void* out_final, int64_t b, int64_t s, int64_t h, int64_t d,
+                         cudaStream_t st);
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, int64_t b,
+                                  int64_t s, int64_t h, int64_t d, cudaStream_t st);
+cudaError_t launch_dq_finalize(const float* acc, void* dq, int64_t n, cudaStream_t st);
+
+// ---- attn_fwd.cu
+struct FwdLaunch {
+  const attn_fwd_params* p;
+  PlanPtrs plan;
+  int64_t nq, nk;
+  CUtensorMap tm_q, tm_k, tm_v;
+};
+cudaError_t launch_attn_fwd(const FwdLaunch& L, cudaStream_t st);
+
+// ---- attn_bwd.cu
+struct BwdLaunch {
+  const attn_bwd_params* p;
+  PlanPtrs plan;
+  int64_t nq, nk;
+  float* D;       // [b, hq, s_q]
+  float* dq_acc;  // [b, s_q, hq, d]
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+};
+cudaError_t launch_attn_bwd(const BwdLaunch& L, cudaStream_t st);
+
+// ---- attn_api.cu
+bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d);
+
+}  // namespace gb300

@@ -1,0 +1,435 @@
+// HBM-bound and integer kernels of the hot path: tile plan, causal
+// load-balancing permutation, online-softmax merge, backward pre/post passes.
+#include <cuda_bf16.h>
+
+#include <climits>
+
+#include "internal.h"
+
+namespace gb300 {
+
+// ============================================================== tile plan
+// Page: "Context parallelism and ring attention", section "Causal attention":
+// skip key blocks entirely in the future, process fully valid blocks without
+// a mask, mask the overlapping ones.  Generalised to segments, padding and a
+// left window through per-tile summaries of the segment descriptors.
+
+__global__ void tile_summary_kernel(const int* __restrict__ ids, const int* __restrict__ pos,
+                                    int64_t b, int64_t s, int64_t ntile,
+                                    TileSummary* __restrict__ out) {
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= b * ntile) return;
+  const int64_t bi = w / ntile, t = w % ntile;
+  int any_valid = 0, has_pad = 0;
+  int id_min = INT_MAX, id_max = INT_MIN, pmin = INT_MAX, pmax = INT_MIN;
+#pragma unroll
+  for (int k = 0; k < kTile / 32; ++k) {
+    const int64_t tok = t * kTile + k * 32 + lane;
+    if (tok < s) {
+      const int id = ids[bi * s + tok];
+      if (id != 0) {
+        const int ps = pos[bi * s + tok];
+        any_valid = 1;
+        id_min = min(id_min, id);
+        id_max = max(id_max, id);
+        pmin = min(pmin, ps);
+        pmax = max(pmax, ps);
+      } else {
+        has_pad = 1;
+      }
+    } else {
+      has_pad = 1;
+    }
+  }
+  any_valid = __reduce_or_sync(0xffffffffu, any_valid);
+  has_pad = __reduce_or_sync(0xffffffffu, has_pad);
+  id_min = __reduce_min_sync(0xffffffffu, id_min);
+  id_max = __reduce_max_sync(0xffffffffu, id_max);
+  pmin = __reduce_min_sync(0xffffffffu, pmin);
+  pmax = __reduce_max_sync(0xffffffffu, pmax);
+  if (lane == 0) {
+    TileSummary r;
+    r.any_valid = any_valid;
+    r.has_pad = has_pad;
+    r.id_min = any_valid ? id_min : 0;
+    r.id_max = any_valid ? id_max : 0;
+    r.pos_min = any_valid ? pmin : 0;
+    r.pos_max = any_valid ? pmax : 0;
+    r.reserved0 = r.reserved1 = 0;
+    out[w] = r;
+  }
+}
+
+__device__ __forceinline__ uint8_t classify(const TileSummary& q, const TileSummary& k, int window) {
+  if (!q.any_valid || !k.any_valid) return kSkip;
+  if (q.id_max < k.id_min || k.id_max < q.id_min) return kSkip;
+  if (k.pos_min > q.pos_max) return kSkip;  // every key after every query
+  if (window >= 0 && (int64_t)k.pos_max < (int64_t)q.pos_min - window) return kSkip;
+  const bool one_id = !q.has_pad && !k.has_pad && q.id_min == q.id_max && k.id_min == k.id_max &&
+                      q.id_min == k.id_min;
+  if (one_id && k.pos_max <= q.pos_min &&
+      (window < 0 || (int64_t)q.pos_max - k.pos_min <= window))
+    return kFull;
+  return kPartial;
+}
+
+// One CTA per (q tile, b): the class of every kv tile and the q-side range.
+__global__ void tile_class_kernel(const TileSummary* __restrict__ qs,
+                                  const TileSummary* __restrict__ ks, int64_t nq, int64_t nk,
+                                  int window, uint8_t* __restrict__ cls, int2* __restrict__ qrange,
+                                  int* __restrict__ qweight) {
+  const int64_t a = blockIdx.x, bi = blockIdx.y;
+  __shared__ int s_first, s_last, s_count;
+  if (threadIdx.x == 0) {
+    s_first = INT_MAX;
+    s_last = -1;
+    s_count = 0;
+  }
+  __syncthreads();
+  const TileSummary q = qs[bi * nq + a];
+  int first = INT_MAX, last = -1, count = 0;
+  for (int64_t c = threadIdx.x; c < nk; c += blockDim.x) {
+    const uint8_t k = classify(q, ks[bi * nk + c], window);
+    cls[(bi * nq + a) * nk + c] = k;
+    if (k != kSkip) {
+      first = min(first, (int)c);
+      last = max(last, (int)c);
+      ++count;
+    }
+  }
+  atomicMin(&s_first, first);
+  atomicMax(&s_last, last);
+  atomicAdd(&s_count, count);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    qrange[bi * nq + a] = s_last < 0 ? make_int2(0, -1) : make_int2(s_first, s_last);
+    qweight[bi * nq + a] = s_count;
+  }
+}
+
+// One CTA per (kv tile, b): the range of q tiles that see it (backward side).
+__global__ void kv_range_kernel(const uint8_t* __restrict__ cls, int64_t nq, int64_t nk,
+                                int2* __restrict__ krange, int* __restrict__ kweight) {
+  const int64_t c = blockIdx.x, bi = blockIdx.y;
+  __shared__ int s_first, s_last, s_count;
+  if (threadIdx.x == 0) {
+    s_first = INT_MAX;
+    s_last = -1;
+    s_count = 0;
+  }
+  __syncthreads();
+  int first = INT_MAX, last = -1, count = 0;
+  for (int64_t a = threadIdx.x; a < nq; a += blockDim.x) {
+    if (cls[(bi * nq + a) * nk + c] != kSkip) {
+      first = min(first, (int)a);
+      last = max(last, (int)a);
+      ++count;
+    }
+  }
+  atomicMin(&s_first, first);
+  atomicMax(&s_last, last);
+  atomicAdd(&s_count, count);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    krange[bi * nk + c] = s_last < 0 ? make_int2(0, -1) : make_int2(s_first, s_last);
+    kweight[bi * nk + c] = s_count;
+  }
+}
+
+// Counting sort of n work rows by weight, heaviest first (single CTA).  Rows
+// of equal weight keep an arbitrary order; weights above kBuckets-1 share the
+// top bucket.
+constexpr int kBuckets = 2048;
+__global__ void heavy_first_kernel(const int* __restrict__ weight, int n, int* __restrict__ order) {
+  __shared__ int hist[kBuckets];
+  __shared__ int start[kBuckets];
+  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    atomicAdd(&hist[min(weight[i], kBuckets - 1)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int w = kBuckets - 1; w >= 0; --w) {
+      start[w] = acc;
+      acc += hist[w];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int slot = atomicAdd(&start[min(weight[i], kBuckets - 1)], 1);
+    order[slot] = i;
+  }
+}
+
+cudaError_t launch_tile_plan(const attn_fwd_params& p, const PlanPtrs& pp, int64_t nq, int64_t nk,
+                             bool need_kv_side, cudaStream_t st) {
+  const int wpb = 8;
+  tile_summary_kernel<<<(unsigned)((p.b * nq + wpb - 1) / wpb), wpb * 32, 0, st>>>(
+      p.q_segment_ids, p.q_segment_pos, p.b, p.s_q, nq, pp.q_sum);
+  tile_summary_kernel<<<(unsigned)((p.b * nk + wpb - 1) / wpb), wpb * 32, 0, st>>>(
+      p.kv_segment_ids, p.kv_segment_pos, p.b, p.s_kv, nk, pp.kv_sum);
+  tile_class_kernel<<<dim3((unsigned)nq, (unsigned)p.b), 256, 0, st>>>(
+      pp.q_sum, pp.kv_sum, nq, nk, p.window_left, pp.classes, pp.q_range, pp.q_weight);
+  heavy_first_kernel<<<1, 1024, 0, st>>>(pp.q_weight, (int)(p.b * nq), pp.q_order);
+  if (need_kv_side) {
+    kv_range_kernel<<<dim3((unsigned)nk, (unsigned)p.b), 256, 0, st>>>(pp.classes, nq, nk,
+                                                                      pp.kv_range, pp.kv_weight);
+    heavy_first_kernel<<<1, 1024, 0, st>>>(pp.kv_weight, (int)(p.b * nk), pp.kv_order);
+  }
+  return cudaGetLastError();
+}
+
+// ============================================================== permutation
+// Page: "Context parallelism and ring attention", section "Load balance"
+// (dual chunk: shard r holds chunks r and 2R-1-r of 2R); TE tutorial section 4
+// (striped: stripe t goes to shard t mod R).  src(i) is the input row of
+// output row i.
+__device__ __forceinline__ int64_t perm_src(int64_t i, int64_t s, int strategy, int R, int stripe) {
+  if (strategy == ATTN_REORDER_DUAL_CHUNK) {
+    const int64_t c = s / (2 * R);
+    const int64_t r = i / (2 * c), w = i - r * 2 * c;
+    return w < c ? r * c + w : (2 * R - 1 - r) * c + (w - c);
+  }
+  const int64_t n = s / R;
+  const int64_t r = i / n, t = i - r * n;
+  return ((t / stripe) * R + r) * stripe + (t % stripe);
+}
+
+// One warp per row; 16-byte vectors along the row.
+__global__ void permute_vec16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                     int64_t rows, int64_t s, int64_t vpr, int strategy, int R,
+                                     int stripe, int inverse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; row < rows;
+       row += nwarps) {
+    const int64_t o = row / s, i = row - o * s;
+    const int64_t j = perm_src(i, s, strategy, R, stripe);
+    const int64_t src = o * s + (inverse ? i : j);
+    const int64_t dst = o * s + (inverse ? j : i);
+    const uint4* a = in + src * vpr;
+    uint4* bptr = out + dst * vpr;
+    int64_t w = lane;
+    for (; w + 96 < vpr; w += 128) {
+      const uint4 x0 = a[w], x1 = a[w + 32], x2 = a[w + 64], x3 = a[w + 96];
+      bptr[w] = x0;
+      bptr[w + 32] = x1;
+      bptr[w + 64] = x2;
+      bptr[w + 96] = x3;
+    }
+    for (; w < vpr; w += 32) bptr[w] = a[w];
+  }
+}
+
+// One thread per element of `esize` bytes (4 or 1).
+template <typename T>
+__global__ void permute_elem_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t rows,
+                                    int64_t s, int64_t epr, int strategy, int R, int stripe,
+                                    int inverse) {
+  const int64_t total = rows * epr;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = e / epr, k = e - row * epr;
+    const int64_t o = row / s, i = row - o * s;
+    const int64_t j = perm_src(i, s, strategy, R, stripe);
+    const int64_t src = o * s + (inverse ? i : j);
+    const int64_t dst = o * s + (inverse ? j : i);
+    out[dst * epr + k] = in[src * epr + k];
+  }
+}
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t s, int64_t inner_bytes,
+                           int strategy, int cp, int stripe, bool inverse, cudaStream_t st) {
+  const int64_t rows = outer * s;
+  const int sms = sm_count();
+  const bool aligned16 = (reinterpret_cast<uintptr_t>(in) % 16 == 0) &&
+                         (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+  if (inner_bytes % 16 == 0 && aligned16) {
+    const int64_t need = (rows + 7) / 8;
+    const unsigned grid = (unsigned)std::min<int64_t>(need, (int64_t)sms * 8);
+    permute_vec16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(in),
+                                               static_cast<uint4*>(out), rows, s, inner_bytes / 16,
+                                               strategy, cp, stripe, inverse ? 1 : 0);
+  } else if (inner_bytes % 4 == 0 && reinterpret_cast<uintptr_t>(in) % 4 == 0 &&
+             reinterpret_cast<uintptr_t>(out) % 4 == 0) {
+    const int64_t total = rows * (inner_bytes / 4);
+    const unsigned grid = (unsigned)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 16);
+    permute_elem_kernel<uint32_t><<<grid, 256, 0, st>>>(
+        static_cast<const uint32_t*>(in), static_cast<uint32_t*>(out), rows, s, inner_bytes / 4,
+        strategy, cp, stripe, inverse ? 1 : 0);
+  } else {
+    const int64_t total = rows * inner_bytes;
+    const unsigned grid = (unsigned)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 16);
+    permute_elem_kernel<uint8_t><<<grid, 256, 0, st>>>(
+        static_cast<const uint8_t*>(in), static_cast<uint8_t*>(out), rows, s, inner_bytes,
+        strategy, cp, stripe, inverse ? 1 : 0);
+  }
+  return cudaGetLastError();
+}
+
+// ============================================================== merge
+// Page: "Context parallelism and ring attention", section "Online softmax".
+// A finished partial (O, LSE) is the running triple (m = LSE, z = 1, u = O);
+// the page's update then gives, with M = max(l_a, l_b):
+//   z' = e^(l_a - M) + e^(l_b - M),  LSE' = M + ln z',
+//   O' = (e^(l_a - M) O_a + e^(l_b - M) O_b) / z'.
+// One warp per (token, head) row; lanes stride over d in 4-float vectors.
+template <bool BLK_BF16, bool FINAL>
+__global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ lse_acc,
+                             const void* __restrict__ out_blk, const float* __restrict__ lse_blk,
+                             __nv_bfloat16* __restrict__ out_final, int64_t b, int64_t s,
+                             int64_t h, int64_t d) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = b * s * h;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t v4 = d / 4;
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows;
+       r += nwarps) {
+    const int64_t hh = r % h;
+    const int64_t ti = (r / h) % s;
+    const int64_t bi = r / (h * s);
+    const int64_t li = (bi * h + hh) * s + ti;
+    const float la = lse_acc[li], lb = lse_blk[li];
+    const float M = fmaxf(la, lb);
+    float ca = 0.f, cb = 0.f, lnew = -INFINITY;
+    if (M != -INFINITY) {
+      const float ea = (la == -INFINITY) ? 0.f : expf(la - M);
+      const float eb = (lb == -INFINITY) ? 0.f : expf(lb - M);
+      const float z = ea + eb;
+      lnew = M + logf(z);
+      ca = ea / z;
+      cb = eb / z;
+    }
+    float4* acc = reinterpret_cast<float4*>(out_acc + r * d);
+    for (int64_t w = lane; w < v4; w += 32) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ca != 0.f) a = acc[w];
+      float4 x;
+      if (BLK_BF16) {
+        const uint2 raw = reinterpret_cast<const uint2*>(
+            static_cast<const __nv_bfloat16*>(out_blk) + r * d)[w];
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        const float2 f0 = __bfloat1622float2(p0), f1 = __bfloat1622float2(p1);
+        x = make_float4(f0.x, f0.y, f1.x, f1.y);
+      } else {
+        x = reinterpret_cast<const float4*>(static_cast<const float*>(out_blk) + r * d)[w];
+      }
+      if (cb == 0.f) x = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 o;
+      o.x = ca * a.x + cb * x.x;
+      o.y = ca * a.y + cb * x.y;
+      o.z = ca * a.z + cb * x.z;
+      o.w = ca * a.w + cb * x.w;
+      if (FINAL) {
+        const __nv_bfloat162 q0 = __floats2bfloat162_rn(o.x, o.y);
+        const __nv_bfloat162 q1 = __floats2bfloat162_rn(o.z, o.w);
+        uint2 raw;
+        raw.x = *reinterpret_cast<const uint32_t*>(&q0);
+        raw.y = *reinterpret_cast<const uint32_t*>(&q1);
+        reinterpret_cast<uint2*>(out_final + r * d)[w] = raw;
+      } else {
+        acc[w] = o;
+      }
+    }
+    if (lane == 0) lse_acc[li] = lnew;
+  }
+}
+
+cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, const float* lse_blk,
+                         int blk_bf16, void* out_final, int64_t b, int64_t s, int64_t h, int64_t d,
+                         cudaStream_t st) {
+  const int64_t rows = b * s * h;
+  const unsigned grid = (unsigned)std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
+  __nv_bfloat16* fin = static_cast<__nv_bfloat16*>(out_final);
+  if (blk_bf16) {
+    if (fin)
+      merge_kernel<true, true><<<grid, 256, 0, st>>>(out_acc, lse_acc, out_blk, lse_blk, fin, b, s, h, d);
+    else
+      merge_kernel<true, false><<<grid, 256, 0, st>>>(out_acc, lse_acc, out_blk, lse_blk, fin, b, s, h, d);
+  } else {
+    if (fin)
+      merge_kernel<false, true><<<grid, 256, 0, st>>>(out_acc, lse_acc, out_blk, lse_blk, fin, b, s, h, d);
+    else
+      merge_kernel<false, false><<<grid, 256, 0, st>>>(out_acc, lse_acc, out_blk, lse_blk, fin, b, s, h, d);
+  }
+  return cudaGetLastError();
+}
+
+// ============================================================== backward helpers
+// D_i = sum_d dO_i * O_i per (b, head, row): the row term of dS = P * (dP - D).
+__global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
+                                      const __nv_bfloat16* __restrict__ dout, float* __restrict__ D,
+                                      int64_t b, int64_t s, int64_t h, int64_t d) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = b * s * h;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t v4 = d / 4;
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows;
+       r += nwarps) {
+    float acc = 0.f;
+    const uint2* po = reinterpret_cast<const uint2*>(out + r * d);
+    const uint2* pd = reinterpret_cast<const uint2*>(dout + r * d);
+    for (int64_t w = lane; w < v4; w += 32) {
+      const uint2 a = po[w], c = pd[w];
+      const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+      const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+      const float2 c0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c.x));
+      const float2 c1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c.y));
+      acc += a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      const int64_t hh = r % h, ti = (r / h) % s, bi = r / (h * s);
+      D[(bi * h + hh) * s + ti] = acc;
+    }
+  }
+}
+
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, int64_t b,
+                                  int64_t s, int64_t h, int64_t d, cudaStream_t st) {
+  const int64_t rows = b * s * h;
+  const unsigned grid = (unsigned)std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
+  bwd_preprocess_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out),
+                                              static_cast<const __nv_bfloat16*>(dout), D, b, s, h,
+                                              d);
+  return cudaGetLastError();
+}
+
+__global__ void dq_finalize_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
+                                   int64_t n4) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = acc[i];
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 c = __floats2bfloat162_rn(v.z, v.w);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&a);
+    o.y = *reinterpret_cast<const uint32_t*>(&c);
+    dq[i] = o;
+  }
+}
+
+cudaError_t launch_dq_finalize(const float* acc, void* dq, int64_t n, cudaStream_t st) {
+  const int64_t n4 = n / 4;
+  const unsigned grid = (unsigned)std::min<int64_t>((n4 + 255) / 256, (int64_t)sm_count() * 16);
+  dq_finalize_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(acc),
+                                           static_cast<uint2*>(dq), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace gb300

@@ -1,0 +1,111 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects invalid arguments on the host before touching
+the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ga():
+    import __graft_entry__
+    __graft_entry__.build()
+    import long_context_attention_attn_gb300 as pkg
+    return pkg
+
+
+def _header_symbols():
+    with open(os.path.join(ROOT, "include", "gb300attn.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^GB300ATTN_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol(ga):
+    syms = _header_symbols()
+    assert len(syms) >= 10
+    lib = ga.lib()
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(syms) == set(ga.EXPORTS)
+
+
+def test_status_strings(ga):
+    assert ga.status_string(0) == "ok"
+    assert "timed out" in ga.status_string(4)
+
+
+def _params(ga, **kw):
+    p = ga.FwdParams()
+    fake = 1 << 20  # aligned non-null fake device address; never dereferenced
+    for f in ("q", "k", "v", "q_segment_ids", "q_segment_pos", "kv_segment_ids",
+              "kv_segment_pos", "out", "lse"):
+        setattr(p, f, fake)
+    p.workspace = fake
+    p.b, p.s_q, p.s_kv, p.h_q, p.h_kv, p.d = 2, 4096, 4096, 16, 2, 128
+    p.window_left, p.window_right, p.scale = -1, 0, 128 ** -0.5
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), 2), (dict(d=256), 2), (dict(window_right=1), 1), (dict(window_left=-2), 1),
+    (dict(h_kv=3), 1), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(b=0), 1),
+    (dict(s_q=0), 1), (dict(q=None), 1), (dict(q=(1 << 20) + 8), 1), (dict(lse=None), 1),
+])
+def test_fwd_rejects_invalid_arguments_on_host(ga, kw, code):
+    p = _params(ga, **kw)
+    assert ga.lib().attn_fwd_workspace_bytes(ctypes.byref(p)) == 0
+    p.workspace_bytes = 1 << 30
+    assert ga.lib().attn_fwd(ctypes.byref(p), None) == code
+
+
+def test_fwd_workspace_checks(ga):
+    p = _params(ga)
+    need = ga.lib().attn_fwd_workspace_bytes(ctypes.byref(p))
+    assert need > 0
+    p.workspace_bytes = need - 1
+    assert ga.lib().attn_fwd(ctypes.byref(p), None) == 1
+    p.workspace_bytes = need
+    p.workspace = (1 << 20) + 128  # not 256-byte aligned
+    assert ga.lib().attn_fwd(ctypes.byref(p), None) == 1
+
+
+def test_bwd_rejects_invalid_arguments_on_host(ga):
+    bp = ga.BwdParams()
+    bp.fwd = _params(ga)
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1  # dout/dq/dk/dv missing
+    bp.dout = bp.dq = bp.dk = bp.dv = 1 << 20
+    bp.fwd.out_fp32 = 1
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
+    bp.fwd.out_fp32 = 0
+    bp.fwd.d = 80
+    assert ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp)) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1 << 20, 1 << 20, 1, 64, 16, 0, 4, 1), 1),           # in == out
+    ((1 << 20, 1 << 21, 1, 60, 16, 0, 4, 1), 1),           # s % 2R != 0
+    ((1 << 20, 1 << 21, 1, 64, 16, 1, 4, 3), 1),           # s % (R*stripe) != 0
+    ((1 << 20, 1 << 21, 1, 64, 16, 2, 4, 1), 1),           # unknown strategy
+    ((1 << 20, (1 << 20) + 512, 1, 64, 16, 0, 4, 1), 1),   # overlapping buffers
+    ((1 << 20, 1 << 21, 1, 64, 16, 0, 0, 1), 1),           # cp_size 0
+])
+def test_reorder_rejects_invalid_arguments_on_host(ga, args, code):
+    assert ga.lib().reorder_causal_lb(*args, None) == code
+    assert ga.lib().inverse_reorder_causal_lb(*args, None) == code
+
+
+def test_merge_rejects_invalid_arguments_on_host(ga):
+    a = 1 << 20
+    assert ga.lib().attn_merge_partial(None, a, a, a, 0, None, 1, 1, 1, 128, None) == 1
+    assert ga.lib().attn_merge_partial(a, a, a, a, 0, None, 1, 1, 1, 12, None) == 1
+    assert ga.lib().attn_merge_partial(a + 4, a, a, a, 0, None, 1, 1, 1, 128, None) == 1
+
+
+def test_device_status_rejects_null(ga):
+    assert ga.lib().attn_read_device_status(None, None) == 1

@@ -1,0 +1,152 @@
+"""GPU parity of attn_fwd through the C ABI against the CPU oracle.
+
+Small cases are checked on every element; the large workloads on sampled
+(batch, head, row-block) outputs that the oracle computes row by row, in the
+same launch configuration the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+import workload
+from oracle import attention as A
+from tests.parity import check_lse, check_out
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def ga():
+    import long_context_attention_attn_gb300 as pkg
+    return pkg
+
+
+def _run(ga, q, k, v, ids, pos, kv_ids, kv_pos, window, scale, out_fp32=False):
+    out, lse = ga.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), ids.to(DEV), pos.to(DEV),
+                           kv_ids.to(DEV), kv_pos.to(DEV), window_left=window, scale=scale,
+                           out_fp32=out_fp32)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+def _full_check(ga, q, k, v, ids, pos, window, scale, kv_ids=None, kv_pos=None, out_fp32=False):
+    kv_ids = ids if kv_ids is None else kv_ids
+    kv_pos = pos if kv_pos is None else kv_pos
+    out, lse = _run(ga, q, k, v, ids, pos, kv_ids, kv_pos, window, scale, out_fp32)
+    ro, rl = A.attn_fwd(q, k, v, ids, pos, kv_ids, kv_pos, window, scale)
+    check_out(out, ro)
+    check_lse(lse, rl)
+    # rows with no visible key are exactly zero
+    empty = np.isneginf(rl)  # [b, h, s]
+    o = out.float().numpy()
+    for bi, h, i in np.argwhere(empty):
+        assert np.all(o[bi, i, h] == 0.0)
+    return out, lse
+
+
+def test_tiny_workload(ga):
+    w = workload.WORKLOADS["tiny"]
+    x = workload.make(w)
+    _full_check(ga, x["q"], x["k"], x["v"], x["ids"], x["pos"], w.window_left, w.scale)
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,window,seed", [
+    (2, 300, 4, 1, 128, 70, 1),     # ragged tail, g = 4
+    (1, 200, 3, 1, 64, -1, 2),      # odd group size: the last pair has one head
+    (1, 384, 2, 2, 128, -1, 3),     # g = 1 (plain MHA)
+    (2, 517, 8, 2, 64, 0, 4),       # window 0: each token sees only itself
+    (1, 1024, 2, 1, 128, 300, 5),
+])
+def test_random_packing(ga, b, s, hq, hkv, d, window, seed):
+    q, k, v = workload.qkv(b, s, hq, hkv, d, seed=seed)
+    ids, pos = workload.random_segments(b, s, seed=seed)
+    _full_check(ga, q, k, v, ids, pos, window, d ** -0.5)
+
+
+def test_fp32_output(ga):
+    q, k, v = workload.qkv(1, 256, 2, 1, 128, seed=9)
+    ids, pos = workload.segments(1, 256, 2)
+    _full_check(ga, q, k, v, ids, pos, -1, 0.1, out_fp32=True)
+
+
+def test_cross_descriptor_and_lengths(ga):
+    """Queries of one shard against keys of another (different lengths)."""
+    q, _, _ = workload.qkv(1, 256, 4, 2, 128, seed=11)
+    _, k, v = workload.qkv(1, 384, 4, 2, 128, seed=12)
+    ids = torch.ones(1, 256, dtype=torch.int32)
+    pos = torch.arange(300, 556, dtype=torch.int32)[None]
+    kv_ids = torch.ones(1, 384, dtype=torch.int32)
+    kv_pos = torch.arange(0, 384, dtype=torch.int32)[None]
+    kv_ids[0, 100:130] = 0
+    _full_check(ga, q, k, v, ids, pos, 200, 0.088, kv_ids, kv_pos)
+
+
+def test_all_padding_and_single_token(ga):
+    q, k, v = workload.qkv(1, 130, 2, 1, 64, seed=13)
+    ids = torch.zeros(1, 130, dtype=torch.int32)
+    pos = torch.zeros(1, 130, dtype=torch.int32)
+    ids[0, 129] = 5
+    _full_check(ga, q, k, v, ids, pos, -1, 0.125)
+
+
+def test_extreme_scores(ga):
+    """Large score ranges exercise the stale-max rescaling."""
+    q, k, v = workload.qkv(1, 512, 2, 1, 128, seed=14)
+    q = (q.float() * 6).to(torch.bfloat16)
+    ids, pos = workload.segments(1, 512, None)
+    _full_check(ga, q, k, v, ids, pos, -1, 0.3)
+
+
+def test_packed_thd_workload_two_groups(ga):
+    w = workload.WORKLOADS["packed_thd"]
+    x = workload.make(w)
+    out, lse = _run(ga, x["q"], x["k"], x["v"], x["ids"], x["pos"], x["ids"], x["pos"],
+                    w.window_left, w.scale)
+    heads = [0, 5, 8, 15]  # both kv groups, both slots of a head pair
+    ro, rl = A.attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"], x["ids"], x["pos"],
+                        w.window_left, w.scale, heads=heads)
+    check_out(out[:, :, heads], ro[:, :, heads])
+    check_lse(lse[:, heads], rl[:, heads])
+    pad = (x["ids"] == 0)
+    assert torch.all(out[pad] == 0)
+    assert torch.all(torch.isneginf(lse.permute(0, 2, 1)[pad]))
+
+
+def _sampled_check(ga, name, samples):
+    w = workload.WORKLOADS[name]
+    x = workload.make(w, device=DEV, with_dout=False)
+    out, lse = ga.attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"],
+                           window_left=w.window_left, scale=w.scale)
+    torch.cuda.synchronize()
+    ids, pos = x["ids"].cpu(), x["pos"].cpu()
+    for bi, h, r0, nrows in samples:
+        rows = np.arange(r0, r0 + nrows)
+        kvh = h // (w.hq // w.hkv)
+        q1 = x["q"][bi:bi + 1, :, h:h + 1].cpu()
+        k1 = x["k"][bi:bi + 1, :, kvh:kvh + 1].cpu()
+        v1 = x["v"][bi:bi + 1, :, kvh:kvh + 1].cpu()
+        ro, rl = A.attn_fwd(q1, k1, v1, ids[bi:bi + 1], pos[bi:bi + 1], ids[bi:bi + 1],
+                            pos[bi:bi + 1], w.window_left, w.scale, rows=rows)
+        check_out(out[bi, r0:r0 + nrows, h].cpu(), ro[0, rows, 0], f"out b{bi} h{h} r{r0}")
+        check_lse(lse[bi, h, r0:r0 + nrows].cpu(), rl[0, 0, rows], f"lse b{bi} h{h} r{r0}")
+    del x, out, lse
+    torch.cuda.empty_cache()
+
+
+def test_packed_swa_sampled(ga):
+    _sampled_check(ga, "packed_swa", [(0, 0, 0, 128), (1, 31, 3000, 200), (0, 9, 4096 + 2900, 300),
+                                      (1, 17, 16384 - 200, 200)])
+
+
+def test_ring_workload_full_attention_sampled(ga):
+    _sampled_check(ga, "ring_cp4", [(0, 0, 0, 128), (0, 63, 32768 - 128, 128), (0, 20, 15000, 64)])
+
+
+def test_full_swa_64k_sampled(ga):
+    """The 64k packed GQA-SWA workload, in the benchmark's launch configuration."""
+    _sampled_check(ga, "full_swa_64k", [
+        (0, 0, 0, 128),                  # slot start
+        (0, 127, 12288 - 128, 160),      # end of slot 1 valid part + padding rows
+        (1, 64, 16384 + 9000, 128),      # window fully active
+        (1, 1, 3 * 16384 + 8100, 200),   # window edge crossing
+    ])

@@ -1,0 +1,118 @@
+"""GPU parity of the integer / HBM-bound kernels through the C ABI:
+reorder + inverse (bit-exact), tile plan (bit-exact), merge (tolerance)."""
+import numpy as np
+import pytest
+import torch
+
+import workload
+from oracle import merge as M
+from oracle import plan as PL
+from oracle import reorder as RO
+from tests.parity import check_lse, check_out
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ga():
+    import long_context_attention_attn_gb300 as pkg
+    return pkg
+
+
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("shape,seq_dim,dtype,strategy,R,stripe", [
+    ((1, 32768, 64, 128), 1, torch.bfloat16, RO.DUAL_CHUNK, 4, 1),   # q of the ring workload
+    ((1, 32768, 8, 128), 1, torch.bfloat16, RO.DUAL_CHUNK, 4, 1),    # k / v
+    ((1, 32768), 1, torch.int32, RO.DUAL_CHUNK, 4, 1),               # ids / pos
+    ((64, 32768), 1, torch.float32, RO.DUAL_CHUNK, 4, 1),            # lse viewed [b*h, s]
+    ((2, 4096, 16, 128), 1, torch.bfloat16, RO.STRIPED, 4, 1),
+    ((2, 65536, 8, 128), 1, torch.bfloat16, RO.STRIPED, 4, 512),
+    ((3, 48, 5), 1, torch.uint8, RO.STRIPED, 3, 2),                  # odd byte rows
+    ((2, 40, 3), 1, torch.int32, RO.DUAL_CHUNK, 2, 1),               # 12-byte rows
+])
+def test_reorder_bit_exact(ga, shape, seq_dim, dtype, strategy, R, stripe):
+    g = torch.Generator(device=DEV).manual_seed(7)
+    if dtype.is_floating_point:
+        x = torch.randn(shape, generator=g, device=DEV).to(dtype)
+    else:
+        x = torch.randint(0, 120, shape, generator=g, device=DEV).to(dtype)
+    y = ga.reorder_causal_lb(x, strategy, R, stripe, seq_dim=seq_dim)
+    torch.cuda.synchronize()
+    src = torch.from_numpy(RO.src_index(shape[seq_dim], strategy, R, stripe)).to(DEV)
+    ref = x.index_select(seq_dim, src)
+    assert torch.equal(y.view(torch.uint8) if dtype != torch.uint8 else y,
+                       ref.view(torch.uint8) if dtype != torch.uint8 else ref)
+    z = ga.inverse_reorder_causal_lb(y, strategy, R, stripe, seq_dim=seq_dim)
+    torch.cuda.synchronize()
+    assert torch.equal(z, x)
+
+
+def test_reorder_matches_oracle_on_host_copy(ga):
+    x = torch.arange(2 * 24 * 3, dtype=torch.int32).reshape(2, 24, 3)
+    y = ga.reorder_causal_lb(x.to(DEV), RO.DUAL_CHUNK, 3).cpu().numpy()
+    assert np.array_equal(y, RO.reorder(x.numpy(), RO.DUAL_CHUNK, 3))
+    y = ga.reorder_causal_lb(x.to(DEV), RO.STRIPED, 4, 2).cpu().numpy()
+    assert np.array_equal(y, RO.reorder(x.numpy(), RO.STRIPED, 4, 2))
+
+
+def _plan_case(ga, ids, pos, window, s_kv_ids=None, s_kv_pos=None):
+    kv_ids = ids if s_kv_ids is None else s_kv_ids
+    kv_pos = pos if s_kv_pos is None else s_kv_pos
+    b, s = ids.shape
+    q = torch.empty(b, s, 2, 64, dtype=torch.bfloat16, device=DEV)
+    k = torch.empty(b, kv_ids.shape[1], 1, 64, dtype=torch.bfloat16, device=DEV)
+    cls, rng = ga.attn_tile_plan(q, k, ids.to(DEV), pos.to(DEV), kv_ids.to(DEV),
+                                 kv_pos.to(DEV), window_left=window)
+    torch.cuda.synchronize()
+    ref = PL.classes(ids.numpy(), pos.numpy(), kv_ids.numpy(), kv_pos.numpy(), window)
+    assert np.array_equal(cls.cpu().numpy(), ref)
+    assert np.array_equal(rng.cpu().numpy(), PL.ranges(ref))
+
+
+@pytest.mark.parametrize("name", ["tiny", "packed_thd", "packed_swa", "ring_cp4", "full_swa_64k"])
+def test_plan_bit_exact_on_workloads(ga, name):
+    w = workload.WORKLOADS[name]
+    ids, pos = workload.segments(w.b, w.s, w.slots)
+    if w.s > 20000:  # keep the pure-Python oracle plan within seconds
+        ids, pos = ids[:1], pos[:1]
+    _plan_case(ga, ids, pos, w.window_left)
+
+
+@pytest.mark.parametrize("seed,s,window", [(1, 1000, -1), (2, 777, 40), (3, 1300, 0)])
+def test_plan_bit_exact_on_random_packing(ga, seed, s, window):
+    ids, pos = workload.random_segments(2, s, seed=seed)
+    _plan_case(ga, ids, pos, window)
+
+
+def test_plan_cross_descriptor(ga):
+    ids, pos = workload.segments(1, 1024, None)
+    kv_ids, kv_pos = ids[:, 256:768].contiguous(), pos[:, 256:768].contiguous()
+    _plan_case(ga, ids, pos, 100, kv_ids, kv_pos)
+
+
+@pytest.mark.parametrize("blk_dtype,final", [(torch.float32, False), (torch.bfloat16, False),
+                                             (torch.float32, True)])
+def test_merge_matches_oracle(ga, blk_dtype, final):
+    b, s, h, d = 2, 1000, 8, 128
+    g = torch.Generator().manual_seed(3)
+    oa = torch.randn(b, s, h, d, generator=g)
+    ob = torch.randn(b, s, h, d, generator=g).to(blk_dtype)
+    la = torch.randn(b, h, s, generator=g) * 3
+    lb = torch.randn(b, h, s, generator=g) * 3
+    la[:, :, :50] = -torch.inf      # accumulator empty
+    lb[:, :, 40:90] = -torch.inf    # block empty
+    oa[:, :50] = float("nan")       # never read where lse_acc = -inf
+    ref_o, ref_l = M.merge_partial(torch.nan_to_num(oa).numpy(), la.numpy(),
+                                   ob.float().numpy(), lb.numpy())
+    ref_o[:, 40:50] = 0.0
+    acc, lacc = oa.to(DEV), la.to(DEV)
+    fin = torch.empty(b, s, h, d, dtype=torch.bfloat16, device=DEV) if final else None
+    o, l = ga.attn_merge_partial(acc, lacc, ob.to(DEV), lb.to(DEV), out_final=fin)
+    torch.cuda.synchronize()
+    got = o.float().cpu().numpy()
+    check_out(got, ref_o)
+    check_lse(l.cpu(), ref_l)
+    if not final:
+        np.testing.assert_allclose(got, ref_o, atol=1e-5, rtol=1e-5)
