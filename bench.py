@@ -1,0 +1,385 @@
+"""Benchmark: packed-THD GQA sliding-window attention, forward + backward.
+
+One step = attn_fwd + attn_bwd (tile plan, fused forward, D pre-pass, fused
+backward, dQ finalise: every row of the hot path that a training step runs)
+on the 64k packed workload of the TE tutorial: b=2, s=65536 (4 slots of 16384
+with 12288 valid tokens), 128 query heads, 8 kv heads, d=128, causal with a
+(8192, 0) window, bf16.  Throughput counts valid (query, key) pairs only:
+4*d FLOP per pair and head forward, 10*d backward (S recomputed).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
+instance of the workload (weak scaling, no data-path collective); the step
+time is the maximum over ranks.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s on valid pairs, % of GB300 dense BF16 peak (1 GPU)"
+WORKLOAD = "full_swa_64k"
+# TE tutorial, section 5: single-GPU fused attention fwd+bwd on this exact
+# workload, 126.687 ms on one GB200 (context, another machine).
+PAGE_GB200_MS = 126.68747901916504
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def valid_pairs(w):
+    """Exact visible-pair count of the workload (per head, all batch rows),
+    counted from the segment descriptor: per segment of L valid tokens with an
+    inclusive window W, sum over positions p of min(p, W) + 1."""
+    import workload
+    ids, pos = workload.segments(w.b, w.s, w.slots)
+    total = 0
+    for bi in range(w.b):
+        i, p = ids[bi].tolist(), pos[bi].tolist()
+        seg_len = {}
+        for sid in i:
+            if sid:
+                seg_len[sid] = seg_len.get(sid, 0) + 1
+        for sid, L in seg_len.items():
+            W = w.window_left
+            if W < 0 or W >= L - 1:
+                total += L * (L + 1) // 2
+            else:
+                total += (W + 1) * (W + 2) // 2 + (L - W - 1) * (W + 1)
+    return total
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return dict(bf16_burst=m["bf16_tflops"], bf16_sustained=m["bf16_tflops_sustained"],
+                    hbm_gbs=m["hbm_gbs"], source="measured (MEASURED_PEAKS.json)")
+    return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm_gbs=6800.0,
+                source="fallback (profiling recipe)")
+
+
+class Clocks:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"]}
+        loaded = sorted(sm)[len(sm) // 4:] or sm  # drop idle ramp samples
+        med = sorted(loaded)[len(loaded) // 2]
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(w, budget_s=12.0, max_blocks=48):
+    """Times the CPU oracle (fwd + bwd) on query-row blocks of one kv group of
+    the workload until ~budget_s seconds of CPU work; returns (TFLOP/s, info)."""
+    import numpy as np
+    import torch
+
+    import workload
+    from oracle import attention as A
+
+    torch.set_num_threads(os.cpu_count() or 1)
+    g = w.hq // w.hkv
+    # Sample: batch row 0, kv group 0 (all its query heads), query-row blocks of
+    # 64 from position 9000 of the first segment (window fully open).  The
+    # inputs are cut to the first segment's valid tokens, which hold every key
+    # those rows can see; positions travel with the tokens.
+    n_tok = 3 * (w.s // w.slots) // 4 if w.slots else w.s
+    ids, pos = workload.segments(1, w.s, w.slots)
+    ids, pos = ids[:, :n_tok].numpy(), pos[:, :n_tok].numpy()
+    q, k, v, dout = (t[:, :n_tok].to(torch.float64).numpy() for t in
+                     workload.qkv(1, w.s, g, 1, w.d, seed=workload.SEED, with_dout=True))
+    flops = 0.0
+    t0 = time.perf_counter()
+    blocks = 0
+    r0 = min(9000, n_tok - 64 * max_blocks)
+    while blocks < max_blocks:
+        rows = np.arange(r0 + 64 * blocks, r0 + 64 * (blocks + 1))
+        A.attn_fwd(q, k, v, ids, pos, ids, pos, w.window_left, w.scale, rows=rows)
+        A.attn_bwd(q, k, v, dout, ids, pos, ids, pos, w.window_left, w.scale, rows=rows)
+        pairs = sum(min(int(p), w.window_left) + 1 for p in pos[0, rows])
+        flops += pairs * g * 14 * w.d
+        blocks += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    info = dict(cores=torch.get_num_threads(),
+                sample=f"{blocks} blocks of 64 query rows from position {r0} x {g} heads (kv group 0, "
+                       f"batch 0) of {w.name}, fwd+bwd, {dt:.1f} s")
+    return flops / dt / 1e12, info
+
+
+def run_reference(args, rank):
+    import workload
+    w = workload.WORKLOADS[WORKLOAD]
+    if rank != 0:
+        return
+    vals = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        val, info = oracle_sample(w, budget_s=2.0, max_blocks=2)
+        if i >= args.warmup:
+            vals.append(val)
+    value = sum(vals) / len(vals)
+    pairs = valid_pairs(w)
+    flops = pairs * w.hq * 14 * w.d
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": flops / (value * 1e12) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "b": w.b, "s": w.s, "hq": w.hq, "hkv": w.hkv, "d": w.d,
+                   "window": [w.window_left, 0], "step": "fwd+bwd (CPU oracle, sampled rows)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": info["cores"],
+                         "kind": "oracle", "sample": info["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import long_context_attention_attn_gb300 as ga
+    import workload
+    from long_context_attention_attn_gb300 import _build
+
+    if not os.path.exists(ga.LIB_PATH):
+        _build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = workload.WORKLOADS[WORKLOAD]
+    pairs = valid_pairs(w)
+    fwd_flop = 4 * w.d * w.hq * pairs
+    bwd_flop = 10 * w.d * w.hq * pairs
+    x = workload.make(w, device=dev, with_dout=True, seed=workload.SEED + rank)
+    q, k, v, dout, ids, pos = x["q"], x["k"], x["v"], x["dout"], x["ids"], x["pos"]
+    out = torch.empty_like(q)
+    lse = torch.empty(w.b, w.hq, w.s, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale, out=out,
+                    lse=lse, workspace=ws)
+        if ev:
+            ev[1].record(stream)
+        ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=w.window_left, scale=w.scale,
+                    dq=dq, dk=dk, dv=dv, workspace=ws)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    status = ga.read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {ga.status_string(status)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = Clocks(local_rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    fwd_ms = sorted(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = sorted(e[1].elapsed_time(e[2]) for e in evs)
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    bwd_avg = sum(bwd_ms) / len(bwd_ms)
+    ms_per_step = total_ms / args.steps
+    if dist:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = world * (fwd_flop + bwd_flop) / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, gradients out
+    e2e = None
+    if not args.no_e2e:
+        h_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v),
+                                                         ("dout", dout), ("ids", ids),
+                                                         ("pos", pos))}
+        h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for n, t in (("dq", dq), ("dk", dk), ("dv", dv))}
+        d_in = {n: torch.empty_like(t, device=dev) for n, t in h_in.items()}
+        bi = sum(t.numel() * t.element_size() for t in h_in.values())
+        bo = sum(t.numel() * t.element_size() for t in h_out.values())
+
+        def e2e_step():
+            for n, t in h_in.items():
+                d_in[n].copy_(t, non_blocking=True)
+            ga.attn_fwd(d_in["q"], d_in["k"], d_in["v"], d_in["ids"], d_in["pos"],
+                        window_left=w.window_left, scale=w.scale, out=out, lse=lse, workspace=ws)
+            ga.attn_bwd(d_in["q"], d_in["k"], d_in["v"], out, lse, d_in["dout"], d_in["ids"],
+                        d_in["pos"], window_left=w.window_left, scale=w.scale, dq=dq, dk=dk,
+                        dv=dv, workspace=ws)
+            h_out["dq"].copy_(dq, non_blocking=True)
+            h_out["dk"].copy_(dk, non_blocking=True)
+            h_out["dv"].copy_(dv, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(2, min(args.steps, 5))
+        if dist:
+            dist.barrier()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b_) / n_e2e
+        if dist:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * (fwd_flop + bwd_flop) / (e2e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo}
+        del h_in, h_out, d_in
+
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    pk = peaks()
+    bwd_tflops = bwd_flop / (bwd_avg * 1e-3) / 1e12
+    fwd_tflops = fwd_flop / (fwd_avg * 1e-3) / 1e12
+    per_gpu = value / world
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        val, info = oracle_sample(w)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
+               "sample": info["sample"]}
+    launches_per_step = 5 + 9  # fwd: 4 plan + 1 fused; bwd: 6 plan + D + fused + dQ finalise
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / world / ((fwd_flop + bwd_flop) / (PAGE_GB200_MS * 1e-3) / 1e12),
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "b": w.b, "s": w.s, "slots": w.slots, "hq": w.hq,
+                   "hkv": w.hkv, "d": w.d, "window": [w.window_left, 0],
+                   "step": "attn_fwd + attn_bwd", "valid_pairs_per_head": pairs,
+                   "flop_per_pair_head": {"fwd": 4 * w.d, "bwd": 10 * w.d},
+                   "l2": "inputs larger than L2 (q, dout 4 GiB each); no flush",
+                   "vs_baseline_ref": "TE tutorial single-GB200 fwd+bwd 126.687 ms on this "
+                                      "workload, converted with the same FLOP count",
+                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+        "pct_of_peak": {"burst": 100 * per_gpu / pk["bf16_burst"],
+                        "sustained": 100 * per_gpu / pk["bf16_sustained"],
+                        "source": pk["source"]},
+        "components": {"fwd_ms": fwd_avg, "bwd_ms": bwd_avg, "fwd_tflops": fwd_tflops,
+                       "bwd_tflops": bwd_tflops},
+        "roofline": {"kernel": "attn_bwd (fused backward + its D pre-pass, plan and dQ "
+                               "finalise; timed per call)",
+                     "bound": "tensor", "achieved": bwd_tflops, "peak": pk["bf16_sustained"],
+                     "unit": "TFLOP/s", "frac": bwd_tflops / pk["bf16_sustained"],
+                     "peak_kind": f"bf16 sustained, {pk['source']}", "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,8 +1,536 @@
-// Backward attention (placeholder until the fused kernel lands).
+// Backward attention over packed THD inputs on sm_103a.
+//
+// Gradient of sum(O * dO) (TE tutorial section 5 differentiates the vdot of
+// the output with dout) through O = softmax(scale * Q K^T + M) V ("Context
+// parallelism and ring attention", section "The attention problem"):
+//   P = exp(scale * S - LSE),  dV = P^T dO,  dP = dO V^T,
+//   dS = P * (dP - D) with D = rowsum(dO * O),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// One CTA owns a 128-key tile of one kv head and keeps dK and dV for it in
+// TMEM while it walks over every (query tile, query head of the GQA group)
+// that can see the tile (a "step").  Per step it recomputes S^T = K Q^T and
+// dP^T = V dO^T on tcgen05 (keys on TMEM lanes), forms P^T and dS^T in
+// registers (one thread per key row), writes them back to TMEM as bf16 (the A
+// operands of dV += P^T dO and dK += dS^T Q), stages dS in shared memory for
+// dQ = dS K, and adds the dQ tile into an fp32 accumulator in global memory.
+//
+// Roles (384 threads): warp 0 TMA producer; warp 1 MMA issuer and TMEM owner;
+// warps 4-7 and 8-11 the two element-wise warpgroups (query columns 0-63 and
+// 64-127 of S^T / dP^T; each also reads back half of the dQ tile).
+// TMEM: dV [0,D)  dK [128,128+D)  S^T [256,384)  dP^T [384,512);
+// P^T / dS^T overwrite the first 64 columns of S^T / dP^T, and the dQ tile
+// lands in the last 64 columns of S^T (d 0-63) and dP^T (d 64-127).
+#include <cuda_bf16.h>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace gb300 {
 
-cudaError_t launch_attn_bwd(const BwdLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BM = 128;  // query rows per step
+constexpr int BN = 128;  // key rows per CTA
+constexpr int NQ = 2;    // Q tile stages
+constexpr int NV = 2;    // per-step vector ring entries
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdArgs {
+  const int* q_ids;
+  const int* q_pos;
+  const int* kv_ids;
+  const int* kv_pos;
+  const float* lse;
+  const float* Dv;
+  float* dq_acc;
+  void* dk;
+  void* dv;
+  const uint8_t* cls;
+  const int2* krange;
+  const int* order;
+  int* status;
+  int b, s_q, s_kv, hq, hkv, g, nq, nk;
+  int window;
+  float scale;
+  float scale_log2;
+};
+
+template <int D>
+struct BLayout {
+  static constexpr int kChunk = 128 * 128;  // 128 rows x 128 bytes
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int k_off = 0;
+  static constexpr int v_off = k_off + kTile;
+  static constexpr int q_off = v_off + kTile;          // NQ stages
+  static constexpr int do_off = q_off + NQ * kTile;    // 1 stage
+  static constexpr int ds_off = do_off + kTile;        // dS: 128 q x 128 keys bf16, MN-major
+  static constexpr int vec_off = ds_off + 2 * kChunk;  // NV x {lse2, D, ids, pos}[128]
+  static constexpr int bar_off = vec_off + NV * 4 * BM * 4;
+  static constexpr int bytes = bar_off + 256;
+  static constexpr int alloc = (bytes + 1024) > 150 * 1024 ? (bytes + 1024) : 150 * 1024;
+};
+
+struct BBars {
+  uint64_t kv_full;
+  uint64_t q_full[NQ];
+  uint64_t q_empty[NQ];
+  uint64_t do_full;
+  uint64_t do_empty;
+  uint64_t vec_full[NV];
+  uint64_t vec_empty[NV];
+  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, dk_done;
+  uint64_t s_read, dp_read;  // both element-wise halves have read S^T / dP^T
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(BBars) <= 256, "barrier block too large");
+
+// Iterates over the steps (query tile, head) of a CTA in a fixed order.
+struct StepIter {
+  int i, hh, i_end, g;
+  const uint8_t* cls_col;  // cls + b*nq*nk + c, stride nk
+  int nk;
+  __device__ bool valid() const { return i <= i_end; }
+  __device__ uint8_t kind() const { return cls_col[(size_t)i * nk]; }
+  __device__ void skip_to_valid() {
+    while (i <= i_end && cls_col[(size_t)i * nk] == kSkip) ++i;
+  }
+  __device__ void next() {
+    if (++hh == g) {
+      hh = 0;
+      ++i;
+      skip_to_valid();
+    }
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs a) {
+  using L = BLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  BBars* bars = reinterpret_cast<BBars*>(smem + L::bar_off);
+  float* vec = reinterpret_cast<float*>(smem + L::vec_off);  // [NV][4][BM]
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (a.status && *reinterpret_cast<volatile int*>(a.status) != kStatusOk) return;
+
+  // ---- work unit: (b, kv tile) heavy first, then kv head
+  const int rank = blockIdx.x / a.hkv;
+  const int kvh = blockIdx.x % a.hkv;
+  const int e = a.order[rank];
+  const int bi = e / a.nk;
+  const int kt = e % a.nk;
+  const int2 rng = a.krange[e];
+  StepIter it0;
+  it0.i = rng.x;
+  it0.hh = 0;
+  it0.i_end = rng.y;
+  it0.g = a.g;
+  it0.cls_col = a.cls + (size_t)bi * a.nq * a.nk + kt;
+  it0.nk = a.nk;
+  it0.skip_to_valid();
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+    }
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&bars->vec_full[i], 1);
+      mbar_init(&bars->vec_empty[i], 256);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, 256);
+    mbar_init(&bars->dk_done, 1);
+    mbar_init(&bars->s_read, 256);
+    mbar_init(&bars->dp_read, 256);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtx ctx{&bars->abort_flag, a.status};
+  constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
+
+  if (warp == 0) {
+    // ======================================================== producer
+    int last_q[NQ] = {-1, -1};
+    int last_do = -1;
+    int nsteps = 0;
+    bool ok = true;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kTile);
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_4d(smem_u32(smem + L::k_off + c * L::kChunk), &tm_k, c * 64, kvh, kt * BN, bi,
+                    &bars->kv_full);
+        tma_load_4d(smem_u32(smem + L::v_off + c * L::kChunk), &tm_v, c * 64, kvh, kt * BN, bi,
+                    &bars->kv_full);
+      }
+    }
+    for (StepIter it = it0; it.valid() && ok; it.next(), ++nsteps) {
+      const int t = nsteps;
+      const int h = kvh * a.g + it.hh;
+      const int qt = it.i;
+      // Q tile
+      if (lane == 0) {
+        const int qs = t % NQ, use = t / NQ;
+        ok = mbar_wait(&bars->q_empty[qs], (use & 1) ^ 1, ctx);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars->q_full[qs], L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_4d(smem_u32(smem + L::q_off + qs * L::kTile + c * L::kChunk), &tm_q, c * 64, h,
+                        qt * BM, bi, &bars->q_full[qs]);
+          last_q[qs] = use;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // per-row vectors: LSE (base 2, +inf for rows without keys), D, ids, pos
+      {
+        const int en = t % NV, use = t / NV;
+        if (lane == 0) ok = mbar_wait(&bars->vec_empty[en], (use & 1) ^ 1, ctx);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        float* v = vec + en * 4 * BM;
+        int* vi = reinterpret_cast<int*>(v);
+        const int64_t lbase = ((int64_t)bi * a.hq + h) * a.s_q;
+        const int64_t ibase = (int64_t)bi * a.s_q;
+        for (int r = lane; r < BM; r += 32) {
+          const int gq = qt * BM + r;
+          const bool in = gq < a.s_q;
+          const float l = in ? a.lse[lbase + gq] : -INFINITY;
+          v[r] = (l == -INFINITY) ? INFINITY : l * kLog2e;
+          v[BM + r] = in ? a.Dv[lbase + gq] : 0.f;
+          vi[2 * BM + r] = in ? a.q_ids[ibase + gq] : 0;
+          vi[3 * BM + r] = in ? a.q_pos[ibase + gq] : 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->vec_full[en]);
+      }
+      // dO tile
+      if (lane == 0) {
+        ok = mbar_wait(&bars->do_empty, (t & 1) ^ 1, ctx);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars->do_full, L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_4d(smem_u32(smem + L::do_off + c * L::kChunk), &tm_do, c * 64, h, qt * BM, bi,
+                        &bars->do_full);
+          last_do = t;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (lane == 0) {
+      mbar_wait_drain(&bars->kv_full, 0, a.status);
+      for (int i = 0; i < NQ; ++i)
+        if (last_q[i] >= 0) mbar_wait_drain(&bars->q_full[i], last_q[i] & 1, a.status);
+      if (last_do >= 0) mbar_wait_drain(&bars->do_full, last_do & 1, a.status);
+    }
+  } else if (warp == 1) {
+    // ======================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);    // dV, dK (A in TMEM)
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);     // dQ halves
+      const uint32_t k_base = smem_u32(smem + L::k_off);
+      const uint32_t v_base = smem_u32(smem + L::v_off);
+      const uint32_t q_base = smem_u32(smem + L::q_off);
+      const uint32_t do_base = smem_u32(smem + L::do_off);
+      const uint32_t ds_base = smem_u32(smem + L::ds_off);
+      bool ok = mbar_wait(&bars->kv_full, 0, ctx);
+      int t = 0;
+      for (StepIter it = it0; it.valid() && ok; it.next(), ++t) {
+        const int qs = t % NQ;
+        ok = mbar_wait(&bars->q_full[qs], (t / NQ) & 1, ctx);
+        if (ok && t > 0) ok = mbar_wait(&bars->dq_empty, (t - 1) & 1, ctx);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qb = q_base + qs * L::kTile;
+        // S^T = K Q^T  (M = keys, N = queries, K = d)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::kChunk + (kk % 4) * 32;
+          mma_ss(tmem + kColS, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
+                 id_kk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full);
+        // dP^T = V dO^T
+        ok = mbar_wait(&bars->do_full, t & 1, ctx);
+        if (ok && t > 0) ok = mbar_wait(&bars->dk_done, (t - 1) & 1, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::kChunk + (kk % 4) * 32;
+          mma_ss(tmem + kColDP, sdesc_sw128(v_base + off, 16, 1024),
+                 sdesc_sw128(do_base + off, 16, 1024), id_kk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->dp_full);
+        // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major)
+        ok = mbar_wait(&bars->p_full, t & 1, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          mma_ts(tmem + kColDV, tmem + kColS + kk * 8,
+                 sdesc_sw128(do_base + kk * 2048, L::kChunk, 1024), id_acc,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->do_empty);
+        // dQ = dS K  (A = dS in smem MN-major, B = K MN-major), 64 d columns per MMA
+        ok = mbar_wait(&bars->ds_full, t & 1, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c) {
+          const uint32_t dst = (c == 0) ? (tmem + kColS + 64) : (tmem + kColDP + 64);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ss(dst, sdesc_sw128(ds_base + kk * 2048, L::kChunk, 1024),
+                   sdesc_sw128(k_base + c * L::kChunk + kk * 2048, L::kChunk, 1024), id_dq,
+                   kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->dq_full);
+        // dK += dS^T Q  (A = dS^T in TMEM, B = Q MN-major)
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          mma_ts(tmem + kColDK, tmem + kColDP + kk * 8, sdesc_sw128(qb + kk * 2048, L::kChunk, 1024),
+                 id_acc, (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->dk_done);
+        mma_commit(&bars->q_empty[qs]);
+      }
+      mma_commit(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0, a.status);
+    }
+  } else if (warp >= 4) {
+    // ======================================================== element-wise
+    const int w = (warp - 4) / 4;  // query columns [64w, 64w + 64)
+    const int wq = warp % 4;
+    const int kr = wq * 32 + lane;  // key row (S^T lanes) / query row (dQ lanes)
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const int key = kt * BN + kr;
+    const bool key_in = key < a.s_kv;
+    const int ik = key_in ? a.kv_ids[(int64_t)bi * a.s_kv + key] : 0;
+    const int pk = key_in ? a.kv_pos[(int64_t)bi * a.s_kv + key] : 0;
+    const float sl2 = a.scale_log2;
+    uint8_t* ds_smem = smem + L::ds_off + w * L::kChunk + kr * 128;
+    int t = 0;
+    bool ok = true;
+    for (StepIter it = it0; it.valid(); it.next(), ++t) {
+      const int h = kvh * a.g + it.hh;
+      const int qt = it.i;
+      const bool partial = it.kind() == kPartial;
+      const int en = t % NV;
+      ok = mbar_wait(&bars->vec_full[en], (t / NV) & 1, ctx);
+      ok = mbar_wait(&bars->s_full, t & 1, ctx) && ok;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2 = vec + en * 4 * BM + 64 * w;
+      const float* dvec = vec + en * 4 * BM + BM + 64 * w;
+      const int* qid = reinterpret_cast<const int*>(vec + en * 4 * BM + 2 * BM) + 64 * w;
+      const int* qpos = reinterpret_cast<const int*>(vec + en * 4 * BM + 3 * BM) + 64 * w;
+      uint32_t r[64];
+      tmem_ld32(tmem + lane_off + kColS + 64 * w, &r[0]);
+      tmem_ld32(tmem + lane_off + kColS + 64 * w + 32, &r[32]);
+      tmem_wait_ld();
+      float p[64];
+#pragma unroll
+      for (int u = 0; u < 64; ++u) p[u] = ex2(fmaf(__uint_as_float(r[u]), sl2, -lse2[u]));
+      if (partial) {
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+          bool vis = (qid[u] == ik) && (ik != 0) && (pk <= qpos[u]);
+          if (a.window >= 0) vis = vis && (qpos[u] - pk <= a.window);
+          if (!vis) p[u] = 0.f;
+        }
+      }
+      uint32_t pk2[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) pk2[u] = pack_bf16(p[2 * u], p[2 * u + 1]);
+      // both halves have read S^T before P^T overwrites it
+      mbar_arrive(&bars->s_read);
+      ok = mbar_wait(&bars->s_read, t & 1, ctx);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tmem_st32(tmem + lane_off + kColS + 32 * w, pk2);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+      // dS^T = P^T * (dP^T - D)
+      ok = mbar_wait(&bars->dp_full, t & 1, ctx);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + kColDP + 64 * w, &r[0]);
+      tmem_ld32(tmem + lane_off + kColDP + 64 * w + 32, &r[32]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        pk2[u] = pack_bf16(p[2 * u] * (__uint_as_float(r[2 * u]) - dvec[2 * u]),
+                           p[2 * u + 1] * (__uint_as_float(r[2 * u + 1]) - dvec[2 * u + 1]));
+      // both halves have read dP^T before dS^T overwrites it
+      mbar_arrive(&bars->dp_read);
+      ok = mbar_wait(&bars->dp_read, t & 1, ctx);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tmem_st32(tmem + lane_off + kColDP + 32 * w, pk2);
+      // dS (queries x keys) in shared memory, MN-major 128B-swizzled: key row kr
+      // holds this half's 64 query values.
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint4 v4 = make_uint4(pk2[4 * u], pk2[4 * u + 1], pk2[4 * u + 2], pk2[4 * u + 3]);
+        *reinterpret_cast<uint4*>(ds_smem + ((u ^ (kr & 7)) * 16)) = v4;
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full);
+      // dQ tile readout: TMEM lanes are query rows here
+      ok = mbar_wait(&bars->dq_full, t & 1, ctx);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      constexpr int kHalf = D / 2;
+      uint32_t q[kHalf];
+      const uint32_t src = (D == 128) ? (tmem + lane_off + (w == 0 ? kColS : kColDP) + 64)
+                                      : (tmem + lane_off + kColS + 64 + 32 * w);
+#pragma unroll
+      for (int c = 0; c < kHalf; c += 32) tmem_ld32(src + c, &q[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->dq_empty);
+      const int gq = qt * BM + kr;
+      const int* qid_all = reinterpret_cast<const int*>(vec + en * 4 * BM + 2 * BM);
+      if (gq < a.s_q && qid_all[kr] != 0) {
+        float4* dst = reinterpret_cast<float4*>(
+            a.dq_acc + (((int64_t)bi * a.s_q + gq) * a.hq + h) * D + w * kHalf);
+        const float sc = a.scale;
+#pragma unroll
+        for (int c = 0; c < kHalf / 4; ++c)
+          atomicAdd(dst + c, make_float4(__uint_as_float(q[4 * c]) * sc,
+                                         __uint_as_float(q[4 * c + 1]) * sc,
+                                         __uint_as_float(q[4 * c + 2]) * sc,
+                                         __uint_as_float(q[4 * c + 3]) * sc));
+      }
+      mbar_arrive(&bars->vec_empty[en]);
+    }
+    // ---- epilogue: dV (half 0) and dK (half 1) rows of this key tile, bf16
+    if (ok && t > 0) {
+      ok = mbar_wait(&bars->dk_done, (t - 1) & 1, ctx);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    if (ok) {
+      const float sc = (w == 0) ? 1.f : a.scale;
+      __nv_bfloat16* dst_base = static_cast<__nv_bfloat16*>(w == 0 ? a.dv : a.dk);
+      const int64_t row = ((int64_t)bi * a.s_kv + key) * a.hkv + kvh;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        if (t > 0) {
+          tmem_ld32(tmem + lane_off + (w == 0 ? kColDV : kColDK) + c, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] = 0u;
+        }
+        if (!key_in) continue;
+        uint4* dst = reinterpret_cast<uint4*>(dst_base + row * D + c);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(o[8 * u + 0]) * sc, __uint_as_float(o[8 * u + 1]) * sc);
+          v.y = pack_bf16(__uint_as_float(o[8 * u + 2]) * sc, __uint_as_float(o[8 * u + 3]) * sc);
+          v.z = pack_bf16(__uint_as_float(o[8 * u + 4]) * sc, __uint_as_float(o[8 * u + 5]) * sc);
+          v.w = pack_bf16(__uint_as_float(o[8 * u + 6]) * sc, __uint_as_float(o[8 * u + 7]) * sc);
+          dst[u] = v;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
+  const attn_bwd_params& p = *Lc.p;
+  const attn_fwd_params& f = p.fwd;
+  BwdArgs a;
+  a.q_ids = f.q_segment_ids;
+  a.q_pos = f.q_segment_pos;
+  a.kv_ids = f.kv_segment_ids;
+  a.kv_pos = f.kv_segment_pos;
+  a.lse = f.lse;
+  a.Dv = Lc.D;
+  a.dq_acc = Lc.dq_acc;
+  a.dk = p.dk;
+  a.dv = p.dv;
+  a.cls = Lc.plan.classes;
+  a.krange = Lc.plan.kv_range;
+  a.order = Lc.plan.kv_order;
+  a.status = Lc.plan.status;
+  a.b = (int)f.b;
+  a.s_q = (int)f.s_q;
+  a.s_kv = (int)f.s_kv;
+  a.hq = (int)f.h_q;
+  a.hkv = (int)f.h_kv;
+  a.g = (int)(f.h_q / f.h_kv);
+  a.nq = (int)Lc.nq;
+  a.nk = (int)Lc.nk;
+  a.window = f.window_left;
+  a.scale = f.scale;
+  a.scale_log2 = f.scale * kLog2e;
+  const int64_t units = f.b * Lc.nk * f.h_kv;
+  if (units == 0) return cudaSuccess;
+  if (f.d == 128) {
+    const int smem = BLayout<128>::alloc;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<128>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_bwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v,
+                                                                  Lc.tm_do, a);
+  } else {
+    const int smem = BLayout<64>::alloc;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_bwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v,
+                                                                 Lc.tm_do, a);
+  }
+  return cudaGetLastError();
+}
 
 }  // namespace gb300

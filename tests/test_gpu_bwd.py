@@ -1,0 +1,114 @@
+"""GPU parity of attn_bwd through the C ABI against the CPU oracle.
+
+The oracle differentiates the exact float64 attention itself (its own O for
+D = rowsum(dO * O)); the GPU consumes its own bf16 forward output and LSE, as
+a training step would.  Small cases are compared on every element; the large
+workloads on sampled query rows (dQ) and sampled key tiles (dK, dV, complete
+because every query row that sees those keys is included)."""
+import numpy as np
+import pytest
+import torch
+
+import workload
+from oracle import attention as A
+from tests.parity import check_grad
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def ga():
+    import long_context_attention_attn_gb300 as pkg
+    return pkg
+
+
+def _gpu_grads(ga, x, window, scale):
+    g = {k: v.to(DEV) for k, v in x.items()}
+    out, lse = ga.attn_fwd(g["q"], g["k"], g["v"], g["ids"], g["pos"], window_left=window,
+                           scale=scale)
+    dq, dk, dv = ga.attn_bwd(g["q"], g["k"], g["v"], out, lse, g["dout"], g["ids"], g["pos"],
+                             window_left=window, scale=scale)
+    torch.cuda.synchronize()
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def _full_check(ga, x, window, scale):
+    dq, dk, dv = _gpu_grads(ga, x, window, scale)
+    rq, rk, rv = A.attn_bwd(x["q"], x["k"], x["v"], x["dout"], x["ids"], x["pos"], x["ids"],
+                            x["pos"], window, scale)
+    check_grad(dq, rq, "dq")
+    check_grad(dk, rk, "dk")
+    check_grad(dv, rv, "dv")
+    pad = (x["ids"] == 0)
+    assert torch.all(dq[pad] == 0) and torch.all(dk[pad] == 0) and torch.all(dv[pad] == 0)
+
+
+def test_tiny_workload(ga):
+    w = workload.WORKLOADS["tiny"]
+    _full_check(ga, workload.make(w, with_dout=True), w.window_left, w.scale)
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,window,seed", [
+    (2, 300, 4, 1, 128, 70, 1),   # ragged tail, g = 4
+    (1, 200, 3, 1, 64, -1, 2),    # odd group
+    (1, 384, 2, 2, 128, -1, 3),   # g = 1
+    (1, 640, 4, 2, 128, 0, 4),    # window 0
+])
+def test_random_packing(ga, b, s, hq, hkv, d, window, seed):
+    q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=seed, with_dout=True)
+    ids, pos = workload.random_segments(b, s, seed=seed)
+    x = dict(q=q, k=k, v=v, dout=dout, ids=ids, pos=pos)
+    _full_check(ga, x, window, d ** -0.5)
+
+
+def _sampled(ga, name, dq_samples, key_samples):
+    w = workload.WORKLOADS[name]
+    x = workload.make(w, device=DEV, with_dout=True)
+    out, lse = ga.attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"], window_left=w.window_left,
+                           scale=w.scale)
+    dq, dk, dv = ga.attn_bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], x["ids"], x["pos"],
+                             window_left=w.window_left, scale=w.scale)
+    torch.cuda.synchronize()
+    del out, lse
+    ids, pos = x["ids"].cpu(), x["pos"].cpu()
+    g = w.hq // w.hkv
+    for bi, kvh, r0, nrows in dq_samples:
+        rows = np.arange(r0, r0 + nrows)
+        hs = slice(kvh * g, kvh * g + g)
+        sl = dict(q=x["q"][bi:bi + 1, :, hs].cpu(), k=x["k"][bi:bi + 1, :, kvh:kvh + 1].cpu(),
+                  v=x["v"][bi:bi + 1, :, kvh:kvh + 1].cpu(),
+                  dout=x["dout"][bi:bi + 1, :, hs].cpu())
+        rq, _, _ = A.attn_bwd(sl["q"], sl["k"], sl["v"], sl["dout"], ids[bi:bi + 1],
+                              pos[bi:bi + 1], ids[bi:bi + 1], pos[bi:bi + 1], w.window_left,
+                              w.scale, rows=rows)
+        check_grad(dq[bi, r0:r0 + nrows, hs].cpu(), rq[0, rows], f"dq b{bi} kvh{kvh} r{r0}")
+    for bi, kvh, k0, nkeys in key_samples:
+        keys = np.arange(k0, k0 + nkeys)
+        rows = A.rows_seeing_keys(ids[bi], pos[bi], ids[bi], pos[bi], w.window_left, keys)
+        hs = slice(kvh * g, kvh * g + g)
+        sl = dict(q=x["q"][bi:bi + 1, :, hs].cpu(), k=x["k"][bi:bi + 1, :, kvh:kvh + 1].cpu(),
+                  v=x["v"][bi:bi + 1, :, kvh:kvh + 1].cpu(),
+                  dout=x["dout"][bi:bi + 1, :, hs].cpu())
+        _, rk, rv = A.attn_bwd(sl["q"], sl["k"], sl["v"], sl["dout"], ids[bi:bi + 1],
+                               pos[bi:bi + 1], ids[bi:bi + 1], pos[bi:bi + 1], w.window_left,
+                               w.scale, rows=rows)
+        check_grad(dk[bi, k0:k0 + nkeys, kvh].cpu(), rk[0, keys, 0], f"dk b{bi} kvh{kvh} k{k0}")
+        check_grad(dv[bi, k0:k0 + nkeys, kvh].cpu(), rv[0, keys, 0], f"dv b{bi} kvh{kvh} k{k0}")
+    pad = (ids == 0).to(DEV)
+    assert torch.all(dq[pad] == 0) and torch.all(dk[pad] == 0) and torch.all(dv[pad] == 0)
+    del x, dq, dk, dv
+    torch.cuda.empty_cache()
+
+
+def test_packed_swa_sampled(ga):
+    _sampled(ga, "packed_swa",
+             dq_samples=[(0, 0, 0, 128), (1, 7, 4096 + 2000, 200), (0, 3, 3 * 4096 + 2900, 200)],
+             key_samples=[(0, 2, 1900, 128), (1, 5, 4096 + 3000, 72), (0, 0, 0, 64)])
+
+
+def test_full_swa_64k_sampled(ga):
+    """The 64k packed GQA-SWA workload in the benchmark's launch configuration."""
+    _sampled(ga, "full_swa_64k",
+             dq_samples=[(0, 0, 9000, 64), (1, 7, 16384 + 12200, 120)],
+             key_samples=[(0, 3, 12160, 128), (1, 6, 2 * 16384 + 12220, 68)])

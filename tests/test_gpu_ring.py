@@ -1,0 +1,66 @@
+"""Ring emulation on one GPU (reorder -> per-step attn_fwd + merge -> inverse
+reorder) must equal full attention and the CPU oracle's ring."""
+import numpy as np
+import pytest
+import torch
+
+import workload
+from oracle import attention as A
+from oracle import reorder as RO
+from oracle import ring as RG
+from tests.parity import check_lse, check_out
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def ring():
+    from long_context_attention_attn_gb300 import ring as mod
+    return mod
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,window,slots,R,strategy,stripe", [
+    (1, 2048, 4, 2, 128, -1, None, 4, RO.DUAL_CHUNK, 1),
+    (2, 1536, 4, 1, 64, 200, 2, 3, RO.DUAL_CHUNK, 1),
+    (1, 4096, 2, 1, 128, -1, 4, 4, RO.STRIPED, 128),
+    (1, 1024, 2, 2, 128, 100, None, 2, RO.STRIPED, 1),
+])
+def test_ring_matches_oracle(ring, b, s, hq, hkv, d, window, slots, R, strategy, stripe):
+    q, k, v = workload.qkv(b, s, hq, hkv, d, seed=R + s)
+    ids, pos = workload.segments(b, s, slots)
+    out, lse = ring.ring_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), ids.to(DEV), pos.to(DEV), R,
+                                  window_left=window, scale=d ** -0.5, strategy=strategy,
+                                  stripe_size=stripe)
+    torch.cuda.synchronize()
+    ro, rl = RG.ring_attention(q, k, v, ids, pos, window, d ** -0.5, R, strategy, stripe)
+    check_out(out.cpu(), ro)
+    check_lse(lse.cpu(), rl)
+    fo, fl = A.attn_fwd(q, k, v, ids, pos, ids, pos, window, d ** -0.5)
+    np.testing.assert_allclose(ro, fo, atol=1e-12)
+
+
+def test_ring_workload_equals_full_attention(ring):
+    """The 32k ring workload: R = 4 dual-chunk shards, compared with the
+    single-call forward on every element and with the oracle on samples."""
+    import long_context_attention_attn_gb300 as ga
+    w = workload.WORKLOADS["ring_cp4"]
+    x = workload.make(w, device=DEV, with_dout=False)
+    out, lse = ring.ring_attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"], w.cp_size,
+                                  window_left=w.window_left, scale=w.scale)
+    full_o, full_l = ga.attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"],
+                                 window_left=w.window_left, scale=w.scale)
+    torch.cuda.synchronize()
+    # ring vs one-shot GPU forward: both within bf16 rounding of each other
+    diff = (out.float() - full_o.float()).abs().max().item()
+    assert diff <= 2e-2, diff
+    assert (lse - full_l).abs().max().item() <= 1e-3
+    ids, pos = x["ids"].cpu(), x["pos"].cpu()
+    for h, r0, nr in ((0, 0, 128), (37, 20000, 64), (63, 32768 - 100, 100)):
+        kvh = h // (w.hq // w.hkv)
+        rows = np.arange(r0, r0 + nr)
+        ro, rl = A.attn_fwd(x["q"][:, :, h:h + 1].cpu(), x["k"][:, :, kvh:kvh + 1].cpu(),
+                            x["v"][:, :, kvh:kvh + 1].cpu(), ids, pos, ids, pos, w.window_left,
+                            w.scale, rows=rows)
+        check_out(out[0, r0:r0 + nr, h].cpu(), ro[0, rows, 0])
+        check_lse(lse[0, h, r0:r0 + nr].cpu(), rl[0, 0, rows])
