@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name (the headline number is full_swa_64k; smaller ones "
+                         "serve profiling)")
     return ap.parse_args()
 
 
@@ -164,7 +167,8 @@ def oracle_sample(w, budget_s=12.0, max_blocks=48):
         rows = np.arange(r0 + 64 * blocks, r0 + 64 * (blocks + 1))
         A.attn_fwd(q, k, v, ids, pos, ids, pos, w.window_left, w.scale, rows=rows)
         A.attn_bwd(q, k, v, dout, ids, pos, ids, pos, w.window_left, w.scale, rows=rows)
-        pairs = sum(min(int(p), w.window_left) + 1 for p in pos[0, rows])
+        W = w.window_left
+        pairs = sum((int(p) if W < 0 else min(int(p), W)) + 1 for p in pos[0, rows])
         flops += pairs * g * 14 * w.d
         blocks += 1
         if time.perf_counter() - t0 > budget_s:
@@ -178,7 +182,7 @@ def oracle_sample(w, budget_s=12.0, max_blocks=48):
 
 def run_reference(args, rank):
     import workload
-    w = workload.WORKLOADS[WORKLOAD]
+    w = workload.WORKLOADS[args.workload]
     if rank != 0:
         return
     vals = []
@@ -220,7 +224,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    w = workload.WORKLOADS[WORKLOAD]
+    w = workload.WORKLOADS[args.workload]
     pairs = valid_pairs(w)
     fwd_flop = 4 * w.d * w.hq * pairs
     bwd_flop = 10 * w.d * w.hq * pairs
