@@ -179,6 +179,28 @@ GB300ATTN_API int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int
  * stopped early and its outputs are undefined). */
 GB300ATTN_API int attn_read_device_status(const void* workspace, attn_stream_t stream);
 
+/* attn_fwd without a caller-provided workspace, for callers that cannot
+ * allocate device memory (for example code inside a host framework that owns
+ * all device memory through its own pool, or a latency-critical path that
+ * cannot afford an allocation's implicit synchronisation).  The pages have no
+ * counterpart to this entry point.
+ *  - Same parameters and results as attn_fwd; p->workspace and
+ *    p->workspace_bytes are ignored.  The caller still provides q, k, v, the
+ *    descriptors, out and lse.
+ *  - The scratch (tile plan + status word) is a fixed 4 MiB array in the
+ *    library's device memory, held on every GPU that loads the library until
+ *    the process exits.  Problems whose attn_fwd_workspace_bytes() exceeds
+ *    4 MiB are rejected with ATTN_ERR_UNSUPPORTED (about b * ceil(s_q/128) *
+ *    ceil(s_kv/128) <= 3.5M tiles, e.g. b=2 with s=160k).
+ *  - No cudaMalloc / cudaFree or other allocating call is made.  The first
+ *    call on a device looks up the array's device address (cudaGetSymbolAddress
+ *    with that device current); make that first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents (the
+ *    status word is cleared at the start of every call): calls that overlap on
+ *    the GPU (different streams, or different host threads) race on it.
+ */
+GB300ATTN_API int attn_fwd_noalloc(const attn_fwd_params* p, attn_stream_t stream);
+
 /* Static description of a status code. */
 GB300ATTN_API const char* attn_status_string(int status);
 

@@ -24,7 +24,7 @@ TILE = 128
 EXPORTS = (
     "attn_fwd_workspace_bytes", "attn_bwd_workspace_bytes", "attn_fwd", "attn_bwd",
     "attn_merge_partial", "reorder_causal_lb", "inverse_reorder_causal_lb", "attn_tile_plan",
-    "attn_read_device_status", "attn_status_string",
+    "attn_read_device_status", "attn_status_string", "attn_fwd_noalloc",
 )
 
 
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         h.attn_tile_plan.restype = c_int
         h.attn_read_device_status.argtypes = [vp, vp]
         h.attn_read_device_status.restype = c_int
+        h.attn_fwd_noalloc.argtypes = [ctypes.POINTER(FwdParams), vp]
+        h.attn_fwd_noalloc.restype = c_int
         h.attn_status_string.argtypes = [c_int]
         h.attn_status_string.restype = ctypes.c_char_p
         _lib_handle = h
