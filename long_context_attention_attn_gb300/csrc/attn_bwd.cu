@@ -33,7 +33,9 @@ namespace {
 constexpr int BM = 128;  // query rows per step
 constexpr int BN = 128;  // key rows per CTA
 constexpr int NQ = 2;    // Q tile stages
-constexpr int NV = 2;    // per-step vector ring entries
+constexpr int NV = 4;    // per-step vector ring entries
+// vector entry: lse2, D, ids, pos (128 each), then kind, query tile, head
+constexpr int kVecEntry = 4 * 128 + 32;
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -49,6 +51,7 @@ struct BwdArgs {
   void* dv;
   const uint8_t* cls;
   const int2* krange;
+  const int* kweight;
   const int* order;
   int* status;
   int b, s_q, s_kv, hq, hkv, g, nq, nk;
@@ -67,8 +70,8 @@ struct BLayout {
   static constexpr int q_off = v_off + kTile;          // NQ stages
   static constexpr int do_off = q_off + NQ * kTile;    // 1 stage
   static constexpr int ds_off = do_off + kTile;        // dS: 128 q x 128 keys bf16, MN-major
-  static constexpr int vec_off = ds_off + 2 * kChunk;  // NV x {lse2, D, ids, pos}[128]
-  static constexpr int bar_off = vec_off + NV * 4 * BM * 4;
+  static constexpr int vec_off = ds_off + 2 * kChunk;  // NV x kVecEntry words
+  static constexpr int bar_off = vec_off + NV * kVecEntry * 4;
   static constexpr int bytes = bar_off + 256;
   static constexpr int alloc = (bytes + 1024) > 150 * 1024 ? (bytes + 1024) : 150 * 1024;
 };
@@ -118,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   BBars* bars = reinterpret_cast<BBars*>(smem + L::bar_off);
-  float* vec = reinterpret_cast<float*>(smem + L::vec_off);  // [NV][4][BM]
+  float* vec = reinterpret_cast<float*>(smem + L::vec_off);  // [NV][kVecEntry]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bi = e / a.nk;
   const int kt = e % a.nk;
   const int2 rng = a.krange[e];
+  const int nsteps_total = a.kweight[e] * a.g;  // (non-SKIP query tile, head) steps
   StepIter it0;
   it0.i = rng.x;
   it0.hh = 0;
@@ -176,6 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx ctx{&bars->abort_flag, a.status};
   constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
+  if (warp < 4) {
+  regs_dec<kRegsControl>();
   if (warp == 0) {
     // ======================================================== producer
     int last_q[NQ] = {-1, -1};
@@ -213,28 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      // per-row vectors: LSE (base 2, +inf for rows without keys), D, ids, pos
-      {
-        const int en = t % NV, use = t / NV;
-        if (lane == 0) ok = mbar_wait(&bars->vec_empty[en], (use & 1) ^ 1, ctx);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        float* v = vec + en * 4 * BM;
-        int* vi = reinterpret_cast<int*>(v);
-        const int64_t lbase = ((int64_t)bi * a.hq + h) * a.s_q;
-        const int64_t ibase = (int64_t)bi * a.s_q;
-        for (int r = lane; r < BM; r += 32) {
-          const int gq = qt * BM + r;
-          const bool in = gq < a.s_q;
-          const float l = in ? a.lse[lbase + gq] : -INFINITY;
-          v[r] = (l == -INFINITY) ? INFINITY : l * kLog2e;
-          v[BM + r] = in ? a.Dv[lbase + gq] : 0.f;
-          vi[2 * BM + r] = in ? a.q_ids[ibase + gq] : 0;
-          vi[3 * BM + r] = in ? a.q_pos[ibase + gq] : 0;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->vec_full[en]);
-      }
       // dO tile
       if (lane == 0) {
         ok = mbar_wait(&bars->do_empty, (t & 1) ^ 1, ctx);
@@ -266,8 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t do_base = smem_u32(smem + L::do_off);
       const uint32_t ds_base = smem_u32(smem + L::ds_off);
       bool ok = mbar_wait(&bars->kv_full, 0, ctx);
-      int t = 0;
-      for (StepIter it = it0; it.valid() && ok; it.next(), ++t) {
+      for (int t = 0; t < nsteps_total && ok; ++t) {
         const int qs = t % NQ;
         ok = mbar_wait(&bars->q_full[qs], (t / NQ) & 1, ctx);
         if (ok && t > 0) ok = mbar_wait(&bars->dq_empty, (t - 1) & 1, ctx);
@@ -329,7 +312,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, a.status);
     }
-  } else if (warp >= 4) {
+  } else if (warp == 2) {
+    // ======================================================== vector loader
+    // Per step: LSE (base 2; +inf for rows without keys, so P = 0), D, query
+    // ids / pos, and the step's class / query tile / head, into the ring read
+    // by the element-wise warpgroups (off the TMA producer's path).
+    int t = 0;
+    bool ok = true;
+    for (StepIter it = it0; it.valid() && ok; it.next(), ++t) {
+      const int h = kvh * a.g + it.hh;
+      const int qt = it.i;
+      const int en = t % NV, use = t / NV;
+      const int64_t lbase = ((int64_t)bi * a.hq + h) * a.s_q;
+      const int64_t ibase = (int64_t)bi * a.s_q;
+      float vl[BM / 32], vd[BM / 32];
+      int vid[BM / 32], vps[BM / 32];
+#pragma unroll
+      for (int u = 0; u < BM / 32; ++u) {
+        const int gq = qt * BM + u * 32 + lane;
+        const bool in = gq < a.s_q;
+        vl[u] = in ? a.lse[lbase + gq] : -INFINITY;
+        vd[u] = in ? a.Dv[lbase + gq] : 0.f;
+        vid[u] = in ? a.q_ids[ibase + gq] : 0;
+        vps[u] = in ? a.q_pos[ibase + gq] : 0;
+      }
+      const int kind = it.kind();
+      if (lane == 0) ok = mbar_wait(&bars->vec_empty[en], (use & 1) ^ 1, ctx);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      float* v = vec + en * kVecEntry;
+      int* vi = reinterpret_cast<int*>(v);
+#pragma unroll
+      for (int u = 0; u < BM / 32; ++u) {
+        const int r = u * 32 + lane;
+        v[r] = (vl[u] == -INFINITY) ? INFINITY : vl[u] * kLog2e;
+        v[BM + r] = vd[u];
+        vi[2 * BM + r] = vid[u];
+        vi[3 * BM + r] = vps[u];
+      }
+      if (lane == 0) {
+        vi[4 * BM] = kind;
+        vi[4 * BM + 1] = qt;
+        vi[4 * BM + 2] = h;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->vec_full[en]);
+    }
+  }
+  } else {
+  regs_inc<kRegsCompute>();
+  {
     // ======================================================== element-wise
     const int w = (warp - 4) / 4;  // query columns [64w, 64w + 64)
     const int wq = warp % 4;
@@ -343,20 +375,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ds_smem = smem + L::ds_off + w * L::kChunk + kr * 128;
     int t = 0;
     bool ok = true;
-    for (StepIter it = it0; it.valid(); it.next(), ++t) {
-      const int h = kvh * a.g + it.hh;
-      const int qt = it.i;
-      const bool partial = it.kind() == kPartial;
+    for (; t < nsteps_total; ++t) {
       const int en = t % NV;
       ok = mbar_wait(&bars->vec_full[en], (t / NV) & 1, ctx);
       ok = mbar_wait(&bars->s_full, t & 1, ctx) && ok;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = vec + en * 4 * BM + 64 * w;
-      const float* dvec = vec + en * 4 * BM + BM + 64 * w;
-      const int* qid = reinterpret_cast<const int*>(vec + en * 4 * BM + 2 * BM) + 64 * w;
-      const int* qpos = reinterpret_cast<const int*>(vec + en * 4 * BM + 3 * BM) + 64 * w;
+      const float* ventry = vec + en * kVecEntry;
+      const int* vmeta = reinterpret_cast<const int*>(ventry) + 4 * BM;
+      const bool partial = vmeta[0] == kPartial;
+      const int qt = vmeta[1];
+      const int h = vmeta[2];
+      const float* lse2 = ventry + 64 * w;
+      const float* dvec = ventry + BM + 64 * w;
+      const int* qid = reinterpret_cast<const int*>(ventry + 2 * BM) + 64 * w;
+      const int* qpos = reinterpret_cast<const int*>(ventry + 3 * BM) + 64 * w;
       uint32_t r[64];
       tmem_ld32(tmem + lane_off + kColS + 64 * w, &r[0]);
       tmem_ld32(tmem + lane_off + kColS + 64 * w + 32, &r[32]);
@@ -428,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
       const int gq = qt * BM + kr;
-      const int* qid_all = reinterpret_cast<const int*>(vec + en * 4 * BM + 2 * BM);
+      const int* qid_all = reinterpret_cast<const int*>(ventry + 2 * BM);
       if (gq < a.s_q && qid_all[kr] != 0) {
         float4* dst = reinterpret_cast<float4*>(
             a.dq_acc + (((int64_t)bi * a.s_q + gq) * a.hq + h) * D + w * kHalf);
@@ -477,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -500,6 +535,7 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
   a.dv = p.dv;
   a.cls = Lc.plan.classes;
   a.krange = Lc.plan.kv_range;
+  a.kweight = Lc.plan.kv_weight;
   a.order = Lc.plan.kv_order;
   a.status = Lc.plan.status;
   a.b = (int)f.b;
@@ -517,16 +553,28 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
   if (units == 0) return cudaSuccess;
   if (f.d == 128) {
     const int smem = BLayout<128>::alloc;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    static int configured_for = -1;  // device whose attribute is set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+      cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<128>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      configured_for = dev;
+    }
     attn_bwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v,
                                                                   Lc.tm_do, a);
   } else {
     const int smem = BLayout<64>::alloc;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<64>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    static int configured_for = -1;  // device whose attribute is set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+      cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<64>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      configured_for = dev;
+    }
     attn_bwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v,
                                                                  Lc.tm_do, a);
   }

@@ -37,6 +37,8 @@ constexpr int BN = 128;
 constexpr int NST = 4;  // K/V shared-memory slots (K and V tiles alternate)
 constexpr int NID = 4;  // ids/pos ring entries
 constexpr int kThreads = 384;
+// ids/pos ring entry: 128 ids, 128 pos, then the tile's class (PARTIAL/FULL)
+constexpr int kIdEntry = 2 * BN + 32;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -49,6 +51,7 @@ struct FwdArgs {
   float* lse;
   const uint8_t* cls;
   const int2* qrange;
+  const int* qweight;
   const int* order;
   int* status;
   int b, s_q, s_kv, hq, hkv, g, npairs, nq, nk;
@@ -64,8 +67,8 @@ struct Layout {
   static constexpr int kTileBytes = BM * D * 2;       // a Q, K or V tile
   static constexpr int q_off = 0;                     // 2 Q tiles
   static constexpr int kv_off = q_off + 2 * kTileBytes;
-  static constexpr int id_off = kv_off + NST * kTileBytes;  // NID x (128 ids + 128 pos)
-  static constexpr int bar_off = id_off + NID * 2 * BN * 4;
+  static constexpr int id_off = kv_off + NST * kTileBytes;  // NID x kIdEntry ints
+  static constexpr int bar_off = id_off + NID * kIdEntry * 4;
   static constexpr int bytes = bar_off + 256;
   // + slack for 1024-byte alignment; at least 150 KB so that one CTA (which
   // holds all 512 TMEM columns) is resident per SM.
@@ -81,7 +84,7 @@ struct Bars {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::bar_off);
-  int* s_ids = reinterpret_cast<int*>(smem + L::id_off);  // [NID][2][BN]
+  int* s_ids = reinterpret_cast<int*>(smem + L::id_off);  // [NID][kIdEntry]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -115,13 +118,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h0 = kvh * a.g + 2 * pair;
   const int nslots = (2 * pair + 1 < a.g) ? 2 : 1;
   const int2 rng = a.qrange[e];
+  const int nt = a.qweight[e];  // number of non-SKIP kv tiles of this query tile
   const uint8_t* cls_row = a.cls + (size_t)e * a.nk;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < NST; ++i) {
       mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->kv_empty[i], 4 * nslots);  // one arrival per softmax warp
     }
     for (int i = 0; i < NID; ++i) {
       mbar_init(&bars->id_full[i], 1);
@@ -132,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[i], 128);
       mbar_init(&bars->o_done[i], 1);
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain[0], 1);
+    mbar_init(&bars->drain[1], 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -146,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtx ctx{&bars->abort_flag, a.status};
 
+  if (warp < 4) {
+  regs_dec<kRegsControl>();
   if (warp == 0) {
     // ======================================================== TMA producer
     if (lane == 0) {
@@ -181,23 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
-      // ids / pos of the key tile (for the element mask)
-      {
-        const int en = n % NID, use = n / NID;
-        if (lane == 0) ok = mbar_wait(&bars->id_empty[en], (use & 1) ^ 1, ctx);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        int* dst = s_ids + en * 2 * BN;
-        const int64_t base = (int64_t)bi * a.s_kv;
-        for (int t = lane; t < BN; t += 32) {
-          const int tok = j * BN + t;
-          const bool in = tok < a.s_kv;
-          dst[t] = in ? a.kv_ids[base + tok] : 0;
-          dst[BN + t] = in ? a.kv_pos[base + tok] : 0;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->id_full[en]);
-      }
       // V tile
       {
         const int ld = 2 * n + 1, slot = ld % NST, use = ld / NST;
@@ -223,63 +213,90 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < NST; ++i)
         if (last_use[i] >= 0) mbar_wait_drain(&bars->kv_full[i], last_use[i] & 1, a.status);
     }
-  } else if (warp == 1) {
-    // ======================================================== MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 3) {
+    // ======================================================== MMA issuers
+    // One issuing thread per head slot (warp 1: slot 0, warp 3: slot 1), each a
+    // plain in-order loop S(n) -> [softmax] -> PV(n), so a group that blocks
+    // while the tensor core drains its queue never delays the other slot.
+    const int sl = warp == 1 ? 0 : 1;
+    if (lane == 0 && sl < nslots) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
+      // base descriptors: K-major Q / K tiles, MN-major V tiles (128B swizzle)
+      const uint32_t da = sdesc_lo(smem_u32(smem + L::q_off + sl * L::kTileBytes), 16);
+      const uint32_t kv_lo_k = sdesc_lo(smem_u32(smem + L::kv_off), 16);
+      const uint32_t kv_lo_v = sdesc_lo(smem_u32(smem + L::kv_off), L::kChunk);
+      const uint32_t d_s = tmem + sl * BN;
+      const uint32_t d_o = tmem + 2 * BN + sl * D;
       bool ok = mbar_wait(&bars->q_full, 0, ctx);
-      const uint32_t q_base = smem_u32(smem + L::q_off);
-      const uint32_t kv_base = smem_u32(smem + L::kv_off);
-      int n = 0;
-      for (int j = rng.x; j <= rng.y && ok; ++j) {
-        if (cls_row[j] == kSkip) continue;
-        // S_h = Q_h K^T
+      for (int n = 0; n < nt && ok; ++n) {
+        // S_sl(n) = Q_sl K(n)^T: needs K(n), and PV_sl(n-1) done (P_sl lives in S_sl)
         const int ldk = 2 * n, slot_k = ldk % NST;
         ok = mbar_wait(&bars->kv_full[slot_k], (ldk / NST) & 1, ctx);
+        if (ok && n > 0) ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
         if (!ok) break;
-        for (int sl = 0; sl < nslots && ok; ++sl) {
-          if (n > 0) ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t qa = q_base + sl * L::kTileBytes;
-          const uint32_t kb = kv_base + slot_k * L::kTileBytes;
+        tc_fence_after();
+        const uint32_t db = kv_lo_k + ((slot_k * L::kTileBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * L::kChunk + (kk % 4) * 32;
-            mma_ss(tmem + sl * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                   idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars->s_full[sl]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
+          mma_ss_lo(d_s, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        mma_commit(&bars->kv_empty[slot_k]);
-        // O_h += P_h V
+        mma_commit(&bars->s_full[sl]);
+        // O_sl += P_sl(n) V(n): needs V(n) and the softmax of tile n
         const int ldv = 2 * n + 1, slot_v = ldv % NST;
         ok = mbar_wait(&bars->kv_full[slot_v], (ldv / NST) & 1, ctx);
+        if (ok) ok = mbar_wait(&bars->p_full[sl], n & 1, ctx);
         if (!ok) break;
-        for (int sl = 0; sl < nslots && ok; ++sl) {
-          ok = mbar_wait(&bars->p_full[sl], n & 1, ctx);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t vb = kv_base + slot_v * L::kTileBytes;
+        tc_fence_after();
+        const uint32_t dv = kv_lo_v + ((slot_v * L::kTileBytes) >> 4);
+        const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            mma_ts(tmem + 2 * BN + sl * D, tmem + sl * BN + kk * 8,
-                   sdesc_sw128(vb + kk * 16 * 128, L::kChunk, 1024), idesc_o,
-                   (n > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars->o_done[sl]);
-        }
-        if (!ok) break;
-        mma_commit(&bars->kv_empty[slot_v]);
-        ++n;
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_lo(d_o, d_s + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_o, kk > 0 ? 1u : acc0);
+        mma_commit(&bars->o_done[sl]);
       }
       // Drain: all MMAs issued by this thread complete before TMEM is freed.
-      mma_commit(&bars->drain);
-      mbar_wait_drain(&bars->drain, 0, a.status);
+      mma_commit(&bars->drain[sl]);
+      mbar_wait_drain(&bars->drain[sl], 0, a.status);
     }
-  } else if (warp >= 4) {
+  } else if (warp == 2) {
+    // ======================================================== descriptor loader
+    // ids / pos / class of each non-SKIP key tile into the ring read by the
+    // softmax warpgroups (off the TMA producer's path).
+    int n = 0;
+    bool ok = true;
+    for (int j = rng.x; j <= rng.y && ok; ++j) {
+      const uint8_t kind = cls_row[j];
+      if (kind == kSkip) continue;
+      const int en = n % NID, use = n / NID;
+      const int64_t base = (int64_t)bi * a.s_kv;
+      int vid[BN / 32], vpos[BN / 32];
+#pragma unroll
+      for (int u = 0; u < BN / 32; ++u) {
+        const int tok = j * BN + u * 32 + lane;
+        const bool in = tok < a.s_kv;
+        vid[u] = in ? a.kv_ids[base + tok] : 0;
+        vpos[u] = in ? a.kv_pos[base + tok] : 0;
+      }
+      if (lane == 0) ok = mbar_wait(&bars->id_empty[en], (use & 1) ^ 1, ctx);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      int* dst = s_ids + en * kIdEntry;
+#pragma unroll
+      for (int u = 0; u < BN / 32; ++u) {
+        dst[u * 32 + lane] = vid[u];
+        dst[BN + u * 32 + lane] = vpos[u];
+      }
+      if (lane == 0) dst[2 * BN] = kind;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->id_full[en]);
+      ++n;
+    }
+  }
+  } else {
+  regs_inc<kRegsCompute>();
+  {
     // ======================================================== softmax
     const int sl = (warp - 4) / 4;
     const int wq = warp % 4;  // TMEM lane quarter this warp may access
@@ -297,24 +314,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l = 0.f;        // running denominator relative to m
       int n = 0;
       bool ok = true;
-      for (int j = rng.x; j <= rng.y; ++j) {
-        const uint8_t kind = cls_row[j];
-        if (kind == kSkip) continue;
+      for (; n < nt;) {
         const int en = n % NID;
         ok = mbar_wait(&bars->id_full[en], (n / NID) & 1, ctx);
         ok = mbar_wait(&bars->s_full[sl], n & 1, ctx) && ok;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        // S_sl(n) is complete, so this slot is done with K(n) and (its S(n) was
+        // issued after PV_sl(n-1) completed) with V(n-1): release both slots.
+        if (lane == 0) {
+          mbar_arrive(&bars->kv_empty[(2 * n) % NST]);
+          if (n > 0) mbar_arrive(&bars->kv_empty[(2 * n - 1) % NST]);
+        }
         uint32_t sr[BN];
         tmem_ld32(t_s + 0, &sr[0]);
         tmem_ld32(t_s + 32, &sr[32]);
         tmem_ld32(t_s + 64, &sr[64]);
         tmem_ld32(t_s + 96, &sr[96]);
         tmem_wait_ld();
+        const int kind = s_ids[en * kIdEntry + 2 * BN];
         if (kind == kPartial) {
-          const int4* ids4 = reinterpret_cast<const int4*>(s_ids + en * 2 * BN);
-          const int4* pos4 = reinterpret_cast<const int4*>(s_ids + en * 2 * BN + BN);
+          const int4* ids4 = reinterpret_cast<const int4*>(s_ids + en * kIdEntry);
+          const int4* pos4 = reinterpret_cast<const int4*>(s_ids + en * kIdEntry + BN);
 #pragma unroll
           for (int c = 0; c < BN / 4; ++c) {
             const int4 ik = ids4[c];
@@ -441,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- teardown (the producer and MMA threads drained their async work above)
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -460,6 +483,7 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   a.lse = p.lse;
   a.cls = Lc.plan.classes;
   a.qrange = Lc.plan.q_range;
+  a.qweight = Lc.plan.q_weight;
   a.order = Lc.plan.q_order;
   a.status = Lc.plan.status;
   a.b = (int)p.b;
@@ -478,15 +502,27 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   if (units == 0) return cudaSuccess;
   if (p.d == 128) {
     const int smem = Layout<128>::alloc;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    static int configured_for = -1;  // device whose attribute is set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+      cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      configured_for = dev;
+    }
     attn_fwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
   } else {
     const int smem = Layout<64>::alloc;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    static int configured_for = -1;  // device whose attribute is set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+      cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      configured_for = dev;
+    }
     attn_fwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
   }
   return cudaGetLastError();

@@ -371,31 +371,59 @@ cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, co
 
 // ============================================================== backward helpers
 // D_i = sum_d dO_i * O_i per (b, head, row): the row term of dS = P * (dP - D).
-__global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
-                                      const __nv_bfloat16* __restrict__ dout, float* __restrict__ D,
-                                      int64_t b, int64_t s, int64_t h, int64_t d) {
+// Each thread reads 16 bytes (8 bf16) of O and of dO; a row-head of d values
+// is handled by d/8 consecutive lanes (16 for d = 128), reduced by shuffles.
+// The LSE/D layout is [b, h, s] so each row-head writes one float.
+template <int D>
+__global__ void bwd_preprocess_kernel(const uint4* __restrict__ out, const uint4* __restrict__ dout,
+                                      float* __restrict__ Dv, int64_t b, int64_t s, int64_t h) {
+  constexpr int kLanes = D / 8;            // lanes per row-head
+  constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = threadIdx.x & 31;
+  const int sub = lane % kLanes;
   const int64_t nrows = b * s * h;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
-  const int64_t v4 = d / 4;
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows;
-       r += nwarps) {
-    float acc = 0.f;
-    const uint2* po = reinterpret_cast<const uint2*>(out + r * d);
-    const uint2* pd = reinterpret_cast<const uint2*>(dout + r * d);
-    for (int64_t w = lane; w < v4; w += 32) {
-      const uint2 a = po[w], c = pd[w];
-      const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
-      const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
-      const float2 c0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c.x));
-      const float2 c1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c.y));
-      acc += a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
+  const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  for (int64_t r0 = warp0 * kRowsPerWarp; r0 < nrows; r0 += nwarps * kRowsPerWarp * 2) {
+    // two independent row groups per iteration keep more bytes in flight
+    const int64_t ra = r0 + lane / kLanes;
+    const int64_t rb = ra + nwarps * kRowsPerWarp;
+    uint4 oa = make_uint4(0, 0, 0, 0), da = oa, ob = oa, db = oa;
+    if (ra < nrows) {
+      oa = out[ra * kLanes + sub];
+      da = dout[ra * kLanes + sub];
     }
+    if (rb < nrows) {
+      ob = out[rb * kLanes + sub];
+      db = dout[rb * kLanes + sub];
+    }
+    auto dot8 = [](const uint4& x, const uint4& y) {
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+      const uint32_t ys[4] = {y.x, y.y, y.z, y.w};
+      float acc = 0.f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      const int64_t hh = r % h, ti = (r / h) % s, bi = r / (h * s);
-      D[(bi * h + hh) * s + ti] = acc;
+      for (int k = 0; k < 4; ++k) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[k]));
+        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[k]));
+        acc += a.x * c.x + a.y * c.y;
+      }
+      return acc;
+    };
+    float sa = dot8(oa, da), sb = dot8(ob, db);
+#pragma unroll
+    for (int off = kLanes / 2; off > 0; off >>= 1) {
+      sa += __shfl_xor_sync(0xffffffffu, sa, off);
+      sb += __shfl_xor_sync(0xffffffffu, sb, off);
+    }
+    if (sub == 0) {
+      if (ra < nrows) {
+        const int64_t hh = ra % h, ti = (ra / h) % s, bi = ra / (h * s);
+        Dv[(bi * h + hh) * s + ti] = sa;
+      }
+      if (rb < nrows) {
+        const int64_t hh = rb % h, ti = (rb / h) % s, bi = rb / (h * s);
+        Dv[(bi * h + hh) * s + ti] = sb;
+      }
     }
   }
 }
@@ -403,10 +431,15 @@ __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, int64_t b,
                                   int64_t s, int64_t h, int64_t d, cudaStream_t st) {
   const int64_t rows = b * s * h;
-  const unsigned grid = (unsigned)std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
-  bwd_preprocess_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out),
-                                              static_cast<const __nv_bfloat16*>(dout), D, b, s, h,
-                                              d);
+  const int rows_per_cta = 8 * (d == 128 ? 2 : 4);
+  const unsigned grid =
+      (unsigned)std::min<int64_t>((rows + rows_per_cta - 1) / rows_per_cta, (int64_t)sm_count() * 16);
+  if (d == 128)
+    bwd_preprocess_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
+                                                     static_cast<const uint4*>(dout), D, b, s, h);
+  else
+    bwd_preprocess_kernel<64><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
+                                                    static_cast<const uint4*>(dout), D, b, s, h);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared abort flag + global status word: any bounded wait that gives up
 // records ATTN_ERR_TIMEOUT and makes every other wait of the CTA return early.
 struct WaitCtx {
@@ -86,6 +99,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
   }
 }
+
+// Idle-time bound for polling loops (an issuer that probes several barriers
+// with mbar_test): call idle() whenever a pass made no progress and
+// progress() otherwise; idle() returns false once the CTA must stop.
+struct PollGuard {
+  uint64_t t0 = 0;
+  uint32_t spins = 0;
+  __device__ __forceinline__ void progress() { spins = 0; }
+  __device__ __forceinline__ bool idle(const WaitCtx& ctx) {
+    if (spins == 0) t0 = global_timer_ns();
+    if (++spins % 64 != 0) return true;
+    if (*ctx.abort_flag) return false;
+    if (ctx.status && *reinterpret_cast<volatile int*>(ctx.status) != kStatusOk) {
+      *ctx.abort_flag = 1;
+      return false;
+    }
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *ctx.abort_flag = 1;
+      if (ctx.status) atomicMax(ctx.status, kStatusTimeout);
+      return false;
+    }
+    return true;
+  }
+};
 
 // Bounded wait used while tearing down: ignores the abort flag (the async
 // work it waits for completes on its own), records a timeout in `status`.
@@ -164,6 +201,46 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= 1ull << 46;  // descriptor version (tcgen05)
   d |= 2ull << 61;  // swizzle mode: 128B
   return d;
+}
+
+// The start-address field is the low 14 bits (address >> 4); shared memory
+// addresses stay below 2^18, so a byte offset advances a descriptor by a plain
+// 64-bit add of (offset >> 4) without carrying into the other fields.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t byte_offset) {
+  return desc + (uint64_t)(byte_offset >> 4);
+}
+
+// Split form of sdesc_sw128: the high word (stride 1024 B, version, 128B
+// swizzle) is the same for every operand here, so only the low word (start
+// address >> 4 | leading offset >> 4 << 16) is kept in a register.
+constexpr uint32_t kSdescHi = ((1024u >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with split descriptors (low words)
+__device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %5};\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSdescHi)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] with a split B descriptor
+__device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSdescHi)
+      : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T   (cta_group::1, kind::f16)
@@ -264,6 +341,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+
+// Per-warpgroup register budget (all four warps of the warpgroup execute it).
+// The block is launched with 168 registers x 384 threads = 64512; the
+// producer/MMA warpgroup releases down to 80 and the two compute warpgroups
+// grow to 208: 128*80 + 256*208 = 63488 <= 64512.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+constexpr int kRegsControl = 80;
+constexpr int kRegsCompute = 208;
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
 
