@@ -82,6 +82,20 @@ bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [b, s, h, d] accumulator viewed as (d, head, token, batch); box =
+// 32 d (128 bytes, swizzled) x 1 head x 128 tokens, for tiled reduce-adds.
+bool encode_acc_map(CUtensorMap* m, const float* base, int64_t b, int64_t s, int64_t h, int64_t d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)h, (cuuint64_t)s, (cuuint64_t)b};
+  cuuint64_t strides[3] = {(cuuint64_t)(d * 4), (cuuint64_t)(h * d * 4), (cuuint64_t)(s * h * d * 4)};
+  cuuint32_t box[4] = {32, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gb300
 
 extern "C" {
@@ -166,7 +180,8 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   if (!encode_qkv_map(&bl.tm_q, f->q, f->b, f->s_q, f->h_q, f->d) ||
       !encode_qkv_map(&bl.tm_k, f->k, f->b, f->s_kv, f->h_kv, f->d) ||
       !encode_qkv_map(&bl.tm_v, f->v, f->b, f->s_kv, f->h_kv, f->d) ||
-      !encode_qkv_map(&bl.tm_do, p->dout, f->b, f->s_q, f->h_q, f->d))
+      !encode_qkv_map(&bl.tm_do, p->dout, f->b, f->s_q, f->h_q, f->d) ||
+      !encode_acc_map(&bl.tm_dq, bl.dq_acc, f->b, f->s_q, f->h_q, f->d))
     return ATTN_ERR_CUDA;
   const size_t n_dq = (size_t)(f->b * f->s_q * f->h_q * f->d);
   cudaError_t e = cudaMemsetAsync(bl.plan.status, 0, sizeof(int), st);

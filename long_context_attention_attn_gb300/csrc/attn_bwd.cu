@@ -13,14 +13,21 @@
 // dP^T = V dO^T on tcgen05 (keys on TMEM lanes), forms P^T and dS^T in
 // registers (one thread per key row), writes them back to TMEM as bf16 (the A
 // operands of dV += P^T dO and dK += dS^T Q), stages dS in shared memory for
-// dQ = dS K, and adds the dQ tile into an fp32 accumulator in global memory.
+// dQ = dS K, and adds the dQ tile into an fp32 accumulator in global memory
+// with TMA tiled reduce-adds staged through the (then free) dS buffer.
 //
 // Roles (384 threads): warp 0 TMA producer; warp 1 MMA issuer and TMEM owner;
+// warp 2 per-step vector loader; warp 3 dQ reduce issuer;
 // warps 4-7 and 8-11 the two element-wise warpgroups (query columns 0-63 and
 // 64-127 of S^T / dP^T; each also reads back half of the dQ tile).
 // TMEM: dV [0,D)  dK [128,128+D)  S^T [256,384)  dP^T [384,512);
-// P^T / dS^T overwrite the first 64 columns of S^T / dP^T, and the dQ tile
-// lands in the last 64 columns of S^T (d 0-63) and dP^T (d 64-127).
+// P^T (bf16) overwrites S^T columns [256,320) and dS^T columns [320,384); the
+// dQ tile (one N = d MMA group) lands in the dP^T columns [384, 384+D).  So the
+// next step's S^T only waits for dK, and only its dP^T waits for the dQ tile
+// to be read out.
+// dQ leaves through shared memory: one half through the dS buffer, the other
+// through the just-finished Q stage; warp 3 issues the TMA reduce-adds and
+// releases both buffers when the TMA has read them.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -85,7 +92,8 @@ struct BBars {
   uint64_t vec_full[NV];
   uint64_t vec_empty[NV];
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, dk_done;
-  uint64_t s_read, dp_read;  // both element-wise halves have read S^T / dP^T
+  uint64_t s_read;  // both element-wise halves have read S^T
+  uint64_t stg_ready, stg_free;  // dQ staging boxes written / read by the TMA
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -115,7 +123,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
   using L = BLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -164,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dq_empty, 256);
     mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->s_read, 256);
-    mbar_init(&bars->dp_read, 256);
+    mbar_init(&bars->stg_ready, 256);
+    mbar_init(&bars->stg_free, 1);  // arrived by the reduce issuer once the TMA read the staging
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -179,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtx ctx{&bars->abort_flag, a.status};
   constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
+  constexpr uint32_t kColP = 256, kColDS = 320, kColDQ = 384;
 
   if (warp < 4) {
   regs_dec<kRegsControl>();
@@ -243,74 +253,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);    // dV, dK (A in TMEM)
-      constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);     // dQ halves
-      const uint32_t k_base = smem_u32(smem + L::k_off);
-      const uint32_t v_base = smem_u32(smem + L::v_off);
-      const uint32_t q_base = smem_u32(smem + L::q_off);
-      const uint32_t do_base = smem_u32(smem + L::do_off);
-      const uint32_t ds_base = smem_u32(smem + L::ds_off);
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);      // dQ
+      // split descriptors (low words): K-major for S^T / dP^T, MN-major otherwise
+      const uint32_t k_km = sdesc_lo(smem_u32(smem + L::k_off), 16);
+      const uint32_t v_km = sdesc_lo(smem_u32(smem + L::v_off), 16);
+      const uint32_t q_km = sdesc_lo(smem_u32(smem + L::q_off), 16);
+      const uint32_t do_km = sdesc_lo(smem_u32(smem + L::do_off), 16);
+      const uint32_t k_mn = sdesc_lo(smem_u32(smem + L::k_off), L::kChunk);
+      const uint32_t q_mn = sdesc_lo(smem_u32(smem + L::q_off), L::kChunk);
+      const uint32_t do_mn = sdesc_lo(smem_u32(smem + L::do_off), L::kChunk);
+      const uint32_t ds_mn = sdesc_lo(smem_u32(smem + L::ds_off), L::kChunk);
+      const uint32_t t_s = tmem + kColS, t_dp = tmem + kColDP, t_p = tmem + kColP;
+      const uint32_t t_ds = tmem + kColDS, t_dq = tmem + kColDQ;
       bool ok = mbar_wait(&bars->kv_full, 0, ctx);
       for (int t = 0; t < nsteps_total && ok; ++t) {
         const int qs = t % NQ;
+        const uint32_t qstage = (qs * L::kTile) >> 4;
         ok = mbar_wait(&bars->q_full[qs], (t / NQ) & 1, ctx);
-        if (ok && t > 0) ok = mbar_wait(&bars->dq_empty, (t - 1) & 1, ctx);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t qb = q_base + qs * L::kTile;
-        // S^T = K Q^T  (M = keys, N = queries, K = d)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::kChunk + (kk % 4) * 32;
-          mma_ss(tmem + kColS, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
-                 id_kk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->s_full);
-        // dP^T = V dO^T
-        ok = mbar_wait(&bars->do_full, t & 1, ctx);
+        // S^T overwrites P^T / dS^T of the previous step: dV and dK must be done
         if (ok && t > 0) ok = mbar_wait(&bars->dk_done, (t - 1) & 1, ctx);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::kChunk + (kk % 4) * 32;
-          mma_ss(tmem + kColDP, sdesc_sw128(v_base + off, 16, 1024),
-                 sdesc_sw128(do_base + off, 16, 1024), id_kk, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
+          mma_ss_lo(t_s, k_km + off, q_km + qstage + off, id_kk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full);
+        // dP^T = V dO^T
+        ok = mbar_wait(&bars->do_full, t & 1, ctx);
+        // dP^T overwrites the previous dQ tile: it must have been read out
+        if (ok && t > 0) ok = mbar_wait(&bars->dq_empty, (t - 1) & 1, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
+          mma_ss_lo(t_dp, v_km + off, do_km + off, id_kk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dp_full);
         // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major)
         ok = mbar_wait(&bars->p_full, t & 1, ctx);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tmem + kColDV, tmem + kColS + kk * 8,
-                 sdesc_sw128(do_base + kk * 2048, L::kChunk, 1024), id_acc,
-                 (t > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_lo(tmem + kColDV, t_p + kk * 8, do_mn + ((kk * 2048) >> 4), id_acc,
+                    kk > 0 ? 1u : acc0);
         mma_commit(&bars->do_empty);
-        // dQ = dS K  (A = dS in smem MN-major, B = K MN-major), 64 d columns per MMA
+        // dQ = dS K  (A = dS in smem MN-major, B = K MN-major), N = d
         ok = mbar_wait(&bars->ds_full, t & 1, ctx);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) {
-          const uint32_t dst = (c == 0) ? (tmem + kColS + 64) : (tmem + kColDP + 64);
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(dst, sdesc_sw128(ds_base + kk * 2048, L::kChunk, 1024),
-                   sdesc_sw128(k_base + c * L::kChunk + kk * 2048, L::kChunk, 1024), id_dq,
-                   kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss_lo(t_dq, ds_mn + ((kk * 2048) >> 4), k_mn + ((kk * 2048) >> 4), id_dq,
+                    kk > 0 ? 1u : 0u);
         mma_commit(&bars->dq_full);
         // dK += dS^T Q  (A = dS^T in TMEM, B = Q MN-major)
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tmem + kColDK, tmem + kColDP + kk * 8, sdesc_sw128(qb + kk * 2048, L::kChunk, 1024),
-                 id_acc, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_lo(tmem + kColDK, t_ds + kk * 8, q_mn + qstage + ((kk * 2048) >> 4), id_acc,
+                    kk > 0 ? 1u : acc0);
         mma_commit(&bars->dk_done);
-        mma_commit(&bars->q_empty[qs]);
       }
       mma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, a.status);
+    }
+  } else if (warp == 3) {
+    // ======================================================== dQ reduce issuer
+    if (lane == 0) {
+      int t = 0;
+      bool ok = true;
+      for (StepIter it = it0; it.valid() && ok; it.next(), ++t) {
+        const int h = kvh * a.g + it.hh;
+        const int qt = it.i;
+        ok = mbar_wait(&bars->stg_ready, t & 1, ctx);
+        if (!ok) break;
+        constexpr int kHalfR = D / 2, kRoundsR = kHalfR / 32;
+        const uint32_t s0 = smem_u32(smem + L::ds_off);
+        const uint32_t s1 = smem_u32(smem + L::q_off + (t % NQ) * L::kTile);
+#pragma unroll
+        for (int k = 0; k < kRoundsR; ++k) {
+          tma_reduce_add_4d(&tm_dq, s0 + k * L::kChunk, 32 * k, h, qt * BM, bi);
+          tma_reduce_add_4d(&tm_dq, s1 + k * L::kChunk, kHalfR + 32 * k, h, qt * BM, bi);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&bars->stg_free);           // dS buffer reusable
+        mbar_arrive(&bars->q_empty[t % NQ]);    // Q stage reusable
+      }
+      bulk_wait_group0();  // every dQ reduce-add has landed before the CTA exits
     }
   } else if (warp == 2) {
     // ======================================================== vector loader
@@ -373,6 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pk = key_in ? a.kv_pos[(int64_t)bi * a.s_kv + key] : 0;
     const float sl2 = a.scale_log2;
     uint8_t* ds_smem = smem + L::ds_off + w * L::kChunk + kr * 128;
+    constexpr int kHalf = D / 2;         // dQ columns read back by this half
+    constexpr int kRounds = kHalf / 32;  // 32-column staging boxes per half
     int t = 0;
     bool ok = true;
     for (; t < nsteps_total; ++t) {
@@ -395,15 +431,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_off + kColS + 64 * w, &r[0]);
       tmem_ld32(tmem + lane_off + kColS + 64 * w + 32, &r[32]);
       tmem_wait_ld();
+      // per-column vectors are read from shared memory 16 bytes at a time
+      const float4* lse4 = reinterpret_cast<const float4*>(lse2);
       float p[64];
 #pragma unroll
-      for (int u = 0; u < 64; ++u) p[u] = ex2(fmaf(__uint_as_float(r[u]), sl2, -lse2[u]));
-      if (partial) {
+      for (int c = 0; c < 16; ++c) {
+        const float4 l = lse4[c];
+        const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-        for (int u = 0; u < 64; ++u) {
-          bool vis = (qid[u] == ik) && (ik != 0) && (pk <= qpos[u]);
-          if (a.window >= 0) vis = vis && (qpos[u] - pk <= a.window);
-          if (!vis) p[u] = 0.f;
+        for (int u = 0; u < 4; ++u) p[4 * c + u] = ex2(fmaf(__uint_as_float(r[4 * c + u]), sl2, -lv[u]));
+      }
+      if (partial) {
+        const int4* id4 = reinterpret_cast<const int4*>(qid);
+        const int4* ps4 = reinterpret_cast<const int4*>(qpos);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int4 i4 = id4[c];
+          const int4 q4 = ps4[c];
+          const int ia[4] = {i4.x, i4.y, i4.z, i4.w};
+          const int qa[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            bool vis = (ia[u] == ik) && (ik != 0) && (pk <= qa[u]);
+            if (a.window >= 0) vis = vis && (qa[u] - pk <= a.window);
+            if (!vis) p[4 * c + u] = 0.f;
+          }
         }
       }
       uint32_t pk2[32];
@@ -414,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(&bars->s_read, t & 1, ctx);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tmem_st32(tmem + lane_off + kColS + 32 * w, pk2);
+      tmem_st32(tmem + lane_off + kColP + 32 * w, pk2);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
@@ -426,16 +478,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_off + kColDP + 64 * w, &r[0]);
       tmem_ld32(tmem + lane_off + kColDP + 64 * w + 32, &r[32]);
       tmem_wait_ld();
+      const float4* d4 = reinterpret_cast<const float4*>(dvec);
 #pragma unroll
-      for (int u = 0; u < 32; ++u)
-        pk2[u] = pack_bf16(p[2 * u] * (__uint_as_float(r[2 * u]) - dvec[2 * u]),
-                           p[2 * u + 1] * (__uint_as_float(r[2 * u + 1]) - dvec[2 * u + 1]));
-      // both halves have read dP^T before dS^T overwrites it
-      mbar_arrive(&bars->dp_read);
-      ok = mbar_wait(&bars->dp_read, t & 1, ctx);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tmem_st32(tmem + lane_off + kColDP + 32 * w, pk2);
+      for (int c = 0; c < 16; ++c) {
+        const float4 dv4 = d4[c];
+        pk2[2 * c] = pack_bf16(p[4 * c] * (__uint_as_float(r[4 * c]) - dv4.x),
+                               p[4 * c + 1] * (__uint_as_float(r[4 * c + 1]) - dv4.y));
+        pk2[2 * c + 1] = pack_bf16(p[4 * c + 2] * (__uint_as_float(r[4 * c + 2]) - dv4.z),
+                                   p[4 * c + 3] * (__uint_as_float(r[4 * c + 3]) - dv4.w));
+      }
+      tmem_st32(tmem + lane_off + kColDS + 32 * w, pk2);
+      // The dS buffer doubles as the dQ staging area of the previous step: wait
+      // until the TMA has read it.
+      if (t > 0) {
+        ok = mbar_wait(&bars->stg_free, (t - 1) & 1, ctx);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
       // dS (queries x keys) in shared memory, MN-major 128B-swizzled: key row kr
       // holds this half's 64 query values.
 #pragma unroll
@@ -452,27 +511,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      constexpr int kHalf = D / 2;
       uint32_t q[kHalf];
-      const uint32_t src = (D == 128) ? (tmem + lane_off + (w == 0 ? kColS : kColDP) + 64)
-                                      : (tmem + lane_off + kColS + 64 + 32 * w);
+      const uint32_t src = tmem + lane_off + kColDQ + kHalf * w;
 #pragma unroll
       for (int c = 0; c < kHalf; c += 32) tmem_ld32(src + c, &q[c]);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
-      const int gq = qt * BM + kr;
-      const int* qid_all = reinterpret_cast<const int*>(ventry + 2 * BM);
-      if (gq < a.s_q && qid_all[kr] != 0) {
-        float4* dst = reinterpret_cast<float4*>(
-            a.dq_acc + (((int64_t)bi * a.s_q + gq) * a.hq + h) * D + w * kHalf);
+      // dQ (x scale) into the fp32 accumulator.  Half 0 stages its columns in
+      // the dS buffer (free: the dQ MMA has read it), half 1 in the Q stage of
+      // this step (free once dK, its last reader, is done), as 32-column boxes
+      // of 128 rows x 128 B (128B-swizzled); warp 3 issues the reduce-adds.
+      if (w == 1) {
+        ok = mbar_wait(&bars->dk_done, t & 1, ctx);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      {
+        uint8_t* stage = (w == 0) ? smem + L::ds_off : smem + L::q_off + (t % NQ) * L::kTile;
         const float sc = a.scale;
 #pragma unroll
-        for (int c = 0; c < kHalf / 4; ++c)
-          atomicAdd(dst + c, make_float4(__uint_as_float(q[4 * c]) * sc,
-                                         __uint_as_float(q[4 * c + 1]) * sc,
-                                         __uint_as_float(q[4 * c + 2]) * sc,
-                                         __uint_as_float(q[4 * c + 3]) * sc));
+        for (int k = 0; k < kRounds; ++k) {
+          uint8_t* box = stage + k * L::kChunk + kr * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 v4 = make_float4(__uint_as_float(q[32 * k + 4 * u]) * sc,
+                                          __uint_as_float(q[32 * k + 4 * u + 1]) * sc,
+                                          __uint_as_float(q[32 * k + 4 * u + 2]) * sc,
+                                          __uint_as_float(q[32 * k + 4 * u + 3]) * sc);
+            *reinterpret_cast<float4*>(box + ((u ^ (kr & 7)) * 16)) = v4;
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->stg_ready);
       }
       mbar_arrive(&bars->vec_empty[en]);
     }
@@ -563,7 +634,7 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
       configured_for = dev;
     }
     attn_bwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v,
-                                                                  Lc.tm_do, a);
+                                                                  Lc.tm_do, Lc.tm_dq, a);
   } else {
     const int smem = BLayout<64>::alloc;
     static int configured_for = -1;  // device whose attribute is set
@@ -576,7 +647,7 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
       configured_for = dev;
     }
     attn_bwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v,
-                                                                 Lc.tm_do, a);
+                                                                 Lc.tm_do, Lc.tm_dq, a);
   }
   return cudaGetLastError();
 }

@@ -115,10 +115,12 @@ struct BwdLaunch {
   float* D;       // [b, hq, s_q]
   float* dq_acc;  // [b, s_q, hq, d]
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_dq;  // fp32 dQ accumulator, 32 d x 128 rows boxes, 128B swizzle
 };
 cudaError_t launch_attn_bwd(const BwdLaunch& L, cudaStream_t st);
 
 // ---- attn_api.cu
 bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d);
+bool encode_acc_map(CUtensorMap* m, const float* base, int64_t b, int64_t s, int64_t h, int64_t d);
 
 }  // namespace gb300

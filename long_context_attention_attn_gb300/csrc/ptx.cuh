@@ -76,26 +76,40 @@ struct WaitCtx {
   int* status;               // global memory (may be null)
 };
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about `hint_ns` elapses, so waiting warps do not take
+// issue slots from the warps doing the math.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSleepHintNs = 200000;  // 0.2 ms per sleep; woken early on completion
+
 // Waits until the barrier phase with the given parity has completed.
 // Returns false if the CTA is aborting (timeout here or elsewhere).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
-    if (++spins % 64 == 0) {
-      if (*ctx.abort_flag) return false;
-      if (ctx.status && *reinterpret_cast<volatile int*>(ctx.status) != kStatusOk) {
-        *ctx.abort_flag = 1;  // another CTA timed out: stop early
-        return false;
-      }
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *ctx.abort_flag = 1;
-        if (ctx.status) atomicMax(ctx.status, kStatusTimeout);
-        return false;
-      }
+    if (mbar_try_wait_sleep(a, parity, kSleepHintNs)) return true;
+    if (*ctx.abort_flag) return false;
+    if (ctx.status && *reinterpret_cast<volatile int*>(ctx.status) != kStatusOk) {
+      *ctx.abort_flag = 1;  // another CTA timed out: stop early
+      return false;
+    }
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *ctx.abort_flag = 1;
+      if (ctx.status) atomicMax(ctx.status, kStatusTimeout);
+      return false;
     }
   }
 }
@@ -130,10 +144,9 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
-    if (++spins % 64 == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    if (mbar_try_wait_sleep(a, parity, kSleepHintNs)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
       if (status) atomicMax(status, kStatusTimeout);
       return false;
     }
@@ -153,6 +166,27 @@ __device__ __forceinline__ void tma_load_4d(uint32_t smem_dst, const CUtensorMap
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 4-D tiled reduce-add of a shared-memory box into global memory (bulk group).
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, uint32_t smem_src, int c0,
+                                                  int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(smem_src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until the shared-memory sources of all committed bulk groups are read.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until all committed bulk groups have completed (global writes done).
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
