@@ -180,6 +180,50 @@ def oracle_sample(w, budget_s=12.0, max_blocks=48):
     return flops / dt / 1e12, info
 
 
+def hbm_components(ga, dev, pk):
+    """HBM-bound rows of the hot path at the ring workload's shapes (b=1,
+    s=32768, 64 query heads, d=128): one merge of a full-sequence fp32 partial
+    into an fp32 accumulator (12*d+12 bytes per row-head), and the dual-chunk
+    reorder of q (2 x 1 GiB).  CUDA events, median of 10 after 3 warm-ups."""
+    import torch
+
+    b, s, h, d = 1, 32768, 64, 128
+    g = torch.Generator(device=dev).manual_seed(5)
+    acc = torch.randn(b, s, h, d, generator=g, device=dev)
+    blk = torch.randn(b, s, h, d, generator=g, device=dev)
+    la = torch.randn(b, h, s, generator=g, device=dev)
+    lb = torch.randn(b, h, s, generator=g, device=dev)
+    q = torch.randn(b, s, h, d, generator=g, device=dev).to(torch.bfloat16)
+    qo = torch.empty_like(q)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return sorted(ts)[len(ts) // 2]
+
+    merge_ms = timed(lambda: ga.attn_merge_partial(acc, la, blk, lb))
+    merge_bytes = b * s * h * (12 * d + 12)
+    reorder_ms = timed(lambda: ga.reorder_causal_lb(q, ga.DUAL_CHUNK, 4, out=qo))
+    reorder_bytes = 2 * q.numel() * q.element_size()
+    out = {"merge_gbs": merge_bytes / (merge_ms * 1e-3) / 1e9,
+           "merge_bytes": merge_bytes, "merge_ms": merge_ms,
+           "reorder_gbs": reorder_bytes / (reorder_ms * 1e-3) / 1e9,
+           "reorder_bytes": reorder_bytes, "reorder_ms": reorder_ms}
+    out["merge_pct_hbm"] = 100 * out["merge_gbs"] / pk["hbm_gbs"]
+    out["reorder_pct_hbm"] = 100 * out["reorder_gbs"] / pk["hbm_gbs"]
+    del acc, blk, la, lb, q, qo
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args, rank):
     import workload
     w = workload.WORKLOADS[args.workload]
@@ -333,6 +377,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     pk = peaks()
+    hbm = hbm_components(ga, dev, pk)
     bwd_tflops = bwd_flop / (bwd_avg * 1e-3) / 1e12
     fwd_tflops = fwd_flop / (fwd_avg * 1e-3) / 1e12
     per_gpu = value / world
@@ -360,7 +405,10 @@ def run_ours(args, rank, world, local_rank):
                         "sustained": 100 * per_gpu / pk["bf16_sustained"],
                         "source": pk["source"]},
         "components": {"fwd_ms": fwd_avg, "bwd_ms": bwd_avg, "fwd_tflops": fwd_tflops,
-                       "bwd_tflops": bwd_tflops},
+                       "bwd_tflops": bwd_tflops,
+                       "fwd_pct_of_burst_peak": 100 * fwd_tflops / pk["bf16_burst"],
+                       "bwd_pct_of_burst_peak": 100 * bwd_tflops / pk["bf16_burst"],
+                       "hbm_rows": hbm},
         "roofline": {"kernel": "attn_bwd (fused backward + its D pre-pass, plan and dQ "
                                "finalise; timed per call)",
                      "bound": "tensor", "achieved": bwd_tflops, "peak": pk["bf16_sustained"],

@@ -138,7 +138,8 @@ GB300ATTN_API int attn_bwd(const attn_bwd_params* p, attn_stream_t stream);
  *  out_final NULL, or bf16 [b, s, h, d]: then O' goes there (as bf16, RNE)
  *            instead of into out_acc.
  * A row whose accumulator LSE is -inf takes the block as is (its out_acc
- * value is not read).  Pointers 16-byte aligned; d % 8 == 0.
+ * value is ignored, so the accumulator needs no initialisation).  Pointers
+ * 16-byte aligned; d % 8 == 0.
  */
 GB300ATTN_API int attn_merge_partial(float* out_acc, float* lse_acc, const void* out_blk,
                        const float* lse_blk, int blk_is_bf16, void* out_final,

@@ -100,20 +100,30 @@ struct BBars {
 };
 static_assert(sizeof(BBars) <= 256, "barrier block too large");
 
-// Iterates over the steps (query tile, head) of a CTA in a fixed order.
+// Iterates over the steps (head, query tile) of a CTA: heads outer, query
+// tiles inner.  CTAs of neighbouring key tiles of one kv head run at the same
+// time and walk the same head in step, so a dQ tile receives its reduce-adds
+// from them on consecutive steps while it is still in L2.
 struct StepIter {
-  int i, hh, i_end, g;
+  int i, hh, i_first, i_end, g;
   const uint8_t* cls_col;  // cls + b*nq*nk + c, stride nk
   int nk;
-  __device__ bool valid() const { return i <= i_end; }
+  __device__ bool valid() const { return hh < g; }
   __device__ uint8_t kind() const { return cls_col[(size_t)i * nk]; }
   __device__ void skip_to_valid() {
     while (i <= i_end && cls_col[(size_t)i * nk] == kSkip) ++i;
   }
+  __device__ void start() {
+    i = i_first;
+    skip_to_valid();
+    if (i > i_end) hh = g;  // no visible query tile at all
+  }
   __device__ void next() {
-    if (++hh == g) {
-      hh = 0;
-      ++i;
+    ++i;
+    skip_to_valid();
+    if (i > i_end) {
+      ++hh;
+      i = i_first;
       skip_to_valid();
     }
   }
@@ -135,22 +145,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   if (a.status && *reinterpret_cast<volatile int*>(a.status) != kStatusOk) return;
 
-  // ---- work unit: (b, kv tile) heavy first, then kv head
-  const int rank = blockIdx.x / a.hkv;
-  const int kvh = blockIdx.x % a.hkv;
+  // ---- work unit: kv head slowest, then (b, kv tile) heavy first (stable)
+  const int nunits = a.b * a.nk;
+  const int kvh = blockIdx.x / nunits;
+  const int rank = blockIdx.x % nunits;
   const int e = a.order[rank];
   const int bi = e / a.nk;
   const int kt = e % a.nk;
   const int2 rng = a.krange[e];
   const int nsteps_total = a.kweight[e] * a.g;  // (non-SKIP query tile, head) steps
   StepIter it0;
-  it0.i = rng.x;
   it0.hh = 0;
+  it0.i_first = rng.x;
   it0.i_end = rng.y;
   it0.g = a.g;
   it0.cls_col = a.cls + (size_t)bi * a.nq * a.nk + kt;
   it0.nk = a.nk;
-  it0.skip_to_valid();
+  it0.start();
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);

@@ -137,13 +137,17 @@ __global__ void kv_range_kernel(const uint8_t* __restrict__ cls, int64_t nq, int
   }
 }
 
-// Counting sort of n work rows by weight, heaviest first (single CTA).  Rows
-// of equal weight keep an arbitrary order; weights above kBuckets-1 share the
-// top bucket.
+// Stable counting sort of n work rows by weight, heaviest first (single CTA):
+// rows of equal weight keep their index order, so neighbouring tiles stay
+// neighbours in the launch order (their K/V, Q and dQ tiles are then shared
+// through L2 by the CTAs running at the same time).  Weights above
+// kBuckets - 1 share the top bucket.
 constexpr int kBuckets = 2048;
+constexpr int kSortChunk = 1024;
 __global__ void heavy_first_kernel(const int* __restrict__ weight, int n, int* __restrict__ order) {
   __shared__ int hist[kBuckets];
   __shared__ int start[kBuckets];
+  __shared__ int chunk_w[kSortChunk];
   for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x)
@@ -157,9 +161,20 @@ __global__ void heavy_first_kernel(const int* __restrict__ weight, int n, int* _
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int slot = atomicAdd(&start[min(weight[i], kBuckets - 1)], 1);
-    order[slot] = i;
+  for (int c0 = 0; c0 < n; c0 += kSortChunk) {
+    const int m = min(kSortChunk, n - c0);
+    for (int t = threadIdx.x; t < m; t += blockDim.x)
+      chunk_w[t] = min(weight[c0 + t], kBuckets - 1);
+    __syncthreads();
+    for (int t = threadIdx.x; t < m; t += blockDim.x) {
+      const int w = chunk_w[t];
+      int before = 0;  // earlier rows of this chunk with the same weight
+      for (int j = 0; j < t; ++j) before += (chunk_w[j] == w);
+      order[start[w] + before] = c0 + t;
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < m; t += blockDim.x) atomicAdd(&start[chunk_w[t]], 1);
+    __syncthreads();
   }
 }
 
@@ -287,6 +302,20 @@ cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t s, 
 //   z' = e^(l_a - M) + e^(l_b - M),  LSE' = M + ln z',
 //   O' = (e^(l_a - M) O_a + e^(l_b - M) O_b) / z'.
 // One warp per (token, head) row; lanes stride over d in 4-float vectors.
+// All loads of a row (both LSEs, the accumulator and the block) are issued
+// before any arithmetic so their latencies overlap; a row whose weight is 0
+// ignores its (possibly uninitialised) values through a select.
+template <bool BLK_BF16>
+__device__ __forceinline__ float4 load_blk4(const void* out_blk, int64_t idx4) {
+  if (BLK_BF16) {
+    const uint2 raw = reinterpret_cast<const uint2*>(out_blk)[idx4];
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+    return make_float4(f0.x, f0.y, f1.x, f1.y);
+  }
+  return reinterpret_cast<const float4*>(out_blk)[idx4];
+}
+
 template <bool BLK_BF16, bool FINAL>
 __global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ lse_acc,
                              const void* __restrict__ out_blk, const float* __restrict__ lse_blk,
@@ -303,6 +332,13 @@ __global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ ls
     const int64_t bi = r / (h * s);
     const int64_t li = (bi * h + hh) * s + ti;
     const float la = lse_acc[li], lb = lse_blk[li];
+    float4* acc = reinterpret_cast<float4*>(out_acc + r * d);
+    // the common case d <= 128: one vector per lane, loaded before the math
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), x0 = a0;
+    if (lane < v4) {
+      a0 = acc[lane];
+      x0 = load_blk4<BLK_BF16>(out_blk, r * v4 + lane);
+    }
     const float M = fmaxf(la, lb);
     float ca = 0.f, cb = 0.f, lnew = -INFINITY;
     if (M != -INFINITY) {
@@ -313,27 +349,17 @@ __global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ ls
       ca = ea / z;
       cb = eb / z;
     }
-    float4* acc = reinterpret_cast<float4*>(out_acc + r * d);
     for (int64_t w = lane; w < v4; w += 32) {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ca != 0.f) a = acc[w];
-      float4 x;
-      if (BLK_BF16) {
-        const uint2 raw = reinterpret_cast<const uint2*>(
-            static_cast<const __nv_bfloat16*>(out_blk) + r * d)[w];
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-        const float2 f0 = __bfloat1622float2(p0), f1 = __bfloat1622float2(p1);
-        x = make_float4(f0.x, f0.y, f1.x, f1.y);
-      } else {
-        x = reinterpret_cast<const float4*>(static_cast<const float*>(out_blk) + r * d)[w];
+      float4 a = a0, x = x0;
+      if (w != lane) {  // rows wider than 128: further vectors
+        a = acc[w];
+        x = load_blk4<BLK_BF16>(out_blk, r * v4 + w);
       }
-      if (cb == 0.f) x = make_float4(0.f, 0.f, 0.f, 0.f);
       float4 o;
-      o.x = ca * a.x + cb * x.x;
-      o.y = ca * a.y + cb * x.y;
-      o.z = ca * a.z + cb * x.z;
-      o.w = ca * a.w + cb * x.w;
+      o.x = (ca != 0.f ? ca * a.x : 0.f) + (cb != 0.f ? cb * x.x : 0.f);
+      o.y = (ca != 0.f ? ca * a.y : 0.f) + (cb != 0.f ? cb * x.y : 0.f);
+      o.z = (ca != 0.f ? ca * a.z : 0.f) + (cb != 0.f ? cb * x.z : 0.f);
+      o.w = (ca != 0.f ? ca * a.w : 0.f) + (cb != 0.f ? cb * x.w : 0.f);
       if (FINAL) {
         const __nv_bfloat162 q0 = __floats2bfloat162_rn(o.x, o.y);
         const __nv_bfloat162 q1 = __floats2bfloat162_rn(o.z, o.w);
