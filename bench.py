@@ -80,6 +80,31 @@ def peaks():
                 source="fallback (profiling recipe)")
 
 
+def bwd_traffic():
+    """DRAM bytes per launch of the fused backward kernel on the benchmark
+    workload, from the committed ncu summary, or None once the kernel sources
+    differ from the ones that summary was taken with."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "attn_bwd_dram_full_swa_64k.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.split(":")[0] in ("dram_bytes_read_per_launch",
+                                                   "dram_bytes_write_per_launch",
+                                                   "source_sha256"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    csrc = os.path.join(ROOT, "long_context_attention_attn_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("attn_bwd.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    if vals.get("source_sha256") != h.hexdigest():
+        return None
+    return int(vals["dram_bytes_read_per_launch"]) + int(vals["dram_bytes_write_per_launch"])
+
+
 class Clocks:
     """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
 
@@ -413,7 +438,9 @@ def run_ours(args, rank, world, local_rank):
                                "finalise; timed per call)",
                      "bound": "tensor", "achieved": bwd_tflops, "peak": pk["bf16_sustained"],
                      "unit": "TFLOP/s", "frac": bwd_tflops / pk["bf16_sustained"],
-                     "peak_kind": f"bf16 sustained, {pk['source']}", "traffic": None},
+                     "peak_kind": f"bf16 sustained, {pk['source']}",
+                     "traffic": bwd_traffic() if w.name == WORKLOAD else None,
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read+write)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

@@ -301,10 +301,15 @@ cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t s, 
 // the page's update then gives, with M = max(l_a, l_b):
 //   z' = e^(l_a - M) + e^(l_b - M),  LSE' = M + ln z',
 //   O' = (e^(l_a - M) O_a + e^(l_b - M) O_b) / z'.
-// One warp per (token, head) row; lanes stride over d in 4-float vectors.
-// All loads of a row (both LSEs, the accumulator and the block) are issued
-// before any arithmetic so their latencies overlap; a row whose weight is 0
-// ignores its (possibly uninitialised) values through a select.
+// A warp merges 8 consecutive tokens of one (batch, head): lane j < 8 reads
+// and writes the LSE pair of token j (one 32-byte sector per group), and the
+// 8 rows' accumulator / block vectors (d = 128: one float4 per lane per row)
+// are all loaded before the arithmetic, so their latencies overlap.  Warps
+// with consecutive indices take consecutive heads, i.e. adjacent rows of the
+// [b, s, h, d] tensors.  A row whose weight is 0 ignores its (possibly
+// uninitialised) values through a select.
+constexpr int kMergeRows = 8;
+
 template <bool BLK_BF16>
 __device__ __forceinline__ float4 load_blk4(const void* out_blk, int64_t idx4) {
   if (BLK_BF16) {
@@ -316,28 +321,67 @@ __device__ __forceinline__ float4 load_blk4(const void* out_blk, int64_t idx4) {
   return reinterpret_cast<const float4*>(out_blk)[idx4];
 }
 
+__device__ __forceinline__ float4 merge4(float ca, float cb, const float4& a, const float4& x) {
+  float4 o;
+  o.x = (ca != 0.f ? ca * a.x : 0.f) + (cb != 0.f ? cb * x.x : 0.f);
+  o.y = (ca != 0.f ? ca * a.y : 0.f) + (cb != 0.f ? cb * x.y : 0.f);
+  o.z = (ca != 0.f ? ca * a.z : 0.f) + (cb != 0.f ? cb * x.z : 0.f);
+  o.w = (ca != 0.f ? ca * a.w : 0.f) + (cb != 0.f ? cb * x.w : 0.f);
+  return o;
+}
+
+template <bool FINAL>
+__device__ __forceinline__ void store_merged(float* out_acc, __nv_bfloat16* out_final, int64_t idx4,
+                                             const float4& o) {
+  if (FINAL) {
+    const __nv_bfloat162 q0 = __floats2bfloat162_rn(o.x, o.y);
+    const __nv_bfloat162 q1 = __floats2bfloat162_rn(o.z, o.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<const uint32_t*>(&q0);
+    raw.y = *reinterpret_cast<const uint32_t*>(&q1);
+    reinterpret_cast<uint2*>(out_final)[idx4] = raw;
+  } else {
+    reinterpret_cast<float4*>(out_acc)[idx4] = o;
+  }
+}
+
 template <bool BLK_BF16, bool FINAL>
 __global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ lse_acc,
                              const void* __restrict__ out_blk, const float* __restrict__ lse_blk,
                              __nv_bfloat16* __restrict__ out_final, int64_t b, int64_t s,
                              int64_t h, int64_t d) {
   const int lane = threadIdx.x & 31;
-  const int64_t nrows = b * s * h;
+  const int64_t ngroups = (s + kMergeRows - 1) / kMergeRows;
+  const int64_t nwork = b * ngroups * h;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
   const int64_t v4 = d / 4;
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < nrows;
-       r += nwarps) {
-    const int64_t hh = r % h;
-    const int64_t ti = (r / h) % s;
-    const int64_t bi = r / (h * s);
-    const int64_t li = (bi * h + hh) * s + ti;
-    const float la = lse_acc[li], lb = lse_blk[li];
-    float4* acc = reinterpret_cast<float4*>(out_acc + r * d);
-    // the common case d <= 128: one vector per lane, loaded before the math
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), x0 = a0;
-    if (lane < v4) {
-      a0 = acc[lane];
-      x0 = load_blk4<BLK_BF16>(out_blk, r * v4 + lane);
+  for (int64_t wi = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; wi < nwork;
+       wi += nwarps) {
+    const int64_t hh = wi % h;
+    const int64_t tg = (wi / h) % ngroups;
+    const int64_t bi = wi / (h * ngroups);
+    const int64_t t0 = tg * kMergeRows;
+    const int nrows = (s - t0 < kMergeRows) ? (int)(s - t0) : kMergeRows;
+    // LSE pair of token t0 + lane (lanes < nrows)
+    const int64_t lbase = (bi * h + hh) * s + t0;
+    float la = -INFINITY, lb = -INFINITY;
+    if (lane < nrows) {
+      la = lse_acc[lbase + lane];
+      lb = lse_blk[lbase + lane];
+    }
+    // row r of token t: (bi * s + t) * h + hh; one float4 per lane when d <= 128
+    float4 av[kMergeRows], xv[kMergeRows];
+    if (v4 <= 32) {
+#pragma unroll
+      for (int j = 0; j < kMergeRows; ++j) {
+        av[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        xv[j] = av[j];
+        if (j < nrows && lane < v4) {
+          const int64_t r = (bi * s + t0 + j) * h + hh;
+          av[j] = reinterpret_cast<const float4*>(out_acc)[r * v4 + lane];
+          xv[j] = load_blk4<BLK_BF16>(out_blk, r * v4 + lane);
+        }
+      }
     }
     const float M = fmaxf(la, lb);
     float ca = 0.f, cb = 0.f, lnew = -INFINITY;
@@ -349,37 +393,31 @@ __global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ ls
       ca = ea / z;
       cb = eb / z;
     }
-    for (int64_t w = lane; w < v4; w += 32) {
-      float4 a = a0, x = x0;
-      if (w != lane) {  // rows wider than 128: further vectors
-        a = acc[w];
-        x = load_blk4<BLK_BF16>(out_blk, r * v4 + w);
-      }
-      float4 o;
-      o.x = (ca != 0.f ? ca * a.x : 0.f) + (cb != 0.f ? cb * x.x : 0.f);
-      o.y = (ca != 0.f ? ca * a.y : 0.f) + (cb != 0.f ? cb * x.y : 0.f);
-      o.z = (ca != 0.f ? ca * a.z : 0.f) + (cb != 0.f ? cb * x.z : 0.f);
-      o.w = (ca != 0.f ? ca * a.w : 0.f) + (cb != 0.f ? cb * x.w : 0.f);
-      if (FINAL) {
-        const __nv_bfloat162 q0 = __floats2bfloat162_rn(o.x, o.y);
-        const __nv_bfloat162 q1 = __floats2bfloat162_rn(o.z, o.w);
-        uint2 raw;
-        raw.x = *reinterpret_cast<const uint32_t*>(&q0);
-        raw.y = *reinterpret_cast<const uint32_t*>(&q1);
-        reinterpret_cast<uint2*>(out_final + r * d)[w] = raw;
+#pragma unroll
+    for (int j = 0; j < kMergeRows; ++j) {
+      const float caj = __shfl_sync(0xffffffffu, ca, j);
+      const float cbj = __shfl_sync(0xffffffffu, cb, j);
+      if (j >= nrows) continue;
+      const int64_t r = (bi * s + t0 + j) * h + hh;
+      if (v4 <= 32) {
+        if (lane < v4) store_merged<FINAL>(out_acc, out_final, r * v4 + lane, merge4(caj, cbj, av[j], xv[j]));
       } else {
-        acc[w] = o;
+        for (int64_t w = lane; w < v4; w += 32) {
+          const float4 a = reinterpret_cast<const float4*>(out_acc)[r * v4 + w];
+          const float4 x = load_blk4<BLK_BF16>(out_blk, r * v4 + w);
+          store_merged<FINAL>(out_acc, out_final, r * v4 + w, merge4(caj, cbj, a, x));
+        }
       }
     }
-    if (lane == 0) lse_acc[li] = lnew;
+    if (lane < nrows) lse_acc[lbase + lane] = lnew;
   }
 }
 
 cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, const float* lse_blk,
                          int blk_bf16, void* out_final, int64_t b, int64_t s, int64_t h, int64_t d,
                          cudaStream_t st) {
-  const int64_t rows = b * s * h;
-  const unsigned grid = (unsigned)std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
+  const int64_t work = b * ((s + kMergeRows - 1) / kMergeRows) * h;  // warp-sized items
+  const unsigned grid = (unsigned)std::min<int64_t>((work + 7) / 8, (int64_t)sm_count() * 4);
   __nv_bfloat16* fin = static_cast<__nv_bfloat16*>(out_final);
   if (blk_bf16) {
     if (fin)
