@@ -105,6 +105,12 @@ typedef struct attn_fwd_params {
  *  dk, dv   bf16 [b, s_kv, h_kv, d]   (written; summed over the GQA group)
  *  workspace  >= attn_bwd_workspace_bytes() bytes, 256-byte aligned; holds the
  *             fp32 dQ accumulator, D = rowsum(dO * O) and the tile plan.
+ *  accumulate_fp32  0: dq/dk/dv are bf16 and are overwritten.
+ *                   1: dq/dk/dv are fp32 and this call's gradients are ADDED to
+ *                   their contents (ring context parallelism sums per-block
+ *                   contributions; "Context parallelism and ring attention",
+ *                   section "Ring attention").  out / lse must then be the final
+ *                   forward output and LSE of the query rows (D and P use them).
  */
 typedef struct attn_bwd_params {
   attn_fwd_params fwd;
@@ -112,6 +118,7 @@ typedef struct attn_bwd_params {
   void* dq;
   void* dk;
   void* dv;
+  int32_t accumulate_fp32;
 } attn_bwd_params;
 
 /* Scratch sizes (bytes) for the given problem; 0 on invalid sizes. */

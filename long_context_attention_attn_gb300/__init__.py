@@ -51,7 +51,7 @@ class FwdParams(ctypes.Structure):
 class BwdParams(ctypes.Structure):
     _fields_ = [
         ("fwd", FwdParams), ("dout", ctypes.c_void_p), ("dq", ctypes.c_void_p),
-        ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p), ("accumulate_fp32", ctypes.c_int32),
     ]
 
 
@@ -175,17 +175,24 @@ def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: in
 
 def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
              window_left: int = -1, scale: Optional[float] = None, dq=None, dk=None, dv=None,
-             workspace: Optional[torch.Tensor] = None):
-    """Backward attention.  Returns (dq, dk, dv) in bf16."""
+             accumulate_fp32: bool = False, workspace: Optional[torch.Tensor] = None):
+    """Backward attention.  Returns (dq, dk, dv): bf16, or with
+    ``accumulate_fp32`` the given fp32 tensors with this call's gradients added."""
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
-    _need_cuda(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids, kv_pos, workspace)
+    _need_cuda(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids, kv_pos, workspace, dq, dk, dv)
+    if accumulate_fp32:
+        if dq is None or dk is None or dv is None:
+            raise ValueError("accumulate_fp32 needs fp32 dq, dk and dv accumulators")
+        if not all(t.dtype == torch.float32 for t in (dq, dk, dv)):
+            raise ValueError("accumulate_fp32 needs fp32 dq, dk and dv accumulators")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     p = BwdParams()
     p.fwd = _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, False)
     p.dout, p.dq, p.dk, p.dv = dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    p.accumulate_fp32 = 1 if accumulate_fp32 else 0
     need = lib().attn_bwd_workspace_bytes(ctypes.byref(p))
     if workspace is None:
         workspace = _workspace(need, q.device)

@@ -175,8 +175,11 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   bl.nk = cdiv(f->s_kv, kTile);
   char* ws = static_cast<char*>(f->workspace);
   bl.D = reinterpret_cast<float*>(ws + L.end);
-  bl.dq_acc = reinterpret_cast<float*>(
-      ws + L.end + align_up((size_t)(f->b * f->h_q * f->s_q) * 4, 256));
+  const bool acc = p->accumulate_fp32 != 0;
+  // accumulate mode: the dQ reduce-adds go straight into the caller's fp32 dq
+  bl.dq_acc = acc ? static_cast<float*>(p->dq)
+                  : reinterpret_cast<float*>(
+                        ws + L.end + align_up((size_t)(f->b * f->h_q * f->s_q) * 4, 256));
   if (!encode_qkv_map(&bl.tm_q, f->q, f->b, f->s_q, f->h_q, f->d) ||
       !encode_qkv_map(&bl.tm_k, f->k, f->b, f->s_kv, f->h_kv, f->d) ||
       !encode_qkv_map(&bl.tm_v, f->v, f->b, f->s_kv, f->h_kv, f->d) ||
@@ -185,13 +188,13 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
     return ATTN_ERR_CUDA;
   const size_t n_dq = (size_t)(f->b * f->s_q * f->h_q * f->d);
   cudaError_t e = cudaMemsetAsync(bl.plan.status, 0, sizeof(int), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(bl.dq_acc, 0, n_dq * 4, st);
+  if (e == cudaSuccess && !acc) e = cudaMemsetAsync(bl.dq_acc, 0, n_dq * 4, st);
   if (e == cudaSuccess) e = launch_tile_plan(*f, bl.plan, bl.nq, bl.nk, true, st);
   if (e == cudaSuccess)
     e = launch_bwd_preprocess(f->out, p->dout, bl.D, f->b, f->s_q, f->h_q, f->d, st);
   if (e == cudaSuccess) e = launch_attn_bwd(bl, st);
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
-  if (e == cudaSuccess) e = launch_dq_finalize(bl.dq_acc, p->dq, (int64_t)n_dq, st);
+  if (e == cudaSuccess && !acc) e = launch_dq_finalize(bl.dq_acc, p->dq, (int64_t)n_dq, st);
   return cuda_status(e);
 }
 

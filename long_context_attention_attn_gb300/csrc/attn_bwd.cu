@@ -63,6 +63,7 @@ struct BwdArgs {
   int* status;
   int b, s_q, s_kv, hq, hkv, g, nq, nk;
   int window;
+  int accumulate;  // dk / dv are fp32 accumulators (add), else bf16 (overwrite)
   float scale;
   float scale_log2;
 };
@@ -285,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && t > 0) ok = mbar_wait(&bars->dk_done, (t - 1) & 1, ctx);
         if (!ok) break;
         tc_fence_after();
+        // S^T = K Q^T  (M = keys, N = queries, K = d)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
@@ -558,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(&bars->vec_empty[en]);
     }
-    // ---- epilogue: dV (half 0) and dK (half 1) rows of this key tile, bf16
+    // ---- epilogue: dV (half 0) and dK (half 1) rows of this key tile: bf16,
+    // or added into fp32 accumulators
     if (ok && t > 0) {
       ok = mbar_wait(&bars->dk_done, (t - 1) & 1, ctx);
       ok = __all_sync(0xffffffffu, ok);
@@ -566,7 +569,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       const float sc = (w == 0) ? 1.f : a.scale;
-      __nv_bfloat16* dst_base = static_cast<__nv_bfloat16*>(w == 0 ? a.dv : a.dk);
       const int64_t row = ((int64_t)bi * a.s_kv + key) * a.hkv + kvh;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
@@ -579,7 +581,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 32; ++u) o[u] = 0u;
         }
         if (!key_in) continue;
-        uint4* dst = reinterpret_cast<uint4*>(dst_base + row * D + c);
+        if (a.accumulate) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(w == 0 ? a.dv : a.dk) +
+                                                  row * D + c);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            float4 v = dst[u];
+            v.x += __uint_as_float(o[4 * u + 0]) * sc;
+            v.y += __uint_as_float(o[4 * u + 1]) * sc;
+            v.z += __uint_as_float(o[4 * u + 2]) * sc;
+            v.w += __uint_as_float(o[4 * u + 3]) * sc;
+            dst[u] = v;
+          }
+          continue;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(w == 0 ? a.dv : a.dk) +
+                                              row * D + c);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 v;
@@ -592,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-
   }
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -629,6 +646,7 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
   a.nq = (int)Lc.nq;
   a.nk = (int)Lc.nk;
   a.window = f.window_left;
+  a.accumulate = p.accumulate_fp32 ? 1 : 0;
   a.scale = f.scale;
   a.scale_log2 = f.scale * kLog2e;
   const int64_t units = f.b * Lc.nk * f.h_kv;

@@ -1,4 +1,4 @@
-"""Ring-attention context parallelism emulated on one GPU.
+"""Context parallelism (ring and all-gather) emulated on one GPU.
 
 "Context parallelism and ring attention", section "Ring attention": every
 shard keeps its query block and, step by step, attends to the key/value block
@@ -21,8 +21,9 @@ from typing import Optional
 
 import torch
 
-from . import (DUAL_CHUNK, STRIPED, attn_fwd, attn_merge_partial, inverse_reorder_causal_lb,
-               reorder_causal_lb, workspace_bytes_fwd)
+from . import (DUAL_CHUNK, STRIPED, attn_bwd, attn_fwd, attn_merge_partial,
+               inverse_reorder_causal_lb, reorder_causal_lb, workspace_bytes_bwd,
+               workspace_bytes_fwd)
 
 
 def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
@@ -79,3 +80,102 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
         inverse_reorder_causal_lb(out_r, strategy, R, stripe_size, seq_dim=1,
                                   out=out[bi:bi + 1])
     return out, lse
+
+
+def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
+                       scale: Optional[float] = None, strategy: int = STRIPED,
+                       stripe_size: int = 512):
+    """All-gather context parallelism on one GPU (TE tutorial section 5,
+    "AllGather" with a striped reorder, stripe_size 512; "Context parallelism
+    and ring attention", section "Communication choices").
+
+    Each logical shard r keeps its query rows [r*s/R, (r+1)*s/R) of the
+    reordered sequence and attends, in one attn_fwd call, to the whole
+    reordered K/V (what an all-gather of K/V would give every device).  The
+    mask uses the reordered segment positions, so the result equals full
+    attention.  Returns (out bf16 [b,s,Hq,d], lse fp32 [b,Hq,s]) in natural
+    token order.
+    """
+    b, s, hq, d = q.shape
+    R = int(cp_size)
+    if s % R:
+        raise ValueError("sequence length must be divisible by cp_size")
+    n = s // R
+    dev = q.device
+    re = lambda x: reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
+    qr, kr, vr, idr, posr = re(q), re(k), re(v), re(ids), re(pos)
+    out = torch.empty_like(q)
+    lse = torch.empty(b, hq, s, dtype=torch.float32, device=dev)
+    out_r = torch.empty(1, s, hq, d, dtype=q.dtype, device=dev)
+    lse_sh = torch.empty(R, hq, n, dtype=torch.float32, device=dev)
+    ws = torch.empty(workspace_bytes_fwd(qr[:1, :n], kr[:1], idr[:1, :n], posr[:1, :n],
+                                         idr[:1], posr[:1], window_left=window_left),
+                     dtype=torch.uint8, device=dev)
+    for bi in range(b):
+        kv = (kr[bi:bi + 1], vr[bi:bi + 1], idr[bi:bi + 1], posr[bi:bi + 1])
+        for r in range(R):
+            rows = slice(r * n, (r + 1) * n)
+            attn_fwd(qr[bi:bi + 1, rows], kv[0], kv[1], idr[bi:bi + 1, rows],
+                     posr[bi:bi + 1, rows], kv[2], kv[3], window_left=window_left, scale=scale,
+                     out=out_r[:, rows], lse=lse_sh[r:r + 1], workspace=ws)
+        lse_t = reorder_causal_lb(lse_sh.view(1, R * hq * n), STRIPED, hq, n, seq_dim=1)
+        inverse_reorder_causal_lb(lse_t.view(hq, s), strategy, R, stripe_size, seq_dim=1,
+                                  out=lse[bi])
+        inverse_reorder_causal_lb(out_r, strategy, R, stripe_size, seq_dim=1,
+                                  out=out[bi:bi + 1])
+    return out, lse
+
+
+def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_left: int = -1,
+                  scale: Optional[float] = None, strategy: int = DUAL_CHUNK,
+                  stripe_size: int = 1):
+    """Backward of ring attention, emulated on one GPU.
+
+    Shard r keeps its query rows, final output O_r, LSE_r and dO_r; at step t
+    it meets key/value block j = (r - t) mod R and adds that block's share of
+    the gradient: dQ_r += dS_rj K_j, dK_j += dS_rj^T Q_r, dV_j += P_rj^T dO_r,
+    with P_rj = exp(scale Q_r K_j^T - LSE_r) from the FINAL LSE and
+    dS_rj = P_rj * (dP_rj - D_r), D_r = rowsum(dO_r * O_r) from the final output
+    ("Context parallelism and ring attention", sections "Ring attention" and
+    "Online softmax": the blocks' softmax pieces share one denominator).  Every
+    contribution is accumulated in fp32 by attn_bwd's accumulate mode.
+
+    out / lse: the forward results in natural order (e.g. from ring_attn_fwd).
+    Returns fp32 (dq [b,s,Hq,d], dk, dv [b,s,Hkv,d]) in natural order.
+    """
+    b, s, hq, d = q.shape
+    hkv = k.shape[2]
+    R = int(cp_size)
+    if s % R:
+        raise ValueError("sequence length must be divisible by cp_size")
+    n = s // R
+    dev = q.device
+    re = lambda x: reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
+    qr, kr, vr, outr, dor = re(q), re(k), re(v), re(out), re(dout)
+    idr, posr = re(ids), re(pos)
+    dq = torch.zeros(b, s, hq, d, dtype=torch.float32, device=dev)
+    dk = torch.zeros(b, s, hkv, d, dtype=torch.float32, device=dev)
+    dv = torch.zeros(b, s, hkv, d, dtype=torch.float32, device=dev)
+    lse_sh = torch.empty(R, hq, n, dtype=torch.float32, device=dev)
+    ws = torch.empty(workspace_bytes_bwd(qr[:1, :n], kr[:1, :n], idr[:1, :n], posr[:1, :n],
+                                         window_left),
+                     dtype=torch.uint8, device=dev)
+    for bi in range(b):
+        # this row's LSE in reordered order, then [Hq, R*n] -> [R, Hq, n] so that
+        # every shard's LSE is contiguous (the inverse of a striped block transpose)
+        lse_r = reorder_causal_lb(lse[bi], strategy, R, stripe_size, seq_dim=1)
+        inverse_reorder_causal_lb(lse_r.view(1, hq * s), STRIPED, hq, n, seq_dim=1,
+                                  out=lse_sh.view(1, R * hq * n))
+        for r in range(R):
+            rq = slice(r * n, (r + 1) * n)
+            for t in range(R):
+                j = (r - t) % R
+                rk = slice(j * n, (j + 1) * n)
+                attn_bwd(qr[bi:bi + 1, rq], kr[bi:bi + 1, rk], vr[bi:bi + 1, rk],
+                         outr[bi:bi + 1, rq], lse_sh[r:r + 1], dor[bi:bi + 1, rq],
+                         idr[bi:bi + 1, rq], posr[bi:bi + 1, rq], idr[bi:bi + 1, rk],
+                         posr[bi:bi + 1, rk], window_left=window_left, scale=scale,
+                         dq=dq[bi:bi + 1, rq], dk=dk[bi:bi + 1, rk], dv=dv[bi:bi + 1, rk],
+                         accumulate_fp32=True, workspace=ws)
+    inv = lambda x: inverse_reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
+    return inv(dq), inv(dk), inv(dv)

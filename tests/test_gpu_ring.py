@@ -40,6 +40,70 @@ def test_ring_matches_oracle(ring, b, s, hq, hkv, d, window, slots, R, strategy,
     np.testing.assert_allclose(ro, fo, atol=1e-12)
 
 
+@pytest.mark.parametrize("s,window,slots,R,strategy,stripe", [
+    (4096, -1, 4, 4, RO.STRIPED, 512),
+    (2048, 300, None, 4, RO.STRIPED, 1),
+    (3072, -1, 2, 3, RO.DUAL_CHUNK, 1),
+])
+def test_allgather_matches_oracle(ring, s, window, slots, R, strategy, stripe):
+    q, k, v = workload.qkv(1, s, 4, 2, 128, seed=s + R)
+    ids, pos = workload.segments(1, s, slots)
+    out, lse = ring.allgather_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), ids.to(DEV), pos.to(DEV),
+                                       R, window_left=window, scale=0.0884, strategy=strategy,
+                                       stripe_size=stripe)
+    torch.cuda.synchronize()
+    ro, rl = A.attn_fwd(q, k, v, ids, pos, ids, pos, window, 0.0884)
+    check_out(out.cpu(), ro)
+    check_lse(lse.cpu(), rl)
+
+
+def test_allgather_tutorial_shape_sampled(ring):
+    """P1's AllGather case: stripe 512 over 4 shards on the 64k packed workload
+    (sampled rows against the oracle)."""
+    w = workload.WORKLOADS["full_swa_64k"]
+    x = workload.make(w, device=DEV, with_dout=False)
+    out, lse = ring.allgather_attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"], 4,
+                                       window_left=w.window_left, scale=w.scale)
+    torch.cuda.synchronize()
+    ids, pos = x["ids"].cpu(), x["pos"].cpu()
+    for bi, h, r0, nr in ((0, 5, 12000, 96), (1, 100, 2 * 16384 + 700, 64)):
+        kvh = h // (w.hq // w.hkv)
+        rows = np.arange(r0, r0 + nr)
+        ro, rl = A.attn_fwd(x["q"][bi:bi + 1, :, h:h + 1].cpu(), x["k"][bi:bi + 1, :, kvh:kvh + 1].cpu(),
+                            x["v"][bi:bi + 1, :, kvh:kvh + 1].cpu(), ids[bi:bi + 1], pos[bi:bi + 1],
+                            ids[bi:bi + 1], pos[bi:bi + 1], w.window_left, w.scale, rows=rows)
+        check_out(out[bi, r0:r0 + nr, h].cpu(), ro[0, rows, 0])
+        check_lse(lse[bi, h, r0:r0 + nr].cpu(), rl[0, 0, rows])
+    del x, out, lse
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,window,slots,R,strategy,stripe", [
+    (1, 2048, 4, 2, 128, -1, None, 4, RO.DUAL_CHUNK, 1),
+    (2, 1536, 4, 1, 64, 200, 2, 3, RO.DUAL_CHUNK, 1),
+    (1, 4096, 2, 1, 128, 700, 4, 4, RO.STRIPED, 128),
+])
+def test_ring_backward_matches_oracle(ring, b, s, hq, hkv, d, window, slots, R, strategy, stripe):
+    """Ring-emulated backward (per-block contributions with the final LSE/D,
+    fp32 accumulation) equals the oracle's full backward."""
+    from tests.parity import check_grad
+    q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=R * 7 + s, with_dout=True)
+    ids, pos = workload.segments(b, s, slots)
+    g = [x.to(DEV) for x in (q, k, v, dout, ids, pos)]
+    out, lse = ring.ring_attn_fwd(g[0], g[1], g[2], g[4], g[5], R, window_left=window,
+                                  scale=d ** -0.5, strategy=strategy, stripe_size=stripe)
+    dq, dk, dv = ring.ring_attn_bwd(g[0], g[1], g[2], out, lse, g[3], g[4], g[5], R,
+                                    window_left=window, scale=d ** -0.5, strategy=strategy,
+                                    stripe_size=stripe)
+    torch.cuda.synchronize()
+    rq, rk, rv = A.attn_bwd(q, k, v, dout, ids, pos, ids, pos, window, d ** -0.5)
+    check_grad(dq.cpu(), rq, "dq")
+    check_grad(dk.cpu(), rk, "dk")
+    check_grad(dv.cpu(), rv, "dv")
+    pad = (ids == 0).to(DEV)
+    assert torch.all(dq[pad] == 0) and torch.all(dk[pad] == 0) and torch.all(dv[pad] == 0)
+
+
 def test_ring_workload_equals_full_attention(ring):
     """The 32k ring workload: R = 4 dual-chunk shards, compared with the
     single-call forward on every element and with the oracle on samples."""
