@@ -47,6 +47,22 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The slowest rank's figure (every rank calls this with its own)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flop_per_rank_step, ms_per_step):
+    """Whole-job throughput: every rank runs one instance per step (weak
+    scaling), timed by the slowest rank."""
+    return world * flop_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def valid_pairs(w):
     """Exact visible-pair count of the workload (per head, all batch rows),
     counted from the segment descriptor: per segment of L valid tokens with an
@@ -345,12 +361,8 @@ def run_ours(args, rank, world, local_rank):
     bwd_ms = sorted(e[1].elapsed_time(e[2]) for e in evs)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
     bwd_avg = sum(bwd_ms) / len(bwd_ms)
-    ms_per_step = total_ms / args.steps
-    if dist:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = world * (fwd_flop + bwd_flop) / (ms_per_step * 1e-3) / 1e12
+    ms_per_step = max_over_ranks(total_ms / args.steps, dist, dev)
+    value = whole_job_tflops(world, fwd_flop + bwd_flop, ms_per_step)
 
     # end to end through the public API: pinned host inputs in, gradients out
     e2e = None
@@ -387,12 +399,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         b_.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b_) / n_e2e
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * (fwd_flop + bwd_flop) / (e2e_ms * 1e-3) / 1e12,
+        e2e_ms = max_over_ranks(a.elapsed_time(b_) / n_e2e, dist, dev)
+        e2e = {"value": whole_job_tflops(world, fwd_flop + bwd_flop, e2e_ms),
                "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo}
         del h_in, h_out, d_in

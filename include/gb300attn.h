@@ -181,6 +181,14 @@ GB300ATTN_API int inverse_reorder_causal_lb(const void* in, void* out, int64_t o
 GB300ATTN_API int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,
                    attn_stream_t stream);
 
+/* Test hook for the device-side timeout path: runs attn_fwd with every key /
+ * value tile load withheld, so the bounded waits of the launch run out (about
+ * one second) instead of completing.  The kernel then stops early, leaves its
+ * outputs undefined and records ATTN_ERR_TIMEOUT in the status word, which
+ * attn_read_device_status reports; the CUDA context stays usable.  Returns
+ * the launch status like attn_fwd.  Not for production use. */
+GB300ATTN_API int attn_fwd_test_timeout(const attn_fwd_params* p, attn_stream_t stream);
+
 /* Synchronises `stream`, then returns the device status word kept at the start
  * of `workspace` by the last attn_fwd / attn_bwd that used it: ATTN_OK, or
  * ATTN_ERR_TIMEOUT if a bounded device-side wait gave up (the kernel then

@@ -25,6 +25,7 @@ EXPORTS = (
     "attn_fwd_workspace_bytes", "attn_bwd_workspace_bytes", "attn_fwd", "attn_bwd",
     "attn_merge_partial", "reorder_causal_lb", "inverse_reorder_causal_lb", "attn_tile_plan",
     "attn_read_device_status", "attn_status_string", "attn_fwd_noalloc",
+    "attn_fwd_test_timeout",
 )
 
 
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
         h.attn_tile_plan.restype = c_int
         h.attn_read_device_status.argtypes = [vp, vp]
         h.attn_read_device_status.restype = c_int
+        h.attn_fwd_test_timeout.argtypes = [ctypes.POINTER(FwdParams), vp]
+        h.attn_fwd_test_timeout.restype = c_int
         h.attn_fwd_noalloc.argtypes = [ctypes.POINTER(FwdParams), vp]
         h.attn_fwd_noalloc.restype = c_int
         h.attn_status_string.argtypes = [c_int]

@@ -105,7 +105,7 @@ size_t attn_fwd_workspace_bytes(const attn_fwd_params* p) {
   return fwd_layout(p).end;
 }
 
-int attn_fwd(const attn_fwd_params* p, attn_stream_t stream) {
+static int fwd_impl(const attn_fwd_params* p, attn_stream_t stream, bool withhold_kv) {
   int rc = check_fwd(p);
   if (rc != ATTN_OK) return rc;
   const PlanLayout L = fwd_layout(p);
@@ -117,6 +117,7 @@ int attn_fwd(const attn_fwd_params* p, attn_stream_t stream) {
   fl.plan = plan_ptrs(p->workspace, L);
   fl.nq = cdiv(p->s_q, kTile);
   fl.nk = cdiv(p->s_kv, kTile);
+  fl.withhold_kv = withhold_kv;
   if (!encode_qkv_map(&fl.tm_q, p->q, p->b, p->s_q, p->h_q, p->d) ||
       !encode_qkv_map(&fl.tm_k, p->k, p->b, p->s_kv, p->h_kv, p->d) ||
       !encode_qkv_map(&fl.tm_v, p->v, p->b, p->s_kv, p->h_kv, p->d))
@@ -125,6 +126,14 @@ int attn_fwd(const attn_fwd_params* p, attn_stream_t stream) {
   if (e == cudaSuccess) e = launch_tile_plan(*p, fl.plan, fl.nq, fl.nk, false, st);
   if (e == cudaSuccess) e = launch_attn_fwd(fl, st);
   return cuda_status(e);
+}
+
+int attn_fwd(const attn_fwd_params* p, attn_stream_t stream) {
+  return fwd_impl(p, stream, false);
+}
+
+int attn_fwd_test_timeout(const attn_fwd_params* p, attn_stream_t stream) {
+  return fwd_impl(p, stream, true);
 }
 
 int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,

@@ -57,6 +57,7 @@ struct FwdArgs {
   int b, s_q, s_kv, hq, hkv, g, npairs, nq, nk;
   int window;
   int out_fp32;
+  int withhold_kv;  // debug hook: issue no K/V loads, so every wait runs out
   float scale_log2;
 };
 
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int last_use[NST];
     for (int i = 0; i < NST; ++i) last_use[i] = -1;
     bool ok = true;
-    for (int j = rng.x; j <= rng.y && ok; ++j) {
+    for (int j = rng.x; j <= rng.y && ok && !a.withhold_kv; ++j) {
       const uint8_t kind = cls_row[j];
       if (kind == kSkip) continue;
       // K tile
@@ -475,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   const attn_fwd_params& p = *Lc.p;
   FwdArgs a;
+  a.withhold_kv = Lc.withhold_kv ? 1 : 0;
   a.q_ids = p.q_segment_ids;
   a.q_pos = p.q_segment_pos;
   a.kv_ids = p.kv_segment_ids;

@@ -104,6 +104,7 @@ struct FwdLaunch {
   PlanPtrs plan;
   int64_t nq, nk;
   CUtensorMap tm_q, tm_k, tm_v;
+  bool withhold_kv = false;  // debug hook (attn_fwd_test_timeout)
 };
 cudaError_t launch_attn_fwd(const FwdLaunch& L, cudaStream_t st);
 

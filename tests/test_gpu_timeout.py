@@ -1,0 +1,39 @@
+"""Device-side failure detection without a GPU fault: every wait in the
+kernels is bounded.  The test hook withholds all key/value loads, so the
+waits run out; the host must then read ATTN_ERR_TIMEOUT from the workspace
+status word, and the next normal call must run and be correct."""
+import ctypes
+
+import pytest
+import torch
+
+import workload
+from oracle import attention as A
+from tests.parity import check_lse, check_out
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def test_withheld_loads_time_out_and_context_stays_usable():
+    import long_context_attention_attn_gb300 as ga
+    w = workload.WORKLOADS["tiny"]
+    x = workload.make(w)
+    g = {k: v.to(DEV) for k, v in x.items()}
+    out = torch.empty_like(g["q"])
+    lse = torch.empty(w.b, w.hq, w.s, device=DEV)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=DEV)
+    p = ga._fwd_params(g["q"], g["k"], g["v"], g["ids"], g["pos"], g["ids"], g["pos"],
+                       w.window_left, w.scale, out, lse, False)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert ga.lib().attn_fwd_test_timeout(ctypes.byref(p), stream) == ga.ATTN_OK
+    assert ga.read_device_status(ws) == ga.ATTN_ERR_TIMEOUT
+    # the context is still usable: a normal call runs, resets the status and is correct
+    o2, l2 = ga.attn_fwd(g["q"], g["k"], g["v"], g["ids"], g["pos"], window_left=w.window_left,
+                         scale=w.scale, workspace=ws)
+    assert ga.read_device_status(ws) == ga.ATTN_OK
+    ro, rl = A.attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"], x["ids"], x["pos"],
+                        w.window_left, w.scale)
+    check_out(o2.cpu(), ro)
+    check_lse(l2.cpu(), rl)
