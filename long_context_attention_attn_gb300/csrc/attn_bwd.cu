@@ -20,11 +20,13 @@
 // warp 2 per-step vector loader; warp 3 dQ reduce issuer;
 // warps 4-7 and 8-11 the two element-wise warpgroups (query columns 0-63 and
 // 64-127 of S^T / dP^T; each also reads back half of the dQ tile).
-// TMEM: dV [0,D)  dK [128,128+D)  S^T [256,384)  dP^T [384,512);
-// P^T (bf16) overwrites S^T columns [256,320) and dS^T columns [320,384); the
-// dQ tile (one N = d MMA group) lands in the dP^T columns [384, 384+D).  So the
-// next step's S^T only waits for dK, and only its dP^T waits for the dQ tile
-// to be read out.
+// TMEM: dV [0,D)  dK [128,128+D)  S^T [256,384)  dP^T [384,512).  Each
+// element-wise half w owns the S^T columns of its 64 queries, [256+64w, 320+64w),
+// and overwrites them with its bf16 P^T (first 32 columns) and dS^T (last 32),
+// so the halves never wait for each other; the dV / dK MMAs take their A
+// operand from the two halves in turn.  The dQ tile (one N = d MMA group) lands
+// in the dP^T columns [384, 384+D).  So the next step's S^T only waits for dK,
+// and only its dP^T waits for the dQ tile to be read out.
 // dQ leaves through shared memory: one half through the dS buffer, the other
 // through the just-finished Q stage; warp 3 issues the TMA reduce-adds and
 // releases both buffers when the TMA has read them.
@@ -93,7 +95,6 @@ struct BBars {
   uint64_t vec_full[NV];
   uint64_t vec_empty[NV];
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, dk_done;
-  uint64_t s_read;  // both element-wise halves have read S^T
   uint64_t stg_ready, stg_free;  // dQ staging boxes written / read by the TMA
   uint64_t drain;
   uint32_t tmem_base;
@@ -183,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_empty, 256);
     mbar_init(&bars->dk_done, 1);
-    mbar_init(&bars->s_read, 256);
     mbar_init(&bars->stg_ready, 256);
     mbar_init(&bars->stg_free, 1);  // arrived by the reduce issuer once the TMA read the staging
     mbar_init(&bars->drain, 1);
@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtx ctx{&bars->abort_flag, a.status};
   constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
-  constexpr uint32_t kColP = 256, kColDS = 320, kColDQ = 384;
+  // P^T / dS^T of half w: columns [kColS + 64w, +32) / [kColS + 64w + 32, +32)
+  constexpr uint32_t kColDQ = 384;
 
   if (warp < 4) {
   regs_dec<kRegsControl>();
@@ -275,8 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_mn = sdesc_lo(smem_u32(smem + L::q_off), L::kChunk);
       const uint32_t do_mn = sdesc_lo(smem_u32(smem + L::do_off), L::kChunk);
       const uint32_t ds_mn = sdesc_lo(smem_u32(smem + L::ds_off), L::kChunk);
-      const uint32_t t_s = tmem + kColS, t_dp = tmem + kColDP, t_p = tmem + kColP;
-      const uint32_t t_ds = tmem + kColDS, t_dq = tmem + kColDQ;
+      const uint32_t t_s = tmem + kColS, t_dp = tmem + kColDP, t_dq = tmem + kColDQ;
       bool ok = mbar_wait(&bars->kv_full, 0, ctx);
       for (int t = 0; t < nsteps_total && ok; ++t) {
         const int qs = t % NQ;
@@ -310,10 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t acc0 = t > 0 ? 1u : 0u;
+        // K-steps 0-3 read half 0's P^T, 4-7 half 1's
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts_lo(tmem + kColDV, t_p + kk * 8, do_mn + ((kk * 2048) >> 4), id_acc,
-                    kk > 0 ? 1u : acc0);
+          mma_ts_lo(tmem + kColDV, t_s + (kk / 4) * 64 + (kk % 4) * 8,
+                    do_mn + ((kk * 2048) >> 4), id_acc, kk > 0 ? 1u : acc0);
         mma_commit(&bars->do_empty);
         // dQ = dS K  (A = dS in smem MN-major, B = K MN-major), N = d
         ok = mbar_wait(&bars->ds_full, t & 1, ctx);
@@ -327,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dK += dS^T Q  (A = dS^T in TMEM, B = Q MN-major)
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts_lo(tmem + kColDK, t_ds + kk * 8, q_mn + qstage + ((kk * 2048) >> 4), id_acc,
-                    kk > 0 ? 1u : acc0);
+          mma_ts_lo(tmem + kColDK, t_s + (kk / 4) * 64 + 32 + (kk % 4) * 8,
+                    q_mn + qstage + ((kk * 2048) >> 4), id_acc, kk > 0 ? 1u : acc0);
         mma_commit(&bars->dk_done);
       }
       mma_commit(&bars->drain);
@@ -474,12 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk2[32];
 #pragma unroll
       for (int u = 0; u < 32; ++u) pk2[u] = pack_bf16(p[2 * u], p[2 * u + 1]);
-      // both halves have read S^T before P^T overwrites it
-      mbar_arrive(&bars->s_read);
-      ok = mbar_wait(&bars->s_read, t & 1, ctx);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tmem_st32(tmem + lane_off + kColP + 32 * w, pk2);
+      tmem_st32(tmem + lane_off + kColS + 64 * w, pk2);  // own columns: no wait
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
@@ -500,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk2[2 * c + 1] = pack_bf16(p[4 * c + 2] * (__uint_as_float(r[4 * c + 2]) - dv4.z),
                                    p[4 * c + 3] * (__uint_as_float(r[4 * c + 3]) - dv4.w));
       }
-      tmem_st32(tmem + lane_off + kColDS + 32 * w, pk2);
+      tmem_st32(tmem + lane_off + kColS + 64 * w + 32, pk2);
       // The dS buffer doubles as the dQ staging area of the previous step: wait
       // until the TMA has read it.
       if (t > 0) {
