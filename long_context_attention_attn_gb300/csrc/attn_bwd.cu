@@ -28,8 +28,9 @@
 // in the dP^T columns [384, 384+D).  So the next step's S^T only waits for dK,
 // and only its dP^T waits for the dQ tile to be read out.
 // dQ leaves through shared memory: one half through the dS buffer, the other
-// through the just-finished Q stage; warp 3 issues the TMA reduce-adds and
-// releases both buffers when the TMA has read them.
+// through the just-finished Q stage; warp 3 issues the TMA reduce-adds of the
+// dS-buffer half first and hands that buffer back to the next step's dS as soon
+// as the TMA has read it, then those of the Q-stage half.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -43,7 +44,7 @@ constexpr int BM = 128;  // query rows per step
 constexpr int BN = 128;  // key rows per CTA
 constexpr int NQ = 2;    // Q tile stages
 constexpr int NV = 4;    // per-step vector ring entries
-// vector entry: lse2, D, ids, pos (128 each), then kind, query tile, head
+// vector entry: lse2, D, ids, pos (128 each), then the step's tile class
 constexpr int kVecEntry = 4 * 128 + 32;
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -95,7 +96,8 @@ struct BBars {
   uint64_t vec_full[NV];
   uint64_t vec_empty[NV];
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, dk_done;
-  uint64_t stg_ready, stg_free;  // dQ staging boxes written / read by the TMA
+  uint64_t stg_ready[2];  // dQ staging written: [0] dS buffer half, [1] Q stage half
+  uint64_t stg_free;      // the dS buffer half has been read by the TMA
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -184,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_empty, 256);
     mbar_init(&bars->dk_done, 1);
-    mbar_init(&bars->stg_ready, 256);
+    mbar_init(&bars->stg_ready[0], 128);
+    mbar_init(&bars->stg_ready[1], 128);
     mbar_init(&bars->stg_free, 1);  // arrived by the reduce issuer once the TMA read the staging
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -343,27 +346,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (StepIter it = it0; it.valid() && ok; it.next(), ++t) {
         const int h = kvh * a.g + it.hh;
         const int qt = it.i;
-        ok = mbar_wait(&bars->stg_ready, t & 1, ctx);
-        if (!ok) break;
         constexpr int kHalfR = D / 2, kRoundsR = kHalfR / 32;
         const uint32_t s0 = smem_u32(smem + L::ds_off);
         const uint32_t s1 = smem_u32(smem + L::q_off + (t % NQ) * L::kTile);
+        ok = mbar_wait(&bars->stg_ready[0], t & 1, ctx);
+        if (!ok) break;
 #pragma unroll
-        for (int k = 0; k < kRoundsR; ++k) {
+        for (int k = 0; k < kRoundsR; ++k)
           tma_reduce_add_4d(&tm_dq, s0 + k * L::kChunk, 32 * k, h, qt * BM, bi);
-          tma_reduce_add_4d(&tm_dq, s1 + k * L::kChunk, kHalfR + 32 * k, h, qt * BM, bi);
-        }
         bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(&bars->stg_free);           // dS buffer reusable
-        mbar_arrive(&bars->q_empty[t % NQ]);    // Q stage reusable
+        // The next step's stg_ready[1] phase must not complete before this wait
+        // has seen the current one: it follows stg_free below, arrived after.
+        ok = mbar_wait(&bars->stg_ready[1], t & 1, ctx);
+        if (!ok) break;
+#pragma unroll
+        for (int k = 0; k < kRoundsR; ++k)
+          tma_reduce_add_4d(&tm_dq, s1 + k * L::kChunk, kHalfR + 32 * k, h, qt * BM, bi);
+        bulk_commit_group();
+        bulk_wait_group_read<1>();
+        mbar_arrive(&bars->stg_free);  // dS buffer half read: reusable
+        bulk_wait_group_read<0>();
+        mbar_arrive(&bars->q_empty[t % NQ]);  // Q stage reusable
       }
       bulk_wait_group0();  // every dQ reduce-add has landed before the CTA exits
     }
   } else if (warp == 2) {
     // ======================================================== vector loader
     // Per step: LSE (base 2; +inf for rows without keys, so P = 0), D, query
-    // ids / pos, and the step's class / query tile / head, into the ring read
+    // ids / pos, and the step's tile class, into the ring read
     // by the element-wise warpgroups (off the TMA producer's path).
     int t = 0;
     bool ok = true;
@@ -400,8 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) {
         vi[4 * BM] = kind;
-        vi[4 * BM + 1] = qt;
-        vi[4 * BM + 2] = h;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->vec_full[en]);
@@ -435,8 +443,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* ventry = vec + en * kVecEntry;
       const int* vmeta = reinterpret_cast<const int*>(ventry) + 4 * BM;
       const bool partial = vmeta[0] == kPartial;
-      const int qt = vmeta[1];
-      const int h = vmeta[2];
       const float* lse2 = ventry + 64 * w;
       const float* dvec = ventry + BM + 64 * w;
       const int* qid = reinterpret_cast<const int*>(ventry + 2 * BM) + 64 * w;
@@ -552,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars->stg_ready);
+        mbar_arrive(&bars->stg_ready[w]);
       }
       mbar_arrive(&bars->vec_empty[en]);
     }

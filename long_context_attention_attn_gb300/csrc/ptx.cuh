@@ -180,9 +180,11 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, uint32_t
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Waits until the shared-memory sources of all committed bulk groups are read.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// Waits until at most N of the most recently committed bulk groups still have
+// shared-memory sources left to read.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 // Waits until all committed bulk groups have completed (global writes done).
 __device__ __forceinline__ void bulk_wait_group0() {
