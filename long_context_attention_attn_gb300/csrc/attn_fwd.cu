@@ -217,8 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || warp == 3) {
     // ======================================================== MMA issuers
     // One issuing thread per head slot (warp 1: slot 0, warp 3: slot 1), each a
-    // plain in-order loop S(n) -> [softmax] -> PV(n), so a group that blocks
-    // while the tensor core drains its queue never delays the other slot.
+    // plain in-order loop S(n) -> [softmax] -> PV(n), so a wait on one slot's
+    // MMAs (S(n+1) overwrites P(n): it follows PV(n)'s completion) never
+    // delays the other slot.
     const int sl = warp == 1 ? 0 : 1;
     if (lane == 0 && sl < nslots) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
@@ -230,6 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d_s = tmem + sl * BN;
       const uint32_t d_o = tmem + 2 * BN + sl * D;
       bool ok = mbar_wait(&bars->q_full, 0, ctx);
+      // Slot 1 starts once slot 0's first softmax is done, so from then on one
+      // slot's softmax overlaps the other slot's MMAs instead of both softmax
+      // warpgroups running at once while the tensor core idles.
+      if (ok && sl == 1 && nt > 0) ok = mbar_wait(&bars->p_full[0], 0, ctx);
       for (int n = 0; n < nt && ok; ++n) {
         // S_sl(n) = Q_sl K(n)^T: needs K(n), and PV_sl(n-1) done (P_sl lives in S_sl)
         const int ldk = 2 * n, slot_k = ldk % NST;
