@@ -75,6 +75,19 @@ enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
  *  workspace      device scratch of at least attn_fwd_workspace_bytes() bytes,
  *                 256-byte aligned; contents need no initialisation and are
  *                 overwritten (the tile plan and the device status word).
+ *  merge_into_out 0: out / lse receive this call's result.
+ *                 1: out (fp32; out_fp32 must be 1) and lse hold a finished
+ *                 partial (O_acc, LSE_acc) of the same query rows over other
+ *                 key blocks; the kernel's epilogue folds this call's result
+ *                 (O_blk, LSE_blk) into it with exactly the merge of
+ *                 attn_merge_partial below ("Context parallelism and ring
+ *                 attention", section "Online softmax"), so a ring step needs
+ *                 no separate merge pass over HBM.  lse is updated; out is
+ *                 updated unless out_final is given.  A row whose LSE_acc is
+ *                 -inf takes the block as is (its out value is ignored).
+ *  out_final      NULL, or (merge_into_out only) bf16 [b, s_q, h_q, d]: the
+ *                 merged O goes there, rounded to bf16 (RNE), instead of into
+ *                 out (the last ring step).  Must not overlap out.
  */
 typedef struct attn_fwd_params {
   const void* q;
@@ -93,6 +106,8 @@ typedef struct attn_fwd_params {
   float* lse;
   void* workspace;
   size_t workspace_bytes;
+  int32_t merge_into_out;
+  void* out_final;
 } attn_fwd_params;
 
 /* Backward parameters: gradient of sum(out * dout) with respect to q, k, v
@@ -101,6 +116,7 @@ typedef struct attn_fwd_params {
  *  out      bf16 [b, s_q, h_q, d]  forward output (as written by attn_fwd)
  *  lse      fp32 [b, h_q, s_q]     forward LSE (as written by attn_fwd)
  *  dout     bf16 [b, s_q, h_q, d]
+ *  (merge_into_out must be 0 and out_final NULL in the embedded fwd fields)
  *  dq       bf16 [b, s_q, h_q, d]     (written)
  *  dk, dv   bf16 [b, s_kv, h_kv, d]   (written; summed over the GQA group)
  *  workspace  >= attn_bwd_workspace_bytes() bytes, 256-byte aligned; holds the

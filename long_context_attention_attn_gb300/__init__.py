@@ -46,6 +46,7 @@ class FwdParams(ctypes.Structure):
         ("scale", ctypes.c_float), ("out_fp32", ctypes.c_int32),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("merge_into_out", ctypes.c_int32), ("out_final", ctypes.c_void_p),
     ]
 
 
@@ -152,15 +153,21 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 
 def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: int = -1,
              scale: Optional[float] = None, out=None, lse=None, out_fp32: bool = False,
+             merge_into_out: bool = False, out_final=None,
              workspace: Optional[torch.Tensor] = None):
     """Forward attention.  Returns (out [b,s_q,Hq,d], lse fp32 [b,Hq,s_q]).
 
     q bf16 [b,s_q,Hq,d]; k, v bf16 [b,s_kv,Hkv,d]; ids/pos int32 [b,s].
     kv_ids / kv_pos default to the query descriptor (self-attention).
+    With ``merge_into_out`` the given fp32 ``out`` / ``lse`` hold a finished
+    partial over other key blocks and this call's result is merged into them
+    (into bf16 ``out_final`` instead of ``out`` when given).
     """
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
-    _need_cuda(q, k, v, q_ids, q_pos, kv_ids, kv_pos, out, lse, workspace)
+    _need_cuda(q, k, v, q_ids, q_pos, kv_ids, kv_pos, out, lse, workspace, out_final)
+    if merge_into_out and (out is None or lse is None or not out_fp32):
+        raise ValueError("merge_into_out needs the fp32 out and lse accumulators")
     b, s_q, hq, d = q.shape
     if out is None:
         out = torch.empty(b, s_q, hq, d, device=q.device,
@@ -168,6 +175,8 @@ def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: in
     if lse is None:
         lse = torch.empty(b, hq, s_q, device=q.device, dtype=torch.float32)
     p = _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, out_fp32)
+    p.merge_into_out = 1 if merge_into_out else 0
+    p.out_final = out_final.data_ptr() if out_final is not None else None
     need = lib().attn_fwd_workspace_bytes(ctypes.byref(p))
     if workspace is None:
         workspace = _workspace(need, q.device)

@@ -47,6 +47,15 @@ int check_fwd(const attn_fwd_params* p) {
       !aligned(p->lse, 4) || !aligned(p->q_segment_ids, 4) || !aligned(p->q_segment_pos, 4) ||
       !aligned(p->kv_segment_ids, 4) || !aligned(p->kv_segment_pos, 4))
     return ATTN_ERR_INVALID_ARG;
+  if (p->merge_into_out != 0 && p->merge_into_out != 1) return ATTN_ERR_INVALID_ARG;
+  if (p->merge_into_out && !p->out_fp32) return ATTN_ERR_INVALID_ARG;
+  if (p->out_final) {
+    if (!p->merge_into_out || !aligned(p->out_final, 16)) return ATTN_ERR_INVALID_ARG;
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(p->out);
+    const uintptr_t f0 = reinterpret_cast<uintptr_t>(p->out_final);
+    const uintptr_t n = (uintptr_t)(p->b * p->s_q * p->h_q * p->d);
+    if (o0 < f0 + 2 * n && f0 < o0 + 4 * n) return ATTN_ERR_INVALID_ARG;  // overlap
+  }
   const int64_t g = p->h_q / p->h_kv;
   const int64_t units = p->b * cdiv(p->s_q, kTile) * p->h_kv * ((g + 1) / 2);
   if (units > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
@@ -167,7 +176,7 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   if (!p) return ATTN_ERR_INVALID_ARG;
   int rc = check_fwd(&p->fwd);
   if (rc != ATTN_OK) return rc;
-  if (p->fwd.out_fp32) return ATTN_ERR_INVALID_ARG;
+  if (p->fwd.out_fp32 || p->fwd.merge_into_out || p->fwd.out_final) return ATTN_ERR_INVALID_ARG;
   if (!p->dout || !p->dq || !p->dk || !p->dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned(p->dout, 16) || !aligned(p->dq, 16) || !aligned(p->dk, 16) || !aligned(p->dv, 16))
     return ATTN_ERR_INVALID_ARG;

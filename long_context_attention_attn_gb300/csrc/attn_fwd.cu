@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "merge_math.cuh"
 #include "ptx.cuh"
 
 namespace gb300 {
@@ -57,6 +58,8 @@ struct FwdArgs {
   int b, s_q, s_kv, hq, hkv, g, npairs, nq, nk;
   int window;
   int out_fp32;
+  int merge;               // fold the result into (out, lse) instead of writing it
+  __nv_bfloat16* out_final;  // merge mode: merged O as bf16 here instead of into out
   int withhold_kv;  // debug hook: issue no K/V loads, so every wait runs out
   float scale_log2;
 };
@@ -429,8 +432,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         const bool has = l > 0.f;
-        const float inv = has ? 1.f / l : 0.f;
+        float inv = has ? 1.f / l : 0.f;
         const int64_t orow = ((int64_t)bi * a.s_q + grow) * a.hq + h;
+        const int64_t lidx = ((int64_t)bi * a.hq + h) * a.s_q + grow;
+        float lse_row = has ? (m + log2f(l)) * kLn2 : -INFINITY;
+        // merge mode: out = ca * out + cb * (this block's O), lse = merged
+        float ca = 0.f;
+        if (a.merge && row_in) {
+          float cb;
+          merge_coeffs(a.lse[lidx], lse_row, ca, cb, lse_row);
+          inv *= cb;
+        }
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
@@ -442,6 +454,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 32; ++u) o[u] = 0u;
           }
           if (!row_in) continue;
+          if (a.merge) {
+            float* acc = static_cast<float*>(a.out) + orow * D + c;
+            float v[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (ca != 0.f) x = reinterpret_cast<const float4*>(acc)[u];
+              v[4 * u] = merge1(ca, 1.f, x.x, __uint_as_float(o[4 * u]) * inv);
+              v[4 * u + 1] = merge1(ca, 1.f, x.y, __uint_as_float(o[4 * u + 1]) * inv);
+              v[4 * u + 2] = merge1(ca, 1.f, x.z, __uint_as_float(o[4 * u + 2]) * inv);
+              v[4 * u + 3] = merge1(ca, 1.f, x.w, __uint_as_float(o[4 * u + 3]) * inv);
+            }
+            if (a.out_final) {
+              uint4* dst = reinterpret_cast<uint4*>(a.out_final + orow * D + c);
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                dst[u] = make_uint4(pack_bf16(v[8 * u], v[8 * u + 1]), pack_bf16(v[8 * u + 2], v[8 * u + 3]),
+                                    pack_bf16(v[8 * u + 4], v[8 * u + 5]),
+                                    pack_bf16(v[8 * u + 6], v[8 * u + 7]));
+            } else {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                reinterpret_cast<float4*>(acc)[u] =
+                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            }
+            continue;
+          }
           if (a.out_fp32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * D + c);
 #pragma unroll
@@ -462,8 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (row_in)
-          a.lse[((int64_t)bi * a.hq + h) * a.s_q + grow] = has ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (row_in) a.lse[lidx] = lse_row;
       }
     }
   }
@@ -504,6 +542,8 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   a.nk = (int)Lc.nk;
   a.window = p.window_left;
   a.out_fp32 = p.out_fp32 ? 1 : 0;
+  a.merge = p.merge_into_out ? 1 : 0;
+  a.out_final = static_cast<__nv_bfloat16*>(p.out_final);
   a.scale_log2 = p.scale * 1.4426950408889634f;
   const int64_t units = p.b * Lc.nq * p.h_kv * a.npairs;
   if (units == 0) return cudaSuccess;

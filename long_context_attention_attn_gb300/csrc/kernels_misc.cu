@@ -5,6 +5,7 @@
 #include <climits>
 
 #include "internal.h"
+#include "merge_math.cuh"
 
 namespace gb300 {
 
@@ -321,14 +322,6 @@ __device__ __forceinline__ float4 load_blk4(const void* out_blk, int64_t idx4) {
   return reinterpret_cast<const float4*>(out_blk)[idx4];
 }
 
-__device__ __forceinline__ float4 merge4(float ca, float cb, const float4& a, const float4& x) {
-  float4 o;
-  o.x = (ca != 0.f ? ca * a.x : 0.f) + (cb != 0.f ? cb * x.x : 0.f);
-  o.y = (ca != 0.f ? ca * a.y : 0.f) + (cb != 0.f ? cb * x.y : 0.f);
-  o.z = (ca != 0.f ? ca * a.z : 0.f) + (cb != 0.f ? cb * x.z : 0.f);
-  o.w = (ca != 0.f ? ca * a.w : 0.f) + (cb != 0.f ? cb * x.w : 0.f);
-  return o;
-}
 
 template <bool FINAL>
 __device__ __forceinline__ void store_merged(float* out_acc, __nv_bfloat16* out_final, int64_t idx4,
@@ -383,16 +376,8 @@ __global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ ls
         }
       }
     }
-    const float M = fmaxf(la, lb);
-    float ca = 0.f, cb = 0.f, lnew = -INFINITY;
-    if (M != -INFINITY) {
-      const float ea = (la == -INFINITY) ? 0.f : expf(la - M);
-      const float eb = (lb == -INFINITY) ? 0.f : expf(lb - M);
-      const float z = ea + eb;
-      lnew = M + logf(z);
-      ca = ea / z;
-      cb = eb / z;
-    }
+    float ca, cb, lnew;
+    merge_coeffs(la, lb, ca, cb, lnew);
 #pragma unroll
     for (int j = 0; j < kMergeRows; ++j) {
       const float caj = __shfl_sync(0xffffffffu, ca, j);

@@ -12,8 +12,9 @@ Masks use the reordered segment positions, so causality across shard
 boundaries follows global positions.
 
 Every step runs in the library's kernels: reorder / inverse reorder,
-attn_fwd on shard views (fp32 partial output), attn_merge_partial.  This
-module is host control only.
+attn_fwd on shard views (fp32 partial output) with the merge folded into its
+epilogue, or attn_merge_partial as a separate pass.  This module is host
+control only.
 """
 from __future__ import annotations
 
@@ -27,11 +28,14 @@ from . import (DUAL_CHUNK, STRIPED, attn_bwd, attn_fwd, attn_merge_partial,
 
 
 def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
-                  scale: Optional[float] = None, strategy: int = DUAL_CHUNK, stripe_size: int = 1):
+                  scale: Optional[float] = None, strategy: int = DUAL_CHUNK, stripe_size: int = 1,
+                  fused_merge: bool = True):
     """Forward attention computed as cp_size ring steps per logical shard.
 
     q bf16 [b,s,Hq,d]; k, v bf16 [b,s,Hkv,d]; ids/pos int32 [b,s] (natural
     order).  Returns (out bf16 [b,s,Hq,d], lse fp32 [b,Hq,s]) in natural order.
+    ``fused_merge`` folds each step's partial into the running result in the
+    attention kernel's epilogue; otherwise a separate merge pass runs per step.
     """
     b, s, hq, d = q.shape
     R = int(cp_size)
@@ -67,6 +71,10 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
                 elif t == 0:
                     attn_fwd(qv, kv[0], kv[1], iq, pq, kv[2], kv[3], window_left=window_left,
                              scale=scale, out=acc, lse=lacc, out_fp32=True, workspace=ws)
+                elif fused_merge:
+                    attn_fwd(qv, kv[0], kv[1], iq, pq, kv[2], kv[3], window_left=window_left,
+                             scale=scale, out=acc, lse=lacc, out_fp32=True, merge_into_out=True,
+                             out_final=out_r[:, rows] if t == R - 1 else None, workspace=ws)
                 else:
                     attn_fwd(qv, kv[0], kv[1], iq, pq, kv[2], kv[3], window_left=window_left,
                              scale=scale, out=blk, lse=blk_lse, out_fp32=True, workspace=ws)

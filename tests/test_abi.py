@@ -56,6 +56,11 @@ def _params(ga, **kw):
     (dict(d=96), 2), (dict(d=256), 2), (dict(window_right=1), 1), (dict(window_left=-2), 1),
     (dict(h_kv=3), 1), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(b=0), 1),
     (dict(s_q=0), 1), (dict(q=None), 1), (dict(q=(1 << 20) + 8), 1), (dict(lse=None), 1),
+    (dict(merge_into_out=1), 1),                          # merge mode needs fp32 out
+    (dict(merge_into_out=2, out_fp32=1), 1),              # flag is 0 or 1
+    (dict(out_final=1 << 24), 1),                         # out_final only in merge mode
+    (dict(merge_into_out=1, out_fp32=1, out_final=(1 << 24) + 8), 1),  # misaligned
+    (dict(merge_into_out=1, out_fp32=1, out_final=(1 << 20) + 4096), 1),  # overlaps out
 ])
 def test_fwd_rejects_invalid_arguments_on_host(ga, kw, code):
     p = _params(ga, **kw)
@@ -83,6 +88,9 @@ def test_bwd_rejects_invalid_arguments_on_host(ga):
     bp.fwd.out_fp32 = 1
     assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
     bp.fwd.out_fp32 = 0
+    bp.fwd.merge_into_out = 1
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
+    bp.fwd.merge_into_out = 0
     bp.fwd.d = 80
     assert ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp)) == 0
 

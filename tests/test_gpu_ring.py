@@ -20,18 +20,19 @@ def ring():
     return mod
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("b,s,hq,hkv,d,window,slots,R,strategy,stripe", [
     (1, 2048, 4, 2, 128, -1, None, 4, RO.DUAL_CHUNK, 1),
     (2, 1536, 4, 1, 64, 200, 2, 3, RO.DUAL_CHUNK, 1),
     (1, 4096, 2, 1, 128, -1, 4, 4, RO.STRIPED, 128),
     (1, 1024, 2, 2, 128, 100, None, 2, RO.STRIPED, 1),
 ])
-def test_ring_matches_oracle(ring, b, s, hq, hkv, d, window, slots, R, strategy, stripe):
+def test_ring_matches_oracle(ring, b, s, hq, hkv, d, window, slots, R, strategy, stripe, fused):
     q, k, v = workload.qkv(b, s, hq, hkv, d, seed=R + s)
     ids, pos = workload.segments(b, s, slots)
     out, lse = ring.ring_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), ids.to(DEV), pos.to(DEV), R,
                                   window_left=window, scale=d ** -0.5, strategy=strategy,
-                                  stripe_size=stripe)
+                                  stripe_size=stripe, fused_merge=fused)
     torch.cuda.synchronize()
     ro, rl = RG.ring_attention(q, k, v, ids, pos, window, d ** -0.5, R, strategy, stripe)
     check_out(out.cpu(), ro)
@@ -128,3 +129,32 @@ def test_ring_workload_equals_full_attention(ring):
                             w.scale, rows=rows)
         check_out(out[0, r0:r0 + nr, h].cpu(), ro[0, rows, 0])
         check_lse(lse[0, h, r0:r0 + nr].cpu(), rl[0, 0, rows])
+
+
+@pytest.mark.parametrize("final", [False, True])
+def test_fwd_merge_mode_matches_oracle_merge(final):
+    """attn_fwd with merge_into_out folds a block into an accumulator exactly
+    like the oracle's merge of the two partials; rows whose accumulator is
+    empty (LSE -inf, out holding NaN) take the block, rows seeing no key in
+    either keep (0, -inf)."""
+    import long_context_attention_attn_gb300 as ga
+    from oracle import merge as MG
+    b, s, hq, hkv, d = 1, 640, 4, 2, 128
+    q, k, v = workload.qkv(b, 2 * s, hq, hkv, d, seed=77)
+    ids, pos = workload.segments(b, 2 * s, None)
+    ids[:, 600:700] = 0  # padding rows and keys inside both halves
+    qa, ia, pa = q[:, s:], ids[:, s:], pos[:, s:]
+    # accumulator: the second half's queries against the first half's keys
+    acc_o, acc_l = A.attn_fwd(qa, k[:, :s], v[:, :s], ia, pa, ids[:, :s], pos[:, :s], -1, d ** -0.5)
+    blk_o, blk_l = A.attn_fwd(qa, k[:, s:], v[:, s:], ia, pa, ids[:, s:], pos[:, s:], -1, d ** -0.5)
+    want_o, want_l = MG.merge_partial(acc_o, acc_l, blk_o, blk_l)
+    acc = torch.from_numpy(acc_o).float().to(DEV)
+    lacc = torch.from_numpy(acc_l).float().to(DEV)
+    acc[torch.isinf(lacc).transpose(1, 2).unsqueeze(-1).expand_as(acc)] = float("nan")
+    fin = torch.empty(b, s, hq, d, dtype=torch.bfloat16, device=DEV) if final else None
+    ga.attn_fwd(qa.to(DEV), k[:, s:].to(DEV), v[:, s:].to(DEV), ia.to(DEV), pa.to(DEV),
+                ids[:, s:].to(DEV), pos[:, s:].to(DEV), scale=d ** -0.5, out=acc, lse=lacc,
+                out_fp32=True, merge_into_out=True, out_final=fin)
+    torch.cuda.synchronize()
+    check_out((fin if final else acc).float().cpu(), want_o)
+    check_lse(lacc.cpu(), want_l)
