@@ -187,6 +187,26 @@ GB300ATTN_API int inverse_reorder_causal_lb(const void* in, void* out, int64_t o
                               int64_t inner_bytes, int strategy, int cp_size, int stripe_size,
                               attn_stream_t stream);
 
+/* Segment descriptors (ids, pos) from per-row sequence lengths.
+ * TE tutorial section 1 ("Packed THD inputs": a SequenceDescriptor of segment
+ * ids counted from 1, positions from each segment's first token, padding id
+ * 0); TE Cpp attention page, "I/O Contract" (seqlen_q / seqlen_kv inputs).
+ * Covers BSHD batches (nseg = 1 per row), packed variable-length rows
+ * (offsets NULL: segments back to back) and padded slots (explicit offsets).
+ *  seqlens  int32 [b, nseg] segment lengths (negative counts as 0)
+ *  offsets  NULL, or int32 [b, nseg] segment starts, non-decreasing per row;
+ *           NULL = each segment starts where the previous one ends (row 0 at 0)
+ *  ids, pos int32 [b, s] (written): token t belongs to the last segment j of
+ *           its row with start_j <= t; pos = t - start_j and id = j + 1 while
+ *           pos < seqlen_j, else id = 0 (padding); tokens before every start
+ *           get id 0, pos = t.  Segments past s are cut at s.
+ *  1 <= nseg <= 8192; s >= 1; pointers 4-byte aligned; ids / pos must not
+ *  overlap the inputs.
+ */
+GB300ATTN_API int attn_segments_from_seqlens(const int32_t* seqlens, const int32_t* offsets,
+                                             int64_t b, int64_t nseg, int64_t s, int32_t* ids,
+                                             int32_t* pos, attn_stream_t stream);
+
 /* Debug hook: the per-tile work classification the forward pass uses.
  * Page: "Context parallelism and ring attention", section "Causal attention"
  * (skip future blocks, process fully valid blocks, mask overlapping ones).

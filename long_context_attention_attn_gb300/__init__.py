@@ -25,7 +25,7 @@ EXPORTS = (
     "attn_fwd_workspace_bytes", "attn_bwd_workspace_bytes", "attn_fwd", "attn_bwd",
     "attn_merge_partial", "reorder_causal_lb", "inverse_reorder_causal_lb", "attn_tile_plan",
     "attn_read_device_status", "attn_status_string", "attn_fwd_noalloc",
-    "attn_fwd_test_timeout",
+    "attn_fwd_test_timeout", "attn_segments_from_seqlens",
 )
 
 
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         h.attn_fwd_test_timeout.restype = c_int
         h.attn_fwd_noalloc.argtypes = [ctypes.POINTER(FwdParams), vp]
         h.attn_fwd_noalloc.restype = c_int
+        h.attn_segments_from_seqlens.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
+        h.attn_segments_from_seqlens.restype = c_int
         h.attn_status_string.argtypes = [c_int]
         h.attn_status_string.restype = ctypes.c_char_p
         _lib_handle = h
@@ -217,6 +219,24 @@ def workspace_bytes_bwd(q, k, q_ids, q_pos, window_left=-1) -> int:
     p = BwdParams()
     p.fwd = _fwd_params(q, k, k, q_ids, q_pos, q_ids, q_pos, window_left, None, q, q, False)
     return int(lib().attn_bwd_workspace_bytes(ctypes.byref(p)))
+
+
+def segments_from_seqlens(seqlens, s: int, offsets=None):
+    """Segment ids / pos int32 [b, s] from lengths int32 [b, nseg] (and start
+    offsets [b, nseg]; None = segments back to back), on the lengths' device."""
+    _need_cuda(seqlens, offsets)
+    if seqlens.dim() != 2 or seqlens.dtype != torch.int32 or not seqlens.is_contiguous():
+        raise ValueError("seqlens must be a contiguous int32 [b, nseg] tensor")
+    if offsets is not None and (offsets.shape != seqlens.shape or offsets.dtype != torch.int32
+                                or not offsets.is_contiguous()):
+        raise ValueError("offsets must be a contiguous int32 tensor shaped like seqlens")
+    b, nseg = seqlens.shape
+    ids = torch.empty(b, s, dtype=torch.int32, device=seqlens.device)
+    pos = torch.empty(b, s, dtype=torch.int32, device=seqlens.device)
+    _check(lib().attn_segments_from_seqlens(
+        seqlens.data_ptr(), offsets.data_ptr() if offsets is not None else None, b, nseg, s,
+        ids.data_ptr(), pos.data_ptr(), _stream(seqlens.device)), "attn_segments_from_seqlens")
+    return ids, pos
 
 
 def attn_merge_partial(out_acc, lse_acc, out_blk, lse_blk, out_final=None):

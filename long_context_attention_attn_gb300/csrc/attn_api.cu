@@ -216,6 +216,26 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   return cuda_status(e);
 }
 
+int attn_segments_from_seqlens(const int32_t* seqlens, const int32_t* offsets, int64_t b,
+                               int64_t nseg, int64_t s, int32_t* ids, int32_t* pos,
+                               attn_stream_t stream) {
+  if (!seqlens || !ids || !pos || b < 1 || nseg < 1 || s < 1) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(seqlens, 4) || !aligned(ids, 4) || !aligned(pos, 4) || (offsets && !aligned(offsets, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  if (nseg > kSegMax || s > (1ll << 30) || b > 65535) return ATTN_ERR_UNSUPPORTED;
+  const uintptr_t i0 = reinterpret_cast<uintptr_t>(ids), p0 = reinterpret_cast<uintptr_t>(pos);
+  const uintptr_t n = (uintptr_t)(b * s) * 4, m = (uintptr_t)(b * nseg) * 4;
+  const uintptr_t l0 = reinterpret_cast<uintptr_t>(seqlens);
+  const uintptr_t o0 = reinterpret_cast<uintptr_t>(offsets);
+  if (i0 < p0 + n && p0 < i0 + n) return ATTN_ERR_INVALID_ARG;  // ids / pos overlap
+  for (uintptr_t out0 : {i0, p0}) {
+    if (out0 < l0 + m && l0 < out0 + n) return ATTN_ERR_INVALID_ARG;
+    if (offsets && out0 < o0 + m && o0 < out0 + n) return ATTN_ERR_INVALID_ARG;
+  }
+  return cuda_status(launch_segments(seqlens, offsets, b, nseg, s, ids, pos,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int attn_merge_partial(float* out_acc, float* lse_acc, const void* out_blk, const float* lse_blk,
                        int blk_is_bf16, void* out_final, int64_t b, int64_t s, int64_t h, int64_t d,
                        attn_stream_t stream) {

@@ -97,6 +97,9 @@ cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, co
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, int64_t b,
                                   int64_t s, int64_t h, int64_t d, cudaStream_t st);
 cudaError_t launch_dq_finalize(const float* acc, void* dq, int64_t n, cudaStream_t st);
+constexpr int kSegMax = 8192;  // segments per row accepted by launch_segments
+cudaError_t launch_segments(const int* seqlens, const int* offsets, int64_t b, int64_t nseg,
+                            int64_t s, int* ids, int* pos, cudaStream_t st);
 
 // ---- attn_fwd.cu
 struct FwdLaunch {

@@ -514,4 +514,79 @@ cudaError_t launch_dq_finalize(const float* acc, void* dq, int64_t n, cudaStream
   return cudaGetLastError();
 }
 
+// ============================================================== descriptors
+// Segment ids / positions from per-row lengths and optional start offsets
+// (TE tutorial section 1: a packed row's segments are given by ids counted
+// from 1 with positions from each segment's start, padding by id 0; the TE
+// Cpp attention page's I/O contract takes per-row sequence lengths).  Token t
+// of row bi belongs to the last segment j whose start is <= t: pos = t -
+// start_j, id = j + 1 inside the segment's length, else 0; a token before
+// every start is padding with pos = t.  One CTA takes one row slice: it
+// stages the row's starts and lengths in shared memory (running sums of the
+// lengths when no offsets are given, saturated at s) and binary-searches
+// them per token.
+constexpr int kDescTokens = 4096;  // tokens of one row per CTA
+
+__global__ void __launch_bounds__(256) segments_kernel(const int* __restrict__ lens,
+                                                       const int* __restrict__ offs, int nseg,
+                                                       int64_t s, int* __restrict__ ids,
+                                                       int* __restrict__ pos) {
+  __shared__ int start[kSegMax];
+  __shared__ int len_s[kSegMax];
+  const int64_t bi = blockIdx.y;
+  const int* lrow = lens + bi * nseg;
+  for (int j = threadIdx.x; j < nseg; j += blockDim.x) {
+    const int l = lrow[j];
+    len_s[j] = l > 0 ? l : 0;
+    if (offs) start[j] = offs[bi * nseg + j];
+  }
+  __syncthreads();
+  if (!offs && threadIdx.x < 32) {
+    // exclusive running sum of the lengths: lane L scans its own contiguous
+    // chunk, the chunk totals are combined with a warp scan.
+    const int lane = threadIdx.x;
+    const int per = (nseg + 31) / 32;
+    const int j0 = lane * per, j1 = min(j0 + per, nseg);
+    int64_t sum = 0;
+    for (int j = j0; j < j1; ++j) sum += len_s[j];
+    int64_t incl = sum;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int64_t run = incl - sum;
+    for (int j = j0; j < j1; ++j) {
+      start[j] = (int)(run < s ? run : s);  // saturated: tokens are < s
+      run += len_s[j];
+    }
+  }
+  __syncthreads();
+  const int64_t t0 = (int64_t)blockIdx.x * kDescTokens;
+  const int64_t t1 = t0 + kDescTokens < s ? t0 + kDescTokens : s;
+  for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+    int lo = 0, hi = nseg;  // first j with start[j] > t
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((int64_t)start[mid] <= t) lo = mid + 1;
+      else hi = mid;
+    }
+    const int j = lo - 1;
+    int id = 0, p = (int)t;
+    if (j >= 0) {
+      const int64_t rel = t - start[j];
+      p = (int)rel;
+      id = rel < len_s[j] ? j + 1 : 0;
+    }
+    ids[bi * s + t] = id;
+    pos[bi * s + t] = p;
+  }
+}
+
+cudaError_t launch_segments(const int* seqlens, const int* offsets, int64_t b, int64_t nseg,
+                            int64_t s, int* ids, int* pos, cudaStream_t st) {
+  const dim3 grid((unsigned)((s + kDescTokens - 1) / kDescTokens), (unsigned)b);
+  segments_kernel<<<grid, 256, 0, st>>>(seqlens, offsets, (int)nseg, s, ids, pos);
+  return cudaGetLastError();
+}
+
 }  // namespace gb300

@@ -117,3 +117,16 @@ def test_merge_rejects_invalid_arguments_on_host(ga):
 
 def test_device_status_rejects_null(ga):
     assert ga.lib().attn_read_device_status(None, None) == 1
+
+
+def test_segments_rejects_invalid_arguments_on_host(ga):
+    a, o = 1 << 20, 1 << 24
+    f = ga.lib().attn_segments_from_seqlens
+    assert f(None, None, 1, 1, 16, a, o, None) == 1          # no lengths
+    assert f(a, None, 1, 0, 16, o, o + (1 << 20), None) == 1  # nseg 0
+    assert f(a, None, 1, 1, 0, o, o + (1 << 20), None) == 1   # s 0
+    assert f(a + 2, None, 1, 1, 16, o, o + (1 << 20), None) == 1  # misaligned
+    assert f(a, None, 1, 8193, 16, o, o + (1 << 20), None) == 2   # too many segments
+    assert f(a, None, 1, 1, 16, o, o + 32, None) == 1         # ids / pos overlap
+    assert f(a, None, 1, 1, 16, a, o, None) == 1              # ids over the lengths
+    assert f(a, o, 1, 4, 16, o + 8, o + (1 << 20), None) == 1   # ids over the offsets

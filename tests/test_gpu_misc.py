@@ -116,3 +116,34 @@ def test_merge_matches_oracle(ga, blk_dtype, final):
     check_lse(l.cpu(), ref_l)
     if not final:
         np.testing.assert_allclose(got, ref_o, atol=1e-5, rtol=1e-5)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_segments_from_seqlens_bit_exact(seed):
+    """attn_segments_from_seqlens equals the oracle's length -> descriptor map,
+    with and without offsets, including empty, negative and cut-off segments."""
+    import long_context_attention_attn_gb300 as ga
+    from oracle.descriptors import segments_from_seqlens
+    rng = np.random.default_rng(seed)
+    b, nseg, s = 3, [1, 5, 40, 700][seed], [300, 4097, 9000, 70000][seed]
+    lens = rng.integers(-3, max(4, 2 * s // nseg), size=(b, nseg)).astype(np.int32)
+    gaps = rng.integers(0, 9, size=(b, nseg))
+    offs = (np.cumsum(gaps + np.maximum(lens, 0), axis=1) - np.maximum(lens, 0)).astype(np.int32)
+    for offsets in (None, offs):
+        want_i, want_p = segments_from_seqlens(lens, s, offsets)
+        got_i, got_p = ga.segments_from_seqlens(
+            torch.from_numpy(lens).cuda(), s,
+            None if offsets is None else torch.from_numpy(offsets).cuda())
+        np.testing.assert_array_equal(got_i.cpu().numpy(), want_i)
+        np.testing.assert_array_equal(got_p.cpu().numpy(), want_p)
+
+
+def test_segments_from_seqlens_tutorial_row():
+    """The tutorial's padded slots as lengths + offsets reproduce the 64k
+    workload's descriptor bit for bit."""
+    import long_context_attention_attn_gb300 as ga
+    lens = torch.full((2, 4), 12288, dtype=torch.int32, device="cuda")
+    offs = torch.tensor([[0, 16384, 32768, 49152]] * 2, dtype=torch.int32, device="cuda")
+    ids, pos = ga.segments_from_seqlens(lens, 65536, offs)
+    wi, wp = workload.segments(2, 65536, 4)
+    assert torch.equal(ids.cpu(), wi) and torch.equal(pos.cpu(), wp)
