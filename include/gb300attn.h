@@ -88,6 +88,12 @@ enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
  *  out_final      NULL, or (merge_into_out only) bf16 [b, s_q, h_q, d]: the
  *                 merged O goes there, rounded to bf16 (RNE), instead of into
  *                 out (the last ring step).  Must not overlap out.
+ *  kv_token_stride  elements between consecutive tokens of k and of v (and of
+ *                 dk / dv in the backward); 0 = h_kv * d (contiguous).  The
+ *                 packed K/V layout of the TE tutorial (section 1, THD_T2HD:
+ *                 kv [b, s_kv, 2, h_kv, d]) is k = kv, v = kv + h_kv * d,
+ *                 kv_token_stride = 2 * h_kv * d.  Must be >= h_kv * d and a
+ *                 multiple of 8; batch rows are s_kv * kv_token_stride apart.
  */
 typedef struct attn_fwd_params {
   const void* q;
@@ -108,6 +114,7 @@ typedef struct attn_fwd_params {
   size_t workspace_bytes;
   int32_t merge_into_out;
   void* out_final;
+  int64_t kv_token_stride;
 } attn_fwd_params;
 
 /* Backward parameters: gradient of sum(out * dout) with respect to q, k, v
@@ -118,7 +125,8 @@ typedef struct attn_fwd_params {
  *  dout     bf16 [b, s_q, h_q, d]
  *  (merge_into_out must be 0 and out_final NULL in the embedded fwd fields)
  *  dq       bf16 [b, s_q, h_q, d]     (written)
- *  dk, dv   bf16 [b, s_kv, h_kv, d]   (written; summed over the GQA group)
+ *  dk, dv   bf16 [b, s_kv, h_kv, d]   (written; summed over the GQA group),
+ *           tokens fwd.kv_token_stride elements apart like k and v
  *  workspace  >= attn_bwd_workspace_bytes() bytes, 256-byte aligned; holds the
  *             fp32 dQ accumulator, D = rowsum(dO * O) and the tile plan.
  *  accumulate_fp32  0: dq/dk/dv are bf16 and are overwritten.

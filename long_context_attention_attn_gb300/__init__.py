@@ -47,6 +47,7 @@ class FwdParams(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("merge_into_out", ctypes.c_int32), ("out_final", ctypes.c_void_p),
+        ("kv_token_stride", ctypes.c_int64),
     ]
 
 
@@ -125,6 +126,26 @@ def _need_cuda(*ts):
             raise ValueError("gb300attn expects contiguous tensors")
 
 
+def _kv_token_stride(*ts) -> int:
+    """Token stride (elements) shared by k / v-shaped tensors [b, s, h, d]
+    that may be views into a packed K/V tensor [b, s, 2, h, d] (THD_T2HD);
+    0 when they are contiguous."""
+    ref = ts[0]
+    b, s, h, d = ref.shape
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("gb300attn runs on CUDA tensors only")
+        if t.shape != ref.shape or t.stride() != ref.stride():
+            raise ValueError("k and v (and dk, dv) must share one shape and layout")
+    st = ref.stride()
+    if st[3] != 1 or (h > 1 and st[2] != d):
+        raise ValueError("k / v: heads and head dims must be contiguous")
+    ts_ = st[1] if s > 1 else h * d
+    if ts_ < h * d or (b > 1 and st[0] != s * ts_):
+        raise ValueError("k / v: unsupported token or batch stride")
+    return 0 if ts_ == h * d else int(ts_)
+
+
 def _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, out_fp32):
     b, s_q, hq, d = q.shape
     _, s_kv, hkv, _ = k.shape
@@ -167,7 +188,8 @@ def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: in
     """
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
-    _need_cuda(q, k, v, q_ids, q_pos, kv_ids, kv_pos, out, lse, workspace, out_final)
+    _need_cuda(q, q_ids, q_pos, kv_ids, kv_pos, out, lse, workspace, out_final)
+    kv_stride = _kv_token_stride(k, v)
     if merge_into_out and (out is None or lse is None or not out_fp32):
         raise ValueError("merge_into_out needs the fp32 out and lse accumulators")
     b, s_q, hq, d = q.shape
@@ -179,6 +201,7 @@ def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: in
     p = _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, out_fp32)
     p.merge_into_out = 1 if merge_into_out else 0
     p.out_final = out_final.data_ptr() if out_final is not None else None
+    p.kv_token_stride = kv_stride
     need = lib().attn_fwd_workspace_bytes(ctypes.byref(p))
     if workspace is None:
         workspace = _workspace(need, q.device)
@@ -194,7 +217,14 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     ``accumulate_fp32`` the given fp32 tensors with this call's gradients added."""
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
-    _need_cuda(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids, kv_pos, workspace, dq, dk, dv)
+    _need_cuda(q, out, lse, dout, q_ids, q_pos, kv_ids, kv_pos, workspace, dq)
+    kv_stride = _kv_token_stride(k, v)
+    if kv_stride and (dk is None or dv is None):
+        if kv_stride != 2 * k.shape[2] * k.shape[3]:
+            raise ValueError("strided k / v: pass dk and dv in the same layout")
+        dkv = torch.empty(k.shape[0], k.shape[1], 2, k.shape[2], k.shape[3], device=k.device,
+                          dtype=torch.float32 if accumulate_fp32 else k.dtype)
+        dk, dv = (dkv[:, :, 0] if dk is None else dk), (dkv[:, :, 1] if dv is None else dv)
     if accumulate_fp32:
         if dq is None or dk is None or dv is None:
             raise ValueError("accumulate_fp32 needs fp32 dq, dk and dv accumulators")
@@ -203,8 +233,10 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _kv_token_stride(k, v, dk, dv)  # dk / dv must have the layout of k / v
     p = BwdParams()
     p.fwd = _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, False)
+    p.fwd.kv_token_stride = kv_stride
     p.dout, p.dq, p.dk, p.dv = dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
     p.accumulate_fp32 = 1 if accumulate_fp32 else 0
     need = lib().attn_bwd_workspace_bytes(ctypes.byref(p))

@@ -47,6 +47,10 @@ int check_fwd(const attn_fwd_params* p) {
       !aligned(p->lse, 4) || !aligned(p->q_segment_ids, 4) || !aligned(p->q_segment_pos, 4) ||
       !aligned(p->kv_segment_ids, 4) || !aligned(p->kv_segment_pos, 4))
     return ATTN_ERR_INVALID_ARG;
+  if (p->kv_token_stride != 0 &&
+      (p->kv_token_stride < p->h_kv * p->d || p->kv_token_stride % 8 != 0 ||
+       p->kv_token_stride > (1ll << 24)))
+    return ATTN_ERR_INVALID_ARG;
   if (p->merge_into_out != 0 && p->merge_into_out != 1) return ATTN_ERR_INVALID_ARG;
   if (p->merge_into_out && !p->out_fp32) return ATTN_ERR_INVALID_ARG;
   if (p->out_final) {
@@ -78,12 +82,14 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CU
 
 namespace gb300 {
 
-bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d) {
+bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d,
+                    int64_t token_stride) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const int64_t ts = token_stride > 0 ? token_stride : h * d;  // elements between tokens
   // dims innermost first: (d, head, token, batch); box = 64 d x 1 head x 128 tokens.
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)h, (cuuint64_t)s, (cuuint64_t)b};
-  cuuint64_t strides[3] = {(cuuint64_t)(d * 2), (cuuint64_t)(h * d * 2), (cuuint64_t)(s * h * d * 2)};
+  cuuint64_t strides[3] = {(cuuint64_t)(d * 2), (cuuint64_t)(ts * 2), (cuuint64_t)(s * ts * 2)};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
@@ -127,9 +133,9 @@ static int fwd_impl(const attn_fwd_params* p, attn_stream_t stream, bool withhol
   fl.nq = cdiv(p->s_q, kTile);
   fl.nk = cdiv(p->s_kv, kTile);
   fl.withhold_kv = withhold_kv;
-  if (!encode_qkv_map(&fl.tm_q, p->q, p->b, p->s_q, p->h_q, p->d) ||
-      !encode_qkv_map(&fl.tm_k, p->k, p->b, p->s_kv, p->h_kv, p->d) ||
-      !encode_qkv_map(&fl.tm_v, p->v, p->b, p->s_kv, p->h_kv, p->d))
+  if (!encode_qkv_map(&fl.tm_q, p->q, p->b, p->s_q, p->h_q, p->d, 0) ||
+      !encode_qkv_map(&fl.tm_k, p->k, p->b, p->s_kv, p->h_kv, p->d, p->kv_token_stride) ||
+      !encode_qkv_map(&fl.tm_v, p->v, p->b, p->s_kv, p->h_kv, p->d, p->kv_token_stride))
     return ATTN_ERR_CUDA;
   cudaError_t e = cudaMemsetAsync(fl.plan.status, 0, sizeof(int), st);
   if (e == cudaSuccess) e = launch_tile_plan(*p, fl.plan, fl.nq, fl.nk, false, st);
@@ -198,10 +204,10 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   bl.dq_acc = acc ? static_cast<float*>(p->dq)
                   : reinterpret_cast<float*>(
                         ws + L.end + align_up((size_t)(f->b * f->h_q * f->s_q) * 4, 256));
-  if (!encode_qkv_map(&bl.tm_q, f->q, f->b, f->s_q, f->h_q, f->d) ||
-      !encode_qkv_map(&bl.tm_k, f->k, f->b, f->s_kv, f->h_kv, f->d) ||
-      !encode_qkv_map(&bl.tm_v, f->v, f->b, f->s_kv, f->h_kv, f->d) ||
-      !encode_qkv_map(&bl.tm_do, p->dout, f->b, f->s_q, f->h_q, f->d) ||
+  if (!encode_qkv_map(&bl.tm_q, f->q, f->b, f->s_q, f->h_q, f->d, 0) ||
+      !encode_qkv_map(&bl.tm_k, f->k, f->b, f->s_kv, f->h_kv, f->d, f->kv_token_stride) ||
+      !encode_qkv_map(&bl.tm_v, f->v, f->b, f->s_kv, f->h_kv, f->d, f->kv_token_stride) ||
+      !encode_qkv_map(&bl.tm_do, p->dout, f->b, f->s_q, f->h_q, f->d, 0) ||
       !encode_acc_map(&bl.tm_dq, bl.dq_acc, f->b, f->s_q, f->h_q, f->d))
     return ATTN_ERR_CUDA;
   const size_t n_dq = (size_t)(f->b * f->s_q * f->h_q * f->d);

@@ -67,6 +67,7 @@ struct BwdArgs {
   int b, s_q, s_kv, hq, hkv, g, nq, nk;
   int window;
   int accumulate;  // dk / dv are fp32 accumulators (add), else bf16 (overwrite)
+  int64_t kv_stride;  // elements between consecutive tokens of dk / dv
   float scale;
   float scale_log2;
 };
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       const float sc = (w == 0) ? 1.f : a.scale;
-      const int64_t row = ((int64_t)bi * a.s_kv + key) * a.hkv + kvh;
+      const int64_t row0 = ((int64_t)bi * a.s_kv + key) * a.kv_stride + (int64_t)kvh * D;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
@@ -585,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!key_in) continue;
         if (a.accumulate) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(w == 0 ? a.dv : a.dk) +
-                                                  row * D + c);
+                                                  row0 + c);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             float4 v = dst[u];
@@ -598,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(w == 0 ? a.dv : a.dk) +
-                                              row * D + c);
+                                              row0 + c);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 v;
@@ -649,6 +650,7 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
   a.nk = (int)Lc.nk;
   a.window = f.window_left;
   a.accumulate = p.accumulate_fp32 ? 1 : 0;
+  a.kv_stride = f.kv_token_stride > 0 ? f.kv_token_stride : f.h_kv * f.d;
   a.scale = f.scale;
   a.scale_log2 = f.scale * kLog2e;
   const int64_t units = f.b * Lc.nk * f.h_kv;

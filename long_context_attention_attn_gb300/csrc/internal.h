@@ -124,7 +124,8 @@ struct BwdLaunch {
 cudaError_t launch_attn_bwd(const BwdLaunch& L, cudaStream_t st);
 
 // ---- attn_api.cu
-bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d);
+bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d,
+                    int64_t token_stride);
 bool encode_acc_map(CUtensorMap* m, const float* base, int64_t b, int64_t s, int64_t h, int64_t d);
 
 }  // namespace gb300

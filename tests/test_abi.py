@@ -61,6 +61,8 @@ def _params(ga, **kw):
     (dict(out_final=1 << 24), 1),                         # out_final only in merge mode
     (dict(merge_into_out=1, out_fp32=1, out_final=(1 << 24) + 8), 1),  # misaligned
     (dict(merge_into_out=1, out_fp32=1, out_final=(1 << 20) + 4096), 1),  # overlaps out
+    (dict(kv_token_stride=128), 1),                       # below h_kv * d = 256
+    (dict(kv_token_stride=260), 1),                       # not a multiple of 8
 ])
 def test_fwd_rejects_invalid_arguments_on_host(ga, kw, code):
     p = _params(ga, **kw)

@@ -11,7 +11,7 @@ import torch
 
 import workload
 from oracle import attention as A
-from tests.parity import check_grad
+from tests.parity import check_grad, check_lse, check_out
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -112,3 +112,30 @@ def test_full_swa_64k_sampled(ga):
     _sampled(ga, "full_swa_64k",
              dq_samples=[(0, 0, 9000, 64), (1, 7, 16384 + 12200, 120)],
              key_samples=[(0, 3, 12160, 128), (1, 6, 2 * 16384 + 12220, 68)])
+
+
+def test_packed_kv_layout_fwd_bwd():
+    """THD_T2HD (TE tutorial section 1): k and v interleaved in one
+    [b, s, 2, h_kv, d] tensor, passed as strided views; dk / dv come back in
+    the same packed layout.  Same results as the oracle on contiguous k, v."""
+    import long_context_attention_attn_gb300 as ga
+    from oracle import attention as A
+    b, s, hq, hkv, d, window = 2, 1000, 4, 2, 128, 300
+    q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=31, with_dout=True)
+    ids, pos = workload.segments(b, s, None)
+    kv = torch.stack([k, v], dim=2).cuda()          # [b, s, 2, hkv, d]
+    kd, vd = kv[:, :, 0], kv[:, :, 1]
+    assert not kd.is_contiguous()
+    qd, idd, pd, dod = q.cuda(), ids.cuda(), pos.cuda(), dout.cuda()
+    out, lse = ga.attn_fwd(qd, kd, vd, idd, pd, window_left=window, scale=d ** -0.5)
+    dq, dk, dv = ga.attn_bwd(qd, kd, vd, out, lse, dod, idd, pd, window_left=window,
+                             scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert dk.stride() == kd.stride() and dv.data_ptr() - dk.data_ptr() == hkv * d * 2
+    ro, rl = A.attn_fwd(q, k, v, ids, pos, ids, pos, window, d ** -0.5)
+    check_out(out.cpu(), ro)
+    check_lse(lse.cpu(), rl)
+    gq, gk, gv = A.attn_bwd(q, k, v, dout, ids, pos, ids, pos, window, d ** -0.5)
+    check_grad(dq.cpu(), gq, "dq")
+    check_grad(dk.cpu(), gk, "dk")
+    check_grad(dv.cpu(), gv, "dv")
