@@ -83,14 +83,14 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CU
 namespace gb300 {
 
 bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d,
-                    int64_t token_stride) {
+                    int64_t token_stride, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const int64_t ts = token_stride > 0 ? token_stride : h * d;  // elements between tokens
-  // dims innermost first: (d, head, token, batch); box = 64 d x 1 head x 128 tokens.
+  // dims innermost first: (d, head, token, batch); box = 64 d x 1 head x box_rows tokens.
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)h, (cuuint64_t)s, (cuuint64_t)b};
   cuuint64_t strides[3] = {(cuuint64_t)(d * 2), (cuuint64_t)(ts * 2), (cuuint64_t)(s * ts * 2)};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -134,8 +134,10 @@ static int fwd_impl(const attn_fwd_params* p, attn_stream_t stream, bool withhol
   fl.nk = cdiv(p->s_kv, kTile);
   fl.withhold_kv = withhold_kv;
   if (!encode_qkv_map(&fl.tm_q, p->q, p->b, p->s_q, p->h_q, p->d, 0) ||
-      !encode_qkv_map(&fl.tm_k, p->k, p->b, p->s_kv, p->h_kv, p->d, p->kv_token_stride) ||
-      !encode_qkv_map(&fl.tm_v, p->v, p->b, p->s_kv, p->h_kv, p->d, p->kv_token_stride))
+      !encode_qkv_map(&fl.tm_k, p->k, p->b, p->s_kv, p->h_kv, p->d, p->kv_token_stride,
+                      kFwdKeyTile) ||
+      !encode_qkv_map(&fl.tm_v, p->v, p->b, p->s_kv, p->h_kv, p->d, p->kv_token_stride,
+                      kFwdKeyTile))
     return ATTN_ERR_CUDA;
   cudaError_t e = cudaMemsetAsync(fl.plan.status, 0, sizeof(int), st);
   if (e == cudaSuccess) e = launch_tile_plan(*p, fl.plan, fl.nq, fl.nk, false, st);

@@ -7,7 +7,7 @@
 //
 // One CTA computes a 128-row query tile for TWO query heads of one GQA group
 // (both read the same kv head, so every K/V tile loaded into shared memory
-// feeds both).  Roles (384 threads):
+// feeds both), walking the keys in 64-key tiles.  Roles (384 threads):
 //   warp 0        TMA producer: Q tiles once, then K and V tiles into a ring
 //                 of shared-memory slots, plus the key tile's ids/pos.
 //   warp 1        MMA issuer (one thread): S_h = Q_h K^T and O_h += P_h V on
@@ -15,9 +15,12 @@
 //   warps 4-7     softmax for head slot 0 (one thread per query row)
 //   warps 8-11    softmax for head slot 1
 // TMEM (512 columns x 128 lanes, lane = query row):
-//   S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D, 256+2D)
-// P (bf16, 2 per column) overwrites the first 64 columns of its S tile and is
-// the A operand of the P.V MMA straight from TMEM.
+//   slot 0 S buffers [0,64) [64,128), slot 1 [128,192) [192,256),
+//   O0 [256,256+D)  O1 [256+D, 256+2D)
+// Key tile n's scores go to buffer n & 1 of the slot, so S(n+1) is computed
+// while the softmax works on tile n.  P (bf16, 2 per column) overwrites the
+// first 32 columns of its S buffer and is the A operand of the P.V MMA
+// straight from TMEM.
 //
 // Softmax runs in the base-2 domain: x = s * scale * log2(e).  The running
 // maximum m is only raised (and O rescaled) when a row's new maximum exceeds
@@ -34,11 +37,11 @@ namespace gb300 {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int NST = 4;  // K/V shared-memory slots (K and V tiles alternate)
-constexpr int NID = 4;  // ids/pos ring entries
+constexpr int BN = kFwdKeyTile;  // keys per tile (half of the plan's 128-key tile)
+constexpr int NST = 8;   // K/V shared-memory slots (K and V tiles alternate)
+constexpr int NID = 4;   // ids/pos ring entries
 constexpr int kThreads = 384;
-// ids/pos ring entry: 128 ids, 128 pos, then the tile's class (PARTIAL/FULL)
+// ids/pos ring entry: 64 ids, 64 pos, then the tile's class (PARTIAL/FULL)
 constexpr int kIdEntry = 2 * BN + 32;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -66,14 +69,16 @@ struct FwdArgs {
 
 template <int D>
 struct Layout {
-  static constexpr int kChunk = BM * 128;             // one 64-wide bf16 chunk of a 128-row tile
+  static constexpr int kChunk = BM * 128;             // one 64-wide bf16 chunk of a Q tile
+  static constexpr int kChunkKV = BN * 128;           // one 64-wide bf16 chunk of a K / V tile
   static constexpr int kChunks = D / 64;
-  static constexpr int kTileBytes = BM * D * 2;       // a Q, K or V tile
+  static constexpr int kTileBytes = BM * D * 2;       // a Q tile
+  static constexpr int kKVBytes = BN * D * 2;         // a K or V tile
   static constexpr int q_off = 0;                     // 2 Q tiles
   static constexpr int kv_off = q_off + 2 * kTileBytes;
-  static constexpr int id_off = kv_off + NST * kTileBytes;  // NID x kIdEntry ints
+  static constexpr int id_off = kv_off + NST * kKVBytes;  // NID x kIdEntry ints
   static constexpr int bar_off = id_off + NID * kIdEntry * 4;
-  static constexpr int bytes = bar_off + 256;
+  static constexpr int bytes = bar_off + 512;
   // + slack for 1024-byte alignment; at least 150 KB so that one CTA (which
   // holds all 512 TMEM columns) is resident per SM.
   static constexpr int alloc = (bytes + 1024) > 150 * 1024 ? (bytes + 1024) : 150 * 1024;
@@ -85,14 +90,15 @@ struct Bars {
   uint64_t kv_empty[NST];
   uint64_t id_full[NID];
   uint64_t id_empty[NID];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t s_full[2][2];  // [slot][S buffer]
+  uint64_t p_full[2][2];  // [slot][S buffer]
   uint64_t o_done[2];
   uint64_t drain[2];
+  uint64_t slot1_go;  // one phase: slot 0's first softmax is done
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block too large");
+static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h0 = kvh * a.g + 2 * pair;
   const int nslots = (2 * pair + 1 < a.g) ? 2 : 1;
   const int2 rng = a.qrange[e];
-  const int nt = a.qweight[e];  // number of non-SKIP kv tiles of this query tile
+  const int nt = 2 * a.qweight[e];  // 64-key tiles of the non-SKIP 128-key plan tiles
   const uint8_t* cls_row = a.cls + (size_t)e * a.nk;
 
   if (threadIdx.x == 0) {
@@ -136,12 +142,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->id_empty[i], 128 * nslots);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 128);
+      for (int bb = 0; bb < 2; ++bb) {
+        mbar_init(&bars->s_full[i][bb], 1);
+        mbar_init(&bars->p_full[i][bb], 128);
+      }
       mbar_init(&bars->o_done[i], 1);
     }
     mbar_init(&bars->drain[0], 1);
     mbar_init(&bars->drain[1], 1);
+    mbar_init(&bars->slot1_go, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -173,40 +182,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     int last_use[NST];
     for (int i = 0; i < NST; ++i) last_use[i] = -1;
     bool ok = true;
-    for (int j = rng.x; j <= rng.y && ok && !a.withhold_kv; ++j) {
-      const uint8_t kind = cls_row[j];
-      if (kind == kSkip) continue;
-      // K tile
-      {
-        const int ld = 2 * n, slot = ld % NST, use = ld / NST;
+    for (int j2 = 2 * rng.x; j2 <= 2 * rng.y + 1 && ok && !a.withhold_kv; ++j2) {
+      if (cls_row[j2 >> 1] == kSkip) continue;
+      // K tile, then V tile of 64-key tile j2
+#pragma unroll 1
+      for (int kv = 0; kv < 2 && ok; ++kv) {
+        const int ld = 2 * n + kv, slot = ld % NST, use = ld / NST;
         if (lane == 0) {
           ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
           if (ok) {
-            mbar_arrive_expect_tx(&bars->kv_full[slot], L::kTileBytes);
+            mbar_arrive_expect_tx(&bars->kv_full[slot], L::kKVBytes);
             for (int c = 0; c < L::kChunks; ++c)
-              tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kTileBytes + c * L::kChunk), &tm_k,
-                          c * 64, kvh, j * BN, bi, &bars->kv_full[slot]);
+              tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kKVBytes + c * L::kChunkKV),
+                          kv == 0 ? &tm_k : &tm_v, c * 64, kvh, j2 * BN, bi, &bars->kv_full[slot]);
             last_use[slot] = use;
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-      }
-      // V tile
-      {
-        const int ld = 2 * n + 1, slot = ld % NST, use = ld / NST;
-        if (lane == 0) {
-          ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
-          if (ok) {
-            mbar_arrive_expect_tx(&bars->kv_full[slot], L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kTileBytes + c * L::kChunk), &tm_v,
-                          c * 64, kvh, j * BN, bi, &bars->kv_full[slot]);
-            last_use[slot] = use;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
       }
       ++n;
     }
@@ -219,10 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 || warp == 3) {
     // ======================================================== MMA issuers
-    // One issuing thread per head slot (warp 1: slot 0, warp 3: slot 1), each a
-    // plain in-order loop S(n) -> [softmax] -> PV(n), so a wait on one slot's
-    // MMAs (S(n+1) overwrites P(n): it follows PV(n)'s completion) never
-    // delays the other slot.
+    // One issuing thread per head slot (warp 1: slot 0, warp 3: slot 1).  Each
+    // slot has two S buffers in TMEM, so S(n+1) is computed while the softmax
+    // works on S(n): the thread issues S(0), S(1), then per tile
+    // PV(n) -> [PV(n) done: P(n) consumed, its buffer free] -> S(n+2).
     const int sl = warp == 1 ? 0 : 1;
     if (lane == 0 && sl < nslots) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
@@ -230,40 +222,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       // base descriptors: K-major Q / K tiles, MN-major V tiles (128B swizzle)
       const uint32_t da = sdesc_lo(smem_u32(smem + L::q_off + sl * L::kTileBytes), 16);
       const uint32_t kv_lo_k = sdesc_lo(smem_u32(smem + L::kv_off), 16);
-      const uint32_t kv_lo_v = sdesc_lo(smem_u32(smem + L::kv_off), L::kChunk);
-      const uint32_t d_s = tmem + sl * BN;
-      const uint32_t d_o = tmem + 2 * BN + sl * D;
+      const uint32_t kv_lo_v = sdesc_lo(smem_u32(smem + L::kv_off), L::kChunkKV);
+      const uint32_t d_s0 = tmem + 2 * sl * BN;  // buffer bb at d_s0 + bb * BN
+      const uint32_t d_o = tmem + 4 * BN + sl * D;
       bool ok = mbar_wait(&bars->q_full, 0, ctx);
-      // Slot 1 starts once slot 0's first softmax is done, so from then on one
-      // slot's softmax overlaps the other slot's MMAs instead of both softmax
-      // warpgroups running at once while the tensor core idles.
-      if (ok && sl == 1 && nt > 0) ok = mbar_wait(&bars->p_full[0], 0, ctx);
-      for (int n = 0; n < nt && ok; ++n) {
-        // S_sl(n) = Q_sl K(n)^T: needs K(n), and PV_sl(n-1) done (P_sl lives in S_sl)
-        const int ldk = 2 * n, slot_k = ldk % NST;
-        ok = mbar_wait(&bars->kv_full[slot_k], (ldk / NST) & 1, ctx);
-        if (ok && n > 0) ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t db = kv_lo_k + ((slot_k * L::kTileBytes) >> 4);
+      // Slot 1 starts once slot 0's first softmax is done, so the two softmax
+      // warpgroups do not start in step.
+      if (ok && sl == 1 && nt > 0) ok = mbar_wait(&bars->slot1_go, 0, ctx);
+      // n = -2, -1 issue S(0), S(1); every later n issues PV(n), then S(n+2)
+      for (int n = -2; n < nt && ok; ++n) {
+        if (n >= 0) {
+          // O_sl += P_sl(n) V(n): needs V(n) and the softmax of tile n
+          const int ldv = 2 * n + 1, slot_v = ldv % NST;
+          ok = mbar_wait(&bars->kv_full[slot_v], (ldv / NST) & 1, ctx);
+          if (ok) ok = mbar_wait(&bars->p_full[sl][n & 1], (n >> 1) & 1, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dv = kv_lo_v + ((slot_v * L::kKVBytes) >> 4);
+          const uint32_t d_s = d_s0 + (n & 1) * BN;
+          const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
-          mma_ss_lo(d_s, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts_lo(d_o, d_s + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_o,
+                      kk > 0 ? 1u : acc0);
+          mma_commit(&bars->o_done[sl]);
         }
-        mma_commit(&bars->s_full[sl]);
-        // O_sl += P_sl(n) V(n): needs V(n) and the softmax of tile n
-        const int ldv = 2 * n + 1, slot_v = ldv % NST;
-        ok = mbar_wait(&bars->kv_full[slot_v], (ldv / NST) & 1, ctx);
-        if (ok) ok = mbar_wait(&bars->p_full[sl], n & 1, ctx);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t dv = kv_lo_v + ((slot_v * L::kTileBytes) >> 4);
-        const uint32_t acc0 = n > 0 ? 1u : 0u;
+        const int m2 = n + 2;
+        if (m2 < nt) {
+          // S_sl(m2) = Q_sl K(m2)^T into buffer m2 & 1: needs K(m2), and PV(n)
+          // done (P(n) lives in that buffer)
+          const int ldk = 2 * m2, slot_k = ldk % NST;
+          ok = mbar_wait(&bars->kv_full[slot_k], (ldk / NST) & 1, ctx);
+          if (ok && n >= 0) ok = mbar_wait(&bars->o_done[sl], n & 1, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t db = kv_lo_k + ((slot_k * L::kKVBytes) >> 4);
+          const uint32_t d_s = d_s0 + (m2 & 1) * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts_lo(d_o, d_s + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_o, kk > 0 ? 1u : acc0);
-        mma_commit(&bars->o_done[sl]);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t offa = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
+            const uint32_t offb = ((kk / 4) * L::kChunkKV + (kk % 4) * 32) >> 4;
+            mma_ss_lo(d_s, da + offa, db + offb, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[sl][m2 & 1]);
+        }
       }
       // Drain: all MMAs issued by this thread complete before TMEM is freed.
       mma_commit(&bars->drain[sl]);
@@ -275,9 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // softmax warpgroups (off the TMA producer's path).
     int n = 0;
     bool ok = true;
-    for (int j = rng.x; j <= rng.y && ok; ++j) {
-      const uint8_t kind = cls_row[j];
+    for (int j2 = 2 * rng.x; j2 <= 2 * rng.y + 1 && ok; ++j2) {
+      const uint8_t kind = cls_row[j2 >> 1];
       if (kind == kSkip) continue;
+      const int j = j2;  // 64-key tile index
       const int en = n % NID, use = n / NID;
       const int64_t base = (int64_t)bi * a.s_kv;
       int vid[BN / 32], vpos[BN / 32];
@@ -316,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_in = grow < a.s_q;
       const int iq = row_in ? a.q_ids[(int64_t)bi * a.s_q + grow] : 0;
       const int pq = row_in ? a.q_pos[(int64_t)bi * a.s_q + grow] : 0;
-      const uint32_t t_s = tmem + ((uint32_t)(wq * 32) << 16) + sl * BN;
-      const uint32_t t_o = tmem + ((uint32_t)(wq * 32) << 16) + 2 * BN + sl * D;
+      const uint32_t t_s0 = tmem + ((uint32_t)(wq * 32) << 16) + 2 * sl * BN;  // + (n & 1) * BN
+      const uint32_t t_o = tmem + ((uint32_t)(wq * 32) << 16) + 4 * BN + sl * D;
       const float sl2 = a.scale_log2;
       float m = -INFINITY;  // running max (base-2 units)
       float l = 0.f;        // running denominator relative to m
@@ -326,21 +329,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; n < nt;) {
         const int en = n % NID;
         ok = mbar_wait(&bars->id_full[en], (n / NID) & 1, ctx);
-        ok = mbar_wait(&bars->s_full[sl], n & 1, ctx) && ok;
+        ok = mbar_wait(&bars->s_full[sl][n & 1], (n >> 1) & 1, ctx) && ok;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         // S_sl(n) is complete, so this slot is done with K(n) and (its S(n) was
-        // issued after PV_sl(n-1) completed) with V(n-1): release both slots.
+        // issued after PV_sl(n-2) completed) with V(n-2): release both slots.
         if (lane == 0) {
           mbar_arrive(&bars->kv_empty[(2 * n) % NST]);
-          if (n > 0) mbar_arrive(&bars->kv_empty[(2 * n - 1) % NST]);
+          if (n > 1) mbar_arrive(&bars->kv_empty[(2 * n - 3) % NST]);
         }
+        const uint32_t t_s = t_s0 + (n & 1) * BN;
         uint32_t sr[BN];
         tmem_ld32(t_s + 0, &sr[0]);
         tmem_ld32(t_s + 32, &sr[32]);
-        tmem_ld32(t_s + 64, &sr[64]);
-        tmem_ld32(t_s + 96, &sr[96]);
         tmem_wait_ld();
         const int kind = s_ids[en * kIdEntry + 2 * BN];
         if (kind == kPartial) {
@@ -401,8 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l = l * alpha + ((s0 + s1) + (s2 + s3));
         m = m_use;
-        tmem_st32(t_s + 0, &sr[0]);
-        tmem_st32(t_s + 32, &sr[32]);
+        tmem_st32(t_s + 0, &sr[0]);  // P (bf16 pairs) over the first 32 columns
         if (__any_sync(0xffffffffu, rescale) && n > 0) {
           // O += P V of the previous tile must be complete before O is rescaled.
           ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
@@ -421,7 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[sl]);
+        mbar_arrive(&bars->p_full[sl][n & 1]);
+        if (n == 0 && sl == 0 && row == 0 && nslots > 1) mbar_arrive(&bars->slot1_go);
         ++n;
       }
       // ---- epilogue: O = u / z, LSE = ln2 * (m + log2 z)

@@ -10,6 +10,7 @@
 namespace gb300 {
 
 constexpr int kTile = 128;  // query / key tile edge used by the plan and the kernels
+constexpr int kFwdKeyTile = 64;  // keys per tile inside the forward kernel (half a plan tile)
 
 // Per-128-token tile summary of a segment descriptor (32 bytes).
 struct TileSummary {
@@ -125,7 +126,7 @@ cudaError_t launch_attn_bwd(const BwdLaunch& L, cudaStream_t st);
 
 // ---- attn_api.cu
 bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d,
-                    int64_t token_stride);
+                    int64_t token_stride, int box_rows = kTile);
 bool encode_acc_map(CUtensorMap* m, const float* base, int64_t b, int64_t s, int64_t h, int64_t d);
 
 }  // namespace gb300
