@@ -214,10 +214,12 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
     return ATTN_ERR_CUDA;
   const size_t n_dq = (size_t)(f->b * f->s_q * f->h_q * f->d);
   cudaError_t e = cudaMemsetAsync(bl.plan.status, 0, sizeof(int), st);
-  if (e == cudaSuccess && !acc) e = cudaMemsetAsync(bl.dq_acc, 0, n_dq * 4, st);
   if (e == cudaSuccess) e = launch_tile_plan(*f, bl.plan, bl.nq, bl.nk, true, st);
+  // the D pre-pass also zeroes the workspace's fp32 dQ accumulator (not the
+  // caller's accumulator in accumulate mode)
   if (e == cudaSuccess)
-    e = launch_bwd_preprocess(f->out, p->dout, bl.D, f->b, f->s_q, f->h_q, f->d, st);
+    e = launch_bwd_preprocess(f->out, p->dout, bl.D, acc ? nullptr : bl.dq_acc, f->b, f->s_q,
+                              f->h_q, f->d, st);
   if (e == cudaSuccess) e = launch_attn_bwd(bl, st);
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
   if (e == cudaSuccess && !acc) e = launch_dq_finalize(bl.dq_acc, p->dq, (int64_t)n_dq, st);

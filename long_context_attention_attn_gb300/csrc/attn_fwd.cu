@@ -92,7 +92,7 @@ struct Bars {
   uint64_t id_empty[NID];
   uint64_t s_full[2][2];  // [slot][S buffer]
   uint64_t p_full[2][2];  // [slot][S buffer]
-  uint64_t o_done[2];
+  uint64_t o_done[2][2];  // [slot][S buffer of the P.V's tile]
   uint64_t drain[2];
   uint64_t slot1_go;  // one phase: slot 0's first softmax is done
   uint32_t tmem_base;
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->s_full[i][bb], 1);
         mbar_init(&bars->p_full[i][bb], 128);
       }
-      mbar_init(&bars->o_done[i], 1);
+      mbar_init(&bars->o_done[i][0], 1);
+      mbar_init(&bars->o_done[i][1], 1);
     }
     mbar_init(&bars->drain[0], 1);
     mbar_init(&bars->drain[1], 1);
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts_lo(d_o, d_s + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_o,
                       kk > 0 ? 1u : acc0);
-          mma_commit(&bars->o_done[sl]);
+          mma_commit(&bars->o_done[sl][n & 1]);
         }
         const int m2 = n + 2;
         if (m2 < nt) {
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // done (P(n) lives in that buffer)
           const int ldk = 2 * m2, slot_k = ldk % NST;
           ok = mbar_wait(&bars->kv_full[slot_k], (ldk / NST) & 1, ctx);
-          if (ok && n >= 0) ok = mbar_wait(&bars->o_done[sl], n & 1, ctx);
+          if (ok && n >= 0) ok = mbar_wait(&bars->o_done[sl][n & 1], (n >> 1) & 1, ctx);
           if (!ok) break;
           tc_fence_after();
           const uint32_t db = kv_lo_k + ((slot_k * L::kKVBytes) >> 4);
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(t_s + 0, &sr[0]);  // P (bf16 pairs) over the first 32 columns
         if (__any_sync(0xffffffffu, rescale) && n > 0) {
           // O += P V of the previous tile must be complete before O is rescaled.
-          ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
+          ok = mbar_wait(&bars->o_done[sl][(n - 1) & 1], ((n - 1) >> 1) & 1, ctx);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
@@ -427,8 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n;
       }
       // ---- epilogue: O = u / z, LSE = ln2 * (m + log2 z)
+      // The last two P.V groups may both be in flight here (S(n) only waits for
+      // P.V(n-2)), which is why each S buffer has its own o_done barrier: the
+      // last P.V's phase is then never ahead of or behind the waited one by
+      // more than one, and its commit covers every earlier MMA of the slot.
       if (ok && n > 0) {
-        ok = mbar_wait(&bars->o_done[sl], (n - 1) & 1, ctx);
+        ok = mbar_wait(&bars->o_done[sl][(n - 1) & 1], ((n - 1) >> 1) & 1, ctx);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
       }

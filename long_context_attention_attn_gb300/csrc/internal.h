@@ -95,8 +95,10 @@ cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t s, 
 cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, const float* lse_blk,
                          int blk_bf16, void* out_final, int64_t b, int64_t s, int64_t h, int64_t d,
                          cudaStream_t st);
-cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, int64_t b,
-                                  int64_t s, int64_t h, int64_t d, cudaStream_t st);
+// D = rowsum(dout * out) per row-head; also zeroes zero_acc (fp32, out's
+// layout) when it is not null.
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, float* zero_acc,
+                                  int64_t b, int64_t s, int64_t h, int64_t d, cudaStream_t st);
 cudaError_t launch_dq_finalize(const float* acc, void* dq, int64_t n, cudaStream_t st);
 constexpr int kSegMax = 8192;  // segments per row accepted by launch_segments
 cudaError_t launch_segments(const int* seqlens, const int* offsets, int64_t b, int64_t nseg,

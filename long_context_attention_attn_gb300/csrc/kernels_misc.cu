@@ -422,10 +422,13 @@ cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, co
 // D_i = sum_d dO_i * O_i per (b, head, row): the row term of dS = P * (dP - D).
 // Each thread reads 16 bytes (8 bf16) of O and of dO; a row-head of d values
 // is handled by d/8 consecutive lanes (16 for d = 128), reduced by shuffles.
-// The LSE/D layout is [b, h, s] so each row-head writes one float.
+// The LSE/D layout is [b, h, s] so each row-head writes one float.  With
+// zero_acc the same pass clears the fp32 dQ accumulator (out's layout, 32
+// bytes per thread and row), instead of a separate memset over it.
 template <int D>
 __global__ void bwd_preprocess_kernel(const uint4* __restrict__ out, const uint4* __restrict__ dout,
-                                      float* __restrict__ Dv, int64_t b, int64_t s, int64_t h) {
+                                      float* __restrict__ Dv, float4* __restrict__ zero_acc,
+                                      int64_t b, int64_t s, int64_t h) {
   constexpr int kLanes = D / 8;            // lanes per row-head
   constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = threadIdx.x & 31;
@@ -445,6 +448,18 @@ __global__ void bwd_preprocess_kernel(const uint4* __restrict__ out, const uint4
     if (rb < nrows) {
       ob = out[rb * kLanes + sub];
       db = dout[rb * kLanes + sub];
+    }
+    if (zero_acc) {
+      // the fp32 dQ accumulator has out's layout: clear this thread's 8 values
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ra < nrows) {
+        zero_acc[(ra * kLanes + sub) * 2] = z;
+        zero_acc[(ra * kLanes + sub) * 2 + 1] = z;
+      }
+      if (rb < nrows) {
+        zero_acc[(rb * kLanes + sub) * 2] = z;
+        zero_acc[(rb * kLanes + sub) * 2 + 1] = z;
+      }
     }
     auto dot8 = [](const uint4& x, const uint4& y) {
       const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
@@ -477,18 +492,20 @@ __global__ void bwd_preprocess_kernel(const uint4* __restrict__ out, const uint4
   }
 }
 
-cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, int64_t b,
-                                  int64_t s, int64_t h, int64_t d, cudaStream_t st) {
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, float* zero_acc,
+                                  int64_t b, int64_t s, int64_t h, int64_t d, cudaStream_t st) {
   const int64_t rows = b * s * h;
   const int rows_per_cta = 8 * (d == 128 ? 2 : 4);
   const unsigned grid =
       (unsigned)std::min<int64_t>((rows + rows_per_cta - 1) / rows_per_cta, (int64_t)sm_count() * 16);
   if (d == 128)
     bwd_preprocess_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
-                                                     static_cast<const uint4*>(dout), D, b, s, h);
+                                                     static_cast<const uint4*>(dout), D,
+                                                     reinterpret_cast<float4*>(zero_acc), b, s, h);
   else
     bwd_preprocess_kernel<64><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
-                                                    static_cast<const uint4*>(dout), D, b, s, h);
+                                                    static_cast<const uint4*>(dout), D,
+                                                    reinterpret_cast<float4*>(zero_acc), b, s, h);
   return cudaGetLastError();
 }
 
