@@ -56,19 +56,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe: has the phase with this parity completed?
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Shared abort flag + global status word: any bounded wait that gives up
 // records ATTN_ERR_TIMEOUT and makes every other wait of the CTA return early.
 struct WaitCtx {
@@ -113,30 +100,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
   }
 }
-
-// Idle-time bound for polling loops (an issuer that probes several barriers
-// with mbar_test): call idle() whenever a pass made no progress and
-// progress() otherwise; idle() returns false once the CTA must stop.
-struct PollGuard {
-  uint64_t t0 = 0;
-  uint32_t spins = 0;
-  __device__ __forceinline__ void progress() { spins = 0; }
-  __device__ __forceinline__ bool idle(const WaitCtx& ctx) {
-    if (spins == 0) t0 = global_timer_ns();
-    if (++spins % 64 != 0) return true;
-    if (*ctx.abort_flag) return false;
-    if (ctx.status && *reinterpret_cast<volatile int*>(ctx.status) != kStatusOk) {
-      *ctx.abort_flag = 1;
-      return false;
-    }
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *ctx.abort_flag = 1;
-      if (ctx.status) atomicMax(ctx.status, kStatusTimeout);
-      return false;
-    }
-    return true;
-  }
-};
 
 // Bounded wait used while tearing down: ignores the abort flag (the async
 // work it waits for completes on its own), records a timeout in `status`.
@@ -229,26 +192,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 //   MN-major operand: rows of 128 B (64 bf16 of M/N), one row per K index:
 //                    lbo = byte distance between 64-wide M/N blocks,
 //                    sbo = 1024 (next 8 K indices).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;  // descriptor version (tcgen05)
-  d |= 2ull << 61;  // swizzle mode: 128B
-  return d;
-}
-
-// The start-address field is the low 14 bits (address >> 4); shared memory
-// addresses stay below 2^18, so a byte offset advances a descriptor by a plain
-// 64-bit add of (offset >> 4) without carrying into the other fields.
-__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t byte_offset) {
-  return desc + (uint64_t)(byte_offset >> 4);
-}
-
-// Split form of sdesc_sw128: the high word (stride 1024 B, version, 128B
-// swizzle) is the same for every operand here, so only the low word (start
-// address >> 4 | leading offset >> 4 << 16) is kept in a register.
+// Descriptor words: bits 0-13 start address >> 4, 16-29 leading offset >> 4,
+// 32-45 stride offset >> 4 (1024 here), bit 46 descriptor version, bits 61-63
+// swizzle mode (2 = 128B).  The high word is the same for every operand here,
+// so only the low word (start >> 4 | leading offset >> 4 << 16) is kept in a
+// register; a byte offset below 2^18 advances it by a plain add of offset >> 4.
 constexpr uint32_t kSdescHi = ((1024u >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
@@ -276,28 +224,6 @@ __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSdescHi)
-      : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T   (cta_group::1, kind::f16)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -344,17 +270,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-
 // ---------------------------------------------------------------- math
 // Hardware base-2 exponential (MUFU.EX2), flush-to-zero; exp2(-inf) = 0.
 __device__ __forceinline__ float ex2(float x) {
@@ -373,11 +288,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-
-__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // Per-warpgroup register budget (all four warps of the warpgroup execute it).
 // The block is launched with 168 registers x 384 threads = 64512; the
 // producer/MMA warpgroup releases down to 80 and the two compute warpgroups
@@ -392,7 +302,4 @@ __device__ __forceinline__ void regs_inc() {
 }
 constexpr int kRegsControl = 80;
 constexpr int kRegsCompute = 208;
-
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
-
 }  // namespace gb300
