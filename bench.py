@@ -17,6 +17,7 @@ bounded sample of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import tempfile
 import json
 import os
 import subprocess
@@ -131,7 +132,9 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # raw samples (the JSON line carries the summary); BENCH_CLOCKS_DIR keeps them
+        out_dir = os.environ.get("BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_rank{index}.csv")
 
     def __enter__(self):
         try:
