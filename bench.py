@@ -17,11 +17,11 @@ bounded sample of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
-import tempfile
 import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
