@@ -556,27 +556,17 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   if (units == 0) return cudaSuccess;
   if (p.d == 128) {
     const int smem = Layout<128>::alloc;
-    static int configured_for = -1;  // device whose attribute is set
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_for != dev) {
-      cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      configured_for = dev;
-    }
+    static std::atomic<int> smem_set[kMaxDevices];
+    cudaError_t e =
+        ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<128>), smem, smem_set);
+    if (e != cudaSuccess) return e;
     attn_fwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
   } else {
     const int smem = Layout<64>::alloc;
-    static int configured_for = -1;  // device whose attribute is set
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_for != dev) {
-      cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      configured_for = dev;
-    }
+    static std::atomic<int> smem_set[kMaxDevices];
+    cudaError_t e =
+        ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<64>), smem, smem_set);
+    if (e != cudaSuccess) return e;
     attn_fwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
   }
   return cudaGetLastError();

@@ -5,9 +5,27 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "gb300attn.h"
 
 namespace gb300 {
+
+constexpr int kMaxDevices = 64;
+
+// Raises a kernel's dynamic shared memory limit once per device.  Idempotent
+// and safe to call from several host threads: a flag is only set after the
+// attribute call succeeded, and a repeated call is harmless.
+inline cudaError_t ensure_smem_limit(const void* kernel, int bytes, std::atomic<int>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) done[dev].store(1, std::memory_order_release);
+  return e;
+}
 
 constexpr int kTile = 128;  // query / key tile edge used by the plan and the kernels
 constexpr int kFwdKeyTile = 64;  // keys per tile inside the forward kernel (half a plan tile)
