@@ -147,3 +147,44 @@ def test_segments_from_seqlens_tutorial_row():
     ids, pos = ga.segments_from_seqlens(lens, 65536, offs)
     wi, wp = workload.segments(2, 65536, 4)
     assert torch.equal(ids.cpu(), wi) and torch.equal(pos.cpu(), wp)
+
+
+def test_concurrent_calls_from_host_threads():
+    """The library keeps no per-call state: four host threads, each with its own
+    stream and inputs, calling attn_fwd / attn_bwd at once get bit-identical
+    results to the same calls made one after another."""
+    import threading
+    import long_context_attention_attn_gb300 as ga
+    cases = []
+    for i in range(4):
+        q, k, v, dout = workload.qkv(1, 700 + 64 * i, 4, 2, 128 if i % 2 else 64, seed=40 + i,
+                                     with_dout=True)
+        ids, pos = workload.random_segments(1, 700 + 64 * i, seed=40 + i)
+        cases.append(tuple(t.cuda() for t in (q, k, v, dout, ids, pos)))
+
+    def run(c):
+        q, k, v, dout, ids, pos = c
+        out, lse = ga.attn_fwd(q, k, v, ids, pos, window_left=200, scale=0.1)
+        dq, dk, dv = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=200, scale=0.1)
+        return out, lse, dq, dk, dv
+
+    serial = [run(c) for c in cases]
+    torch.cuda.synchronize()
+    results = [None] * len(cases)
+
+    def worker(i):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                results[i] = run(cases[i])
+        s.synchronize()
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    for got, want in zip(results, serial):
+        for g, w in zip(got, want):
+            assert torch.equal(g, w)
