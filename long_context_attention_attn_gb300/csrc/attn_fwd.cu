@@ -9,9 +9,10 @@
 // (both read the same kv head, so every K/V tile loaded into shared memory
 // feeds both), walking the keys in 64-key tiles.  Roles (384 threads):
 //   warp 0        TMA producer: Q tiles once, then K and V tiles into a ring
-//                 of shared-memory slots, plus the key tile's ids/pos.
-//   warp 1        MMA issuer (one thread): S_h = Q_h K^T and O_h += P_h V on
-//                 tcgen05; also owns the TMEM allocation.
+//                 of shared-memory slots.
+//   warps 1, 3    MMA issuers, one thread per head slot: S_h = Q_h K^T and
+//                 O_h += P_h V on tcgen05; warp 1 also owns the TMEM allocation.
+//   warp 2        descriptor loader: each key tile's ids / pos / class.
 //   warps 4-7     softmax for head slot 0 (one thread per query row)
 //   warps 8-11    softmax for head slot 1
 // TMEM (512 columns x 128 lanes, lane = query row):
