@@ -47,6 +47,10 @@ constexpr int NV = 4;    // per-step vector ring entries
 // vector entry: lse2, D, ids, pos (128 each), then the step's tile class
 constexpr int kVecEntry = 4 * 128 + 32;
 constexpr int kThreads = 384;
+// Registers per thread at launch (65536 / 384, rounded down to a multiple of 8).
+constexpr int kLaunchRegs = 168;
+static_assert(128 * kRegsControl + 256 * kRegsCompute <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdArgs {
@@ -659,7 +663,8 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
     const int smem = BLayout<128>::alloc;
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e =
-        ensure_smem_limit(reinterpret_cast<const void*>(attn_bwd_kernel<128>), smem, smem_set);
+        ensure_smem_limit(reinterpret_cast<const void*>(attn_bwd_kernel<128>), smem,
+                          kLaunchRegs, smem_set);
     if (e != cudaSuccess) return e;
     attn_bwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v,
                                                                   Lc.tm_do, Lc.tm_dq, a);
@@ -667,7 +672,8 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
     const int smem = BLayout<64>::alloc;
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e =
-        ensure_smem_limit(reinterpret_cast<const void*>(attn_bwd_kernel<64>), smem, smem_set);
+        ensure_smem_limit(reinterpret_cast<const void*>(attn_bwd_kernel<64>), smem,
+                          kLaunchRegs, smem_set);
     if (e != cudaSuccess) return e;
     attn_bwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v,
                                                                  Lc.tm_do, Lc.tm_dq, a);

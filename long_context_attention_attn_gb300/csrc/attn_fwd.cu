@@ -42,6 +42,10 @@ constexpr int BN = kFwdKeyTile;  // keys per tile (half of the plan's 128-key ti
 constexpr int NST = 8;   // K/V shared-memory slots (K and V tiles alternate)
 constexpr int NID = 4;   // ids/pos ring entries
 constexpr int kThreads = 384;
+// Registers per thread at launch (65536 / 384, rounded down to a multiple of 8).
+constexpr int kLaunchRegs = 168;
+static_assert(128 * kRegsControl + 256 * kRegsCompute <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 // ids/pos ring entry: 64 ids, 64 pos, then the tile's class (PARTIAL/FULL)
 constexpr int kIdEntry = 2 * BN + 32;
 constexpr float kRescaleThreshold = 8.0f;
@@ -559,14 +563,16 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
     const int smem = Layout<128>::alloc;
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e =
-        ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<128>), smem, smem_set);
+        ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<128>), smem,
+                          kLaunchRegs, smem_set);
     if (e != cudaSuccess) return e;
     attn_fwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
   } else {
     const int smem = Layout<64>::alloc;
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e =
-        ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<64>), smem, smem_set);
+        ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<64>), smem,
+                          kLaunchRegs, smem_set);
     if (e != cudaSuccess) return e;
     attn_fwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
   }

@@ -13,15 +13,24 @@ namespace gb300 {
 
 constexpr int kMaxDevices = 64;
 
-// Raises a kernel's dynamic shared memory limit once per device.  Idempotent
-// and safe to call from several host threads: a flag is only set after the
-// attribute call succeeded, and a repeated call is harmless.
-inline cudaError_t ensure_smem_limit(const void* kernel, int bytes, std::atomic<int>* done) {
+// Checks a kernel's register count and raises its dynamic shared memory
+// limit, once per device.  Idempotent and safe to call from several host
+// threads: a flag is only set after both succeeded, and a repeated call is
+// harmless.
+inline cudaError_t ensure_smem_limit(const void* kernel, int bytes, int launch_regs,
+                                     std::atomic<int>* done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const bool cached = dev >= 0 && dev < kMaxDevices;
   if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  // The kernels split the block's registers between warpgroups with
+  // setmaxnreg, which assumes the block was launched with exactly
+  // `launch_regs` per thread; refuse to launch a build that differs.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != launch_regs) return cudaErrorInvalidKernelImage;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && cached) done[dev].store(1, std::memory_order_release);
   return e;

@@ -289,9 +289,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // Per-warpgroup register budget (all four warps of the warpgroup execute it).
-// The block is launched with 168 registers x 384 threads = 64512; the
-// producer/MMA warpgroup releases down to 80 and the two compute warpgroups
-// grow to 208: 128*80 + 256*208 = 63488 <= 64512.
+// The budget is drawn from the registers the block was launched with; each
+// kernel checks its split against that total.  The forward: 168 registers x
+// 384 threads = 64512; the producer/MMA warpgroup releases down to 80 and the
+// two softmax warpgroups grow to 208: 128*80 + 256*208 = 63488 <= 64512.
 template <int N>
 __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
