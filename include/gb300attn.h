@@ -49,7 +49,7 @@ typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t; NULL = legacy def
 enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or flag; nothing launched */
-  ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64,128}) */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64,128,256}) */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
   ATTN_ERR_TIMEOUT = 4      /* a device-side bounded wait gave up (see attn_read_device_status) */
 };
@@ -65,7 +65,8 @@ enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
  *  q, k, v        bf16, layouts above; 16-byte aligned base pointers.
  *  q_segment_ids, q_segment_pos    int32 [b, s_q]
  *  kv_segment_ids, kv_segment_pos  int32 [b, s_kv]  (may alias the q ones)
- *  b, s_q, s_kv, h_q, h_kv, d      sizes; h_q % h_kv == 0; d in {64, 128};
+ *  b, s_q, s_kv, h_q, h_kv, d      sizes; h_q % h_kv == 0; d in {64, 128, 256}
+ *                                  (attn_bwd: d in {64, 128});
  *                                  s_q, s_kv >= 1 (ragged lengths allowed)
  *  window_left    -1 = unlimited, else >= 0 (inclusive, W+1 keys incl. self)
  *  window_right   must be 0 (causal)
@@ -152,7 +153,10 @@ GB300ATTN_API size_t attn_bwd_workspace_bytes(const attn_bwd_params* p);
 /* Forward attention (tile plan + fused tcgen05 kernel).  See attn_fwd_params. */
 GB300ATTN_API int attn_fwd(const attn_fwd_params* p, attn_stream_t stream);
 
-/* Backward attention: D = rowsum(dO*O), fused dQ/dK/dV kernel, dQ finalise. */
+/* Backward attention: D = rowsum(dO*O), fused dQ/dK/dV kernel, dQ finalise.
+ * d must be 64 or 128: at d = 256 a 128-key tile's dK and dV alone would fill
+ * the 512 TMEM columns of a CTA, so d = 256 returns ATTN_ERR_UNSUPPORTED
+ * before any launch. */
 GB300ATTN_API int attn_bwd(const attn_bwd_params* p, attn_stream_t stream);
 
 /* Online-softmax merge of a partial result into an accumulator, per row-head.

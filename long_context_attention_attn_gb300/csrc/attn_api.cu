@@ -42,7 +42,7 @@ int check_fwd(const attn_fwd_params* p) {
   if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;
   if (p->s_q > (1ll << 30) || p->s_kv > (1ll << 30) || p->h_q > 65535 || p->b > 65535)
     return ATTN_ERR_UNSUPPORTED;
-  if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->d != 64 && p->d != 128 && p->d != 256) return ATTN_ERR_UNSUPPORTED;
   if (!aligned(p->q, 16) || !aligned(p->k, 16) || !aligned(p->v, 16) || !aligned(p->out, 16) ||
       !aligned(p->lse, 4) || !aligned(p->q_segment_ids, 4) || !aligned(p->q_segment_pos, 4) ||
       !aligned(p->kv_segment_ids, 4) || !aligned(p->kv_segment_pos, 4))
@@ -61,7 +61,8 @@ int check_fwd(const attn_fwd_params* p) {
     if (o0 < f0 + 2 * n && f0 < o0 + 4 * n) return ATTN_ERR_INVALID_ARG;  // overlap
   }
   const int64_t g = p->h_q / p->h_kv;
-  const int64_t units = p->b * cdiv(p->s_q, kTile) * p->h_kv * ((g + 1) / 2);
+  const int64_t slots = p->d <= 128 ? 2 : 1;  // query heads per forward CTA
+  const int64_t units = p->b * cdiv(p->s_q, kTile) * p->h_kv * ((g + slots - 1) / slots);
   if (units > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
@@ -185,6 +186,8 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   int rc = check_fwd(&p->fwd);
   if (rc != ATTN_OK) return rc;
   if (p->fwd.out_fp32 || p->fwd.merge_into_out || p->fwd.out_final) return ATTN_ERR_INVALID_ARG;
+  // d = 256: dK and dV of a 128-key tile alone would fill the 512 TMEM columns
+  if (p->fwd.d > 128) return ATTN_ERR_UNSUPPORTED;
   if (!p->dout || !p->dq || !p->dk || !p->dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned(p->dout, 16) || !aligned(p->dq, 16) || !aligned(p->dk, 16) || !aligned(p->dv, 16))
     return ATTN_ERR_INVALID_ARG;

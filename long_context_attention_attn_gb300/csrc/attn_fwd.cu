@@ -39,7 +39,11 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = kFwdKeyTile;  // keys per tile (half of the plan's 128-key tile)
-constexpr int NST = 8;   // K/V shared-memory slots (K and V tiles alternate)
+constexpr int NST = 8;   // K/V shared-memory slots (K and V tiles alternate), d <= 128
+// Query heads per CTA and K/V slots by head dim: d = 256 takes one head slot
+// (its O accumulator fills TMEM columns [256, 512)) and four 32 KB slots.
+template <int D> constexpr int kSlots = D <= 128 ? 2 : 1;
+template <int D> constexpr int kNst = D <= 128 ? NST : 4;
 constexpr int NID = 4;   // ids/pos ring entries
 constexpr int kThreads = 384;
 // Registers per thread at launch (65536 / 384, rounded down to a multiple of 8).
@@ -79,9 +83,9 @@ struct Layout {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = BM * D * 2;       // a Q tile
   static constexpr int kKVBytes = BN * D * 2;         // a K or V tile
-  static constexpr int q_off = 0;                     // 2 Q tiles
-  static constexpr int kv_off = q_off + 2 * kTileBytes;
-  static constexpr int id_off = kv_off + NST * kKVBytes;  // NID x kIdEntry ints
+  static constexpr int q_off = 0;                     // kSlots Q tiles
+  static constexpr int kv_off = q_off + kSlots<D> * kTileBytes;
+  static constexpr int id_off = kv_off + kNst<D> * kKVBytes;  // NID x kIdEntry ints
   static constexpr int bar_off = id_off + NID * kIdEntry * 4;
   static constexpr int bytes = bar_off + 512;
   // + slack for 1024-byte alignment; at least 150 KB so that one CTA (which
@@ -130,15 +134,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int e = a.order[rank];
   const int bi = e / a.nq;
   const int qt = e % a.nq;
-  const int h0 = kvh * a.g + 2 * pair;
-  const int nslots = (2 * pair + 1 < a.g) ? 2 : 1;
+  const int h0 = kvh * a.g + kSlots<D> * pair;
+  const int nslots = min(kSlots<D>, a.g - kSlots<D> * pair);
+  constexpr int NSTD = kNst<D>;
+  static_assert(4 * BN + kSlots<D> * D <= 512, "TMEM columns");
   const int2 rng = a.qrange[e];
   const int nt = 2 * a.qweight[e];  // 64-key tiles of the non-SKIP 128-key plan tiles
   const uint8_t* cls_row = a.cls + (size_t)e * a.nk;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < NST; ++i) {
+    for (int i = 0; i < NSTD; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 4 * nslots);  // one arrival per softmax warp
     }
@@ -185,15 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                       c * 64, h0 + sl, qt * BM, bi, &bars->q_full);
     }
     int n = 0;
-    int last_use[NST];
-    for (int i = 0; i < NST; ++i) last_use[i] = -1;
+    int last_use[NSTD];
+    for (int i = 0; i < NSTD; ++i) last_use[i] = -1;
     bool ok = true;
     for (int j2 = 2 * rng.x; j2 <= 2 * rng.y + 1 && ok && !a.withhold_kv; ++j2) {
       if (cls_row[j2 >> 1] == kSkip) continue;
       // K tile, then V tile of 64-key tile j2
 #pragma unroll 1
       for (int kv = 0; kv < 2 && ok; ++kv) {
-        const int ld = 2 * n + kv, slot = ld % NST, use = ld / NST;
+        const int ld = 2 * n + kv, slot = ld % NSTD, use = ld / NSTD;
         if (lane == 0) {
           ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
           if (ok) {
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (already true on the normal path; bounded after an abort).
     if (lane == 0) {
       mbar_wait_drain(&bars->q_full, 0, a.status);
-      for (int i = 0; i < NST; ++i)
+      for (int i = 0; i < NSTD; ++i)
         if (last_use[i] >= 0) mbar_wait_drain(&bars->kv_full[i], last_use[i] & 1, a.status);
     }
   } else if (warp == 1 || warp == 3) {
@@ -239,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = -2; n < nt && ok; ++n) {
         if (n >= 0) {
           // O_sl += P_sl(n) V(n): needs V(n) and the softmax of tile n
-          const int ldv = 2 * n + 1, slot_v = ldv % NST;
-          ok = mbar_wait(&bars->kv_full[slot_v], (ldv / NST) & 1, ctx);
+          const int ldv = 2 * n + 1, slot_v = ldv % NSTD;
+          ok = mbar_wait(&bars->kv_full[slot_v], (ldv / NSTD) & 1, ctx);
           if (ok) ok = mbar_wait(&bars->p_full[sl][n & 1], (n >> 1) & 1, ctx);
           if (!ok) break;
           tc_fence_after();
@@ -257,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (m2 < nt) {
           // S_sl(m2) = Q_sl K(m2)^T into buffer m2 & 1: needs K(m2), and PV(n)
           // done (P(n) lives in that buffer)
-          const int ldk = 2 * m2, slot_k = ldk % NST;
-          ok = mbar_wait(&bars->kv_full[slot_k], (ldk / NST) & 1, ctx);
+          const int ldk = 2 * m2, slot_k = ldk % NSTD;
+          ok = mbar_wait(&bars->kv_full[slot_k], (ldk / NSTD) & 1, ctx);
           if (ok && n >= 0) ok = mbar_wait(&bars->o_done[sl][n & 1], (n >> 1) & 1, ctx);
           if (!ok) break;
           tc_fence_after();
@@ -342,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_sl(n) is complete, so this slot is done with K(n) and (its S(n) was
         // issued after PV_sl(n-2) completed) with V(n-2): release both slots.
         if (lane == 0) {
-          mbar_arrive(&bars->kv_empty[(2 * n) % NST]);
-          if (n > 1) mbar_arrive(&bars->kv_empty[(2 * n - 3) % NST]);
+          mbar_arrive(&bars->kv_empty[(2 * n) % NSTD]);
+          if (n > 1) mbar_arrive(&bars->kv_empty[(2 * n - 3) % NSTD]);
         }
         const uint32_t t_s = t_s0 + (n & 1) * BN;
         uint32_t sr[BN];
@@ -526,6 +532,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, const FwdLaunch& Lc, int64_t units, cudaStream_t st) {
+  const int smem = Layout<D>::alloc;
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<D>), smem,
+                                    kLaunchRegs, smem_set);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<D><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
@@ -549,7 +566,8 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   a.hq = (int)p.h_q;
   a.hkv = (int)p.h_kv;
   a.g = (int)(p.h_q / p.h_kv);
-  a.npairs = (a.g + 1) / 2;
+  const int slots = p.d <= 128 ? 2 : 1;  // query heads per CTA
+  a.npairs = (a.g + slots - 1) / slots;
   a.nq = (int)Lc.nq;
   a.nk = (int)Lc.nk;
   a.window = p.window_left;
@@ -559,24 +577,9 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   a.scale_log2 = p.scale * 1.4426950408889634f;
   const int64_t units = p.b * Lc.nq * p.h_kv * a.npairs;
   if (units == 0) return cudaSuccess;
-  if (p.d == 128) {
-    const int smem = Layout<128>::alloc;
-    static std::atomic<int> smem_set[kMaxDevices];
-    cudaError_t e =
-        ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<128>), smem,
-                          kLaunchRegs, smem_set);
-    if (e != cudaSuccess) return e;
-    attn_fwd_kernel<128><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
-  } else {
-    const int smem = Layout<64>::alloc;
-    static std::atomic<int> smem_set[kMaxDevices];
-    cudaError_t e =
-        ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<64>), smem,
-                          kLaunchRegs, smem_set);
-    if (e != cudaSuccess) return e;
-    attn_fwd_kernel<64><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
-  }
-  return cudaGetLastError();
+  if (p.d == 128) return launch_fwd_d<128>(a, Lc, units, st);
+  if (p.d == 256) return launch_fwd_d<256>(a, Lc, units, st);
+  return launch_fwd_d<64>(a, Lc, units, st);
 }
 
 }  // namespace gb300

@@ -53,7 +53,7 @@ def _params(ga, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(d=96), 2), (dict(d=256), 2), (dict(window_right=1), 1), (dict(window_left=-2), 1),
+    (dict(d=96), 2), (dict(d=192), 2), (dict(window_right=1), 1), (dict(window_left=-2), 1),
     (dict(h_kv=3), 1), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(b=0), 1),
     (dict(s_q=0), 1), (dict(q=None), 1), (dict(q=(1 << 20) + 8), 1), (dict(lse=None), 1),
     (dict(merge_into_out=1), 1),                          # merge mode needs fp32 out
@@ -93,6 +93,11 @@ def test_bwd_rejects_invalid_arguments_on_host(ga):
     bp.fwd.merge_into_out = 1
     assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
     bp.fwd.merge_into_out = 0
+    # the forward takes d = 256, the backward does not (its dK and dV alone
+    # would fill the tensor memory of a CTA)
+    bp.fwd.d, bp.fwd.kv_token_stride = 256, 0
+    bp.fwd.workspace_bytes = 1 << 30
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 2
     bp.fwd.d = 80
     assert ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp)) == 0
 

@@ -56,6 +56,9 @@ def test_tiny_workload(ga):
     (1, 384, 2, 2, 128, -1, 3),     # g = 1 (plain MHA)
     (2, 517, 8, 2, 64, 0, 4),       # window 0: each token sees only itself
     (1, 1024, 2, 1, 128, 300, 5),
+    (2, 300, 4, 2, 256, 70, 6),     # d = 256 (one head per CTA), ragged tail
+    (1, 520, 3, 1, 256, -1, 7),     # d = 256, odd group size
+    (1, 1000, 2, 2, 256, 0, 8),     # d = 256, window 0
 ])
 def test_random_packing(ga, b, s, hq, hkv, d, window, seed):
     q, k, v = workload.qkv(b, s, hq, hkv, d, seed=seed)
@@ -63,10 +66,23 @@ def test_random_packing(ga, b, s, hq, hkv, d, window, seed):
     _full_check(ga, q, k, v, ids, pos, window, d ** -0.5)
 
 
-def test_fp32_output(ga):
-    q, k, v = workload.qkv(1, 256, 2, 1, 128, seed=9)
+@pytest.mark.parametrize("d", [128, 256])
+def test_fp32_output(ga, d):
+    q, k, v = workload.qkv(1, 256, 2, 1, d, seed=9)
     ids, pos = workload.segments(1, 256, 2)
     _full_check(ga, q, k, v, ids, pos, -1, 0.1, out_fp32=True)
+
+
+def test_d256_backward_is_rejected(ga):
+    """The backward takes d = 64 and 128 only: a d = 256 call fails loudly
+    before any launch."""
+    q, k, v, dout = workload.qkv(1, 256, 2, 1, 256, seed=10, with_dout=True)
+    ids, pos = workload.segments(1, 256, 1)
+    g = {n: t.to(DEV) for n, t in dict(q=q, k=k, v=v, dout=dout, ids=ids, pos=pos).items()}
+    out, lse = ga.attn_fwd(g["q"], g["k"], g["v"], g["ids"], g["pos"], scale=256 ** -0.5)
+    with pytest.raises(RuntimeError):
+        ga.attn_bwd(g["q"], g["k"], g["v"], out, lse, g["dout"], g["ids"], g["pos"],
+                    scale=256 ** -0.5)
 
 
 def test_cross_descriptor_and_lengths(ga):
