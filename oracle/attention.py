@@ -103,10 +103,11 @@ def attn_fwd(q, k, v, ids_q, pos_q, ids_kv, pos_kv, window_left, scale,
     ids_q, pos_q, ids_kv, pos_kv = map(_i64, (ids_q, pos_q, ids_kv, pos_kv))
     b, s_q, hq, d = q.shape
     hkv = k.shape[2]
+    dv = v.shape[3]  # O takes V's width; d is the q.k contraction width only
     if hq % hkv:
         raise ValueError("Hq must be a multiple of Hkv")
     g = hq // hkv
-    out = np.zeros((b, s_q, hq, d))
+    out = np.zeros((b, s_q, hq, dv))
     lse = np.full((b, hq, s_q), -np.inf)
     batches = range(b) if batches is None else batches
     heads = range(hq) if heads is None else heads

@@ -11,14 +11,16 @@ import math
 
 
 def attn_fwd(q, k, v, ids_q, pos_q, ids_kv, pos_kv, window_left, scale):
-    """q: nested lists [b][s_q][Hq][d]; k, v: [b][s_kv][Hkv][d]; ids/pos [b][s].
+    """q, k: nested lists [b][s][H][d]; v: [b][s_kv][Hkv][d_v]; ids/pos [b][s].
 
-    Returns out [b][s_q][Hq][d] and lse [b][Hq][s_q] as nested lists.
+    Returns out [b][s_q][Hq][d_v] and lse [b][Hq][s_q] as nested lists (the
+    output has the width of V; d is only the width of the q.k dot product).
     """
     b, s_q, hq, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
     s_kv, hkv = len(k[0]), len(k[0][0])
+    dv = len(v[0][0][0])
     g = hq // hkv
-    out = [[[[0.0] * d for _ in range(hq)] for _ in range(s_q)] for _ in range(b)]
+    out = [[[[0.0] * dv for _ in range(hq)] for _ in range(s_q)] for _ in range(b)]
     lse = [[[-math.inf] * s_q for _ in range(hq)] for _ in range(b)]
     for bi in range(b):
         for h in range(hq):
@@ -39,7 +41,7 @@ def attn_fwd(q, k, v, ids_q, pos_q, ids_kv, pos_kv, window_left, scale):
                 big = max(sv for _, sv in scores)
                 weights = [(j, math.exp(sv - big)) for j, sv in scores]
                 denom = math.fsum(w for _, w in weights)
-                for c in range(d):
+                for c in range(dv):
                     out[bi][i][h][c] = math.fsum(w * v[bi][j][kh][c] for j, w in weights) / denom
                 lse[bi][h][i] = big + math.log(denom)
     return out, lse

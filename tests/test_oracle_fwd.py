@@ -22,8 +22,8 @@ def _nested(x):
     return x.to(torch.float64).tolist()
 
 
-def _small(seed, b=1, s=40, hq=4, hkv=2, d=8, slots=None, random_pack=False):
-    q, k, v = workload.qkv(b, s, hq, hkv, d, seed=seed)
+def _small(seed, b=1, s=40, hq=4, hkv=2, d=8, slots=None, random_pack=False, dv=None):
+    q, k, v = workload.qkv(b, s, hq, hkv, d, seed=seed, dv=dv)
     if random_pack:
         ids, pos = workload.random_segments(b, s, seed=seed)
     else:
@@ -46,6 +46,29 @@ def test_blocked_matches_brute_force(seed, window, random_pack, slots):
     assert np.array_equal(np.isinf(lse), np.isinf(bl))
     fin = np.isfinite(bl)
     np.testing.assert_allclose(lse[fin], bl[fin], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("d,dv,window", [(12, 8, -1), (6, 10, 4)])
+def test_value_width_differs_from_qk_width(d, dv, window):
+    """O takes V's head dim (MLA-style d_qk != d_v): brute force and the
+    library SDPA, which both take V's width as given."""
+    q, k, v, ids, pos = _small(21 + d, b=2, s=36, d=d, dv=dv, random_pack=True)
+    scale = d ** -0.5
+    out, lse = A.attn_fwd(q, k, v, ids, pos, ids, pos, window, scale)
+    assert out.shape == (2, 36, 4, dv)
+    bo, bl = brute.attn_fwd(_nested(q), _nested(k), _nested(v), ids.tolist(), pos.tolist(),
+                            ids.tolist(), pos.tolist(), window, scale)
+    np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
+    for bi in range(2):
+        mask = torch.from_numpy(A.visible(ids[bi].numpy(), pos[bi].numpy(),
+                                          ids[bi].numpy(), pos[bi].numpy(), window))
+        qq = q[bi].to(torch.float64).permute(1, 0, 2)
+        kk = k[bi].to(torch.float64).repeat_interleave(2, dim=1).permute(1, 0, 2)
+        vv = v[bi].to(torch.float64).repeat_interleave(2, dim=1).permute(1, 0, 2)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qq, kk, vv, attn_mask=mask[None], scale=scale).permute(1, 0, 2).numpy()
+        rows = mask.any(dim=1).numpy()
+        np.testing.assert_allclose(out[bi][rows], ref[rows], rtol=0, atol=1e-12)
 
 
 def test_tiny_workload_matches_brute_force_one_group():

@@ -81,14 +81,17 @@ def segments(b: int, s: int, slots: Optional[int]):
 
 
 def qkv(b: int, s: int, hq: int, hkv: int, d: int, *, seed: int = SEED,
-        with_dout: bool = False, device="cpu", s_kv: Optional[int] = None):
-    """bf16 q [b,s,hq,d], k/v [b,s_kv,hkv,d] (and dout [b,s,hq,d]), seeded.
+        with_dout: bool = False, device="cpu", s_kv: Optional[int] = None,
+        dv: Optional[int] = None):
+    """bf16 q [b,s,hq,d], k [b,s_kv,hkv,d], v [b,s_kv,hkv,dv] (and dout
+    [b,s,hq,dv]), seeded; dv defaults to d.
 
     Drawn float32 N(0,1) in the order q, k, v, dout and rounded to bf16.
     A CUDA device uses its own seeded generator (values differ from the CPU
     stream, the distribution is the same).
     """
     s_kv = s if s_kv is None else s_kv
+    dv = d if dv is None else dv
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
 
@@ -98,9 +101,9 @@ def qkv(b: int, s: int, hq: int, hkv: int, d: int, *, seed: int = SEED,
 
     q = draw((b, s, hq, d))
     k = draw((b, s_kv, hkv, d))
-    v = draw((b, s_kv, hkv, d))
+    v = draw((b, s_kv, hkv, dv))
     if with_dout:
-        return q, k, v, draw((b, s, hq, d))
+        return q, k, v, draw((b, s, hq, dv))
     return q, k, v
 
 
