@@ -66,12 +66,14 @@ enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
  *  q_segment_ids, q_segment_pos    int32 [b, s_q]
  *  kv_segment_ids, kv_segment_pos  int32 [b, s_kv]  (may alias the q ones)
  *  b, s_q, s_kv, h_q, h_kv, d      sizes; h_q % h_kv == 0; d in {64, 128, 256}
- *                                  (attn_bwd: d in {64, 128});
+ *                                  (attn_bwd: d in {64, 128}); d is the head
+ *                                  dim of q and k, and of v unless d_v says
+ *                                  otherwise;
  *                                  s_q, s_kv >= 1 (ragged lengths allowed)
  *  window_left    -1 = unlimited, else >= 0 (inclusive, W+1 keys incl. self)
  *  window_right   must be 0 (causal)
  *  scale          softmax scale, usually 1/sqrt(d)
- *  out            bf16 [b, s_q, h_q, d], or fp32 when out_fp32 != 0
+ *  out            bf16 [b, s_q, h_q, d_v], or fp32 when out_fp32 != 0
  *  lse            fp32 [b, h_q, s_q]
  *  workspace      device scratch of at least attn_fwd_workspace_bytes() bytes,
  *                 256-byte aligned; contents need no initialisation and are
@@ -86,7 +88,7 @@ enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
  *                 no separate merge pass over HBM.  lse is updated; out is
  *                 updated unless out_final is given.  A row whose LSE_acc is
  *                 -inf takes the block as is (its out value is ignored).
- *  out_final      NULL, or (merge_into_out only) bf16 [b, s_q, h_q, d]: the
+ *  out_final      NULL, or (merge_into_out only) bf16 [b, s_q, h_q, d_v]: the
  *                 merged O goes there, rounded to bf16 (RNE), instead of into
  *                 out (the last ring step).  Must not overlap out.
  *  kv_token_stride  elements between consecutive tokens of k and of v (and of
@@ -95,6 +97,11 @@ enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
  *                 kv [b, s_kv, 2, h_kv, d]) is k = kv, v = kv + h_kv * d,
  *                 kv_token_stride = 2 * h_kv * d.  Must be >= h_kv * d and a
  *                 multiple of 8; batch rows are s_kv * kv_token_stride apart.
+ *                 Must be 0 when d_v differs from d.
+ *  d_v            head dim of v and out; 0 = d.  Other than d, only d = 192
+ *                 with d_v = 128 (the MLA shape the TE tutorial's closing
+ *                 section points to), forward only: v is then bf16
+ *                 [b, s_kv, h_kv, 128], contiguous.  attn_bwd requires 0 or d.
  */
 typedef struct attn_fwd_params {
   const void* q;
@@ -116,6 +123,7 @@ typedef struct attn_fwd_params {
   int32_t merge_into_out;
   void* out_final;
   int64_t kv_token_stride;
+  int64_t d_v;
 } attn_fwd_params;
 
 /* Backward parameters: gradient of sum(out * dout) with respect to q, k, v

@@ -47,7 +47,7 @@ class FwdParams(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("merge_into_out", ctypes.c_int32), ("out_final", ctypes.c_void_p),
-        ("kv_token_stride", ctypes.c_int64),
+        ("kv_token_stride", ctypes.c_int64), ("d_v", ctypes.c_int64),
     ]
 
 
@@ -154,6 +154,7 @@ def _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, 
     p.q_segment_ids, p.q_segment_pos = q_ids.data_ptr(), q_pos.data_ptr()
     p.kv_segment_ids, p.kv_segment_pos = kv_ids.data_ptr(), kv_pos.data_ptr()
     p.b, p.s_q, p.s_kv, p.h_q, p.h_kv, p.d = b, s_q, s_kv, hq, hkv, d
+    p.d_v = v.shape[3] if v.shape[3] != d else 0  # 0: V has the head dim of q and k
     p.window_left, p.window_right = int(window_left), 0
     p.scale = float(d ** -0.5 if scale is None else scale)
     p.out_fp32 = 1 if out_fp32 else 0
@@ -178,9 +179,10 @@ def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: in
              scale: Optional[float] = None, out=None, lse=None, out_fp32: bool = False,
              merge_into_out: bool = False, out_final=None,
              workspace: Optional[torch.Tensor] = None):
-    """Forward attention.  Returns (out [b,s_q,Hq,d], lse fp32 [b,Hq,s_q]).
+    """Forward attention.  Returns (out [b,s_q,Hq,d_v], lse fp32 [b,Hq,s_q]).
 
-    q bf16 [b,s_q,Hq,d]; k, v bf16 [b,s_kv,Hkv,d]; ids/pos int32 [b,s].
+    q bf16 [b,s_q,Hq,d]; k bf16 [b,s_kv,Hkv,d]; v bf16 [b,s_kv,Hkv,d_v] (d_v = d,
+    or d = 192 with d_v = 128); ids/pos int32 [b,s].
     kv_ids / kv_pos default to the query descriptor (self-attention).
     With ``merge_into_out`` the given fp32 ``out`` / ``lse`` hold a finished
     partial over other key blocks and this call's result is merged into them
@@ -189,10 +191,17 @@ def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: in
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
     _need_cuda(q, q_ids, q_pos, kv_ids, kv_pos, out, lse, workspace, out_final)
-    kv_stride = _kv_token_stride(k, v)
+    if v.shape[3] != k.shape[3]:
+        # V narrower or wider than Q / K (d_qk != d_v): separate, contiguous tensors
+        if not (k.is_contiguous() and v.is_contiguous()) or v.shape[:3] != k.shape[:3]:
+            raise ValueError("k / v of different head dims must be contiguous [b, s, h, d]")
+        kv_stride = 0
+    else:
+        kv_stride = _kv_token_stride(k, v)
     if merge_into_out and (out is None or lse is None or not out_fp32):
         raise ValueError("merge_into_out needs the fp32 out and lse accumulators")
-    b, s_q, hq, d = q.shape
+    b, s_q, hq, _ = q.shape
+    d = v.shape[3]  # the output has V's head dim
     if out is None:
         out = torch.empty(b, s_q, hq, d, device=q.device,
                           dtype=torch.float32 if out_fp32 else torch.bfloat16)

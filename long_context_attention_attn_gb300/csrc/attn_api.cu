@@ -29,6 +29,9 @@ bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % 
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Head dim of v and out (d_v = 0 means d).
+int64_t fwd_dv(const attn_fwd_params* p) { return p->d_v > 0 ? p->d_v : p->d; }
+
 // Shared checks of the forward problem description.
 int check_fwd(const attn_fwd_params* p) {
   if (!p) return ATTN_ERR_INVALID_ARG;
@@ -42,7 +45,12 @@ int check_fwd(const attn_fwd_params* p) {
   if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;
   if (p->s_q > (1ll << 30) || p->s_kv > (1ll << 30) || p->h_q > 65535 || p->b > 65535)
     return ATTN_ERR_UNSUPPORTED;
-  if (p->d != 64 && p->d != 128 && p->d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (p->d_v < 0) return ATTN_ERR_INVALID_ARG;
+  const int64_t dv = fwd_dv(p);
+  // head dims (q/k, v): (64, 64), (128, 128), (256, 256), (192, 128)
+  if (!((dv == p->d && (p->d == 64 || p->d == 128 || p->d == 256)) || (p->d == 192 && dv == 128)))
+    return ATTN_ERR_UNSUPPORTED;
+  if (dv != p->d && p->kv_token_stride != 0) return ATTN_ERR_INVALID_ARG;
   if (!aligned(p->q, 16) || !aligned(p->k, 16) || !aligned(p->v, 16) || !aligned(p->out, 16) ||
       !aligned(p->lse, 4) || !aligned(p->q_segment_ids, 4) || !aligned(p->q_segment_pos, 4) ||
       !aligned(p->kv_segment_ids, 4) || !aligned(p->kv_segment_pos, 4))
@@ -57,11 +65,11 @@ int check_fwd(const attn_fwd_params* p) {
     if (!p->merge_into_out || !aligned(p->out_final, 16)) return ATTN_ERR_INVALID_ARG;
     const uintptr_t o0 = reinterpret_cast<uintptr_t>(p->out);
     const uintptr_t f0 = reinterpret_cast<uintptr_t>(p->out_final);
-    const uintptr_t n = (uintptr_t)(p->b * p->s_q * p->h_q * p->d);
+    const uintptr_t n = (uintptr_t)(p->b * p->s_q * p->h_q * dv);
     if (o0 < f0 + 2 * n && f0 < o0 + 4 * n) return ATTN_ERR_INVALID_ARG;  // overlap
   }
   const int64_t g = p->h_q / p->h_kv;
-  const int64_t slots = p->d <= 128 ? 2 : 1;  // query heads per forward CTA
+  const int64_t slots = dv <= 128 ? 2 : 1;  // query heads per forward CTA
   const int64_t units = p->b * cdiv(p->s_q, kTile) * p->h_kv * ((g + slots - 1) / slots);
   if (units > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
@@ -137,7 +145,7 @@ static int fwd_impl(const attn_fwd_params* p, attn_stream_t stream, bool withhol
   if (!encode_qkv_map(&fl.tm_q, p->q, p->b, p->s_q, p->h_q, p->d, 0) ||
       !encode_qkv_map(&fl.tm_k, p->k, p->b, p->s_kv, p->h_kv, p->d, p->kv_token_stride,
                       kFwdKeyTile) ||
-      !encode_qkv_map(&fl.tm_v, p->v, p->b, p->s_kv, p->h_kv, p->d, p->kv_token_stride,
+      !encode_qkv_map(&fl.tm_v, p->v, p->b, p->s_kv, p->h_kv, fwd_dv(p), p->kv_token_stride,
                       kFwdKeyTile))
     return ATTN_ERR_CUDA;
   cudaError_t e = cudaMemsetAsync(fl.plan.status, 0, sizeof(int), st);
@@ -187,7 +195,7 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   if (rc != ATTN_OK) return rc;
   if (p->fwd.out_fp32 || p->fwd.merge_into_out || p->fwd.out_final) return ATTN_ERR_INVALID_ARG;
   // d = 256: dK and dV of a 128-key tile alone would fill the 512 TMEM columns
-  if (p->fwd.d > 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->fwd.d > 128 || fwd_dv(&p->fwd) != p->fwd.d) return ATTN_ERR_UNSUPPORTED;
   if (!p->dout || !p->dq || !p->dk || !p->dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned(p->dout, 16) || !aligned(p->dq, 16) || !aligned(p->dk, 16) || !aligned(p->dv, 16))
     return ATTN_ERR_INVALID_ARG;

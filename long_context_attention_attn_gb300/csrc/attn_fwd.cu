@@ -17,7 +17,9 @@
 //   warps 8-11    softmax for head slot 1
 // TMEM (512 columns x 128 lanes, lane = query row):
 //   slot 0 S buffers [0,64) [64,128), slot 1 [128,192) [192,256),
-//   O0 [256,256+D)  O1 [256+D, 256+2D)
+//   O0 [256,256+d_v)  O1 [256+d_v, 256+2d_v)
+// (head dims: q / k and v / out both 64, 128 or 256, or 192 / 128; at d_v = 256
+// a CTA takes one head slot, whose O fills columns [256, 512))
 // Key tile n's scores go to buffer n & 1 of the slot, so S(n+1) is computed
 // while the softmax works on tile n.  P (bf16, 2 per column) overwrites the
 // first 32 columns of its S buffer and is the A operand of the P.V MMA
@@ -40,10 +42,11 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = kFwdKeyTile;  // keys per tile (half of the plan's 128-key tile)
 constexpr int NST = 8;   // K/V shared-memory slots (K and V tiles alternate), d <= 128
-// Query heads per CTA and K/V slots by head dim: d = 256 takes one head slot
-// (its O accumulator fills TMEM columns [256, 512)) and four 32 KB slots.
-template <int D> constexpr int kSlots = D <= 128 ? 2 : 1;
-template <int D> constexpr int kNst = D <= 128 ? NST : 4;
+// Query heads per CTA and K/V slots by head dims (DK of q / k, DV of v / out):
+// DV = 256 takes one head slot (its O accumulator fills TMEM columns
+// [256, 512)) and four 32 KB slots; DK = 192 (DV = 128) five 24 KB slots.
+template <int DK, int DV> constexpr int kSlots = DV <= 128 ? 2 : 1;
+template <int DK, int DV> constexpr int kNst = DK <= 128 ? NST : (DK == 192 ? 5 : 4);
 constexpr int NID = 4;   // ids/pos ring entries
 constexpr int kThreads = 384;
 // Registers per thread at launch (65536 / 384, rounded down to a multiple of 8).
@@ -76,16 +79,19 @@ struct FwdArgs {
   float scale_log2;
 };
 
-template <int D>
+template <int DK, int DV>
 struct Layout {
   static constexpr int kChunk = BM * 128;             // one 64-wide bf16 chunk of a Q tile
   static constexpr int kChunkKV = BN * 128;           // one 64-wide bf16 chunk of a K / V tile
-  static constexpr int kChunks = D / 64;
-  static constexpr int kTileBytes = BM * D * 2;       // a Q tile
-  static constexpr int kKVBytes = BN * D * 2;         // a K or V tile
+  static constexpr int kChunksK = DK / 64;            // chunks of a Q or K tile
+  static constexpr int kChunksV = DV / 64;            // chunks of a V tile
+  static constexpr int kTileBytes = BM * DK * 2;      // a Q tile
+  static constexpr int kKBytes = BN * DK * 2;         // a K tile
+  static constexpr int kVBytes = BN * DV * 2;         // a V tile
+  static constexpr int kKVBytes = kKBytes > kVBytes ? kKBytes : kVBytes;  // a K / V slot
   static constexpr int q_off = 0;                     // kSlots Q tiles
-  static constexpr int kv_off = q_off + kSlots<D> * kTileBytes;
-  static constexpr int id_off = kv_off + kNst<D> * kKVBytes;  // NID x kIdEntry ints
+  static constexpr int kv_off = q_off + kSlots<DK, DV> * kTileBytes;
+  static constexpr int id_off = kv_off + kNst<DK, DV> * kKVBytes;  // NID x kIdEntry ints
   static constexpr int bar_off = id_off + NID * kIdEntry * 4;
   static constexpr int bytes = bar_off + 512;
   // + slack for 1024-byte alignment; at least 150 KB so that one CTA (which
@@ -109,11 +115,11 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
-template <int D>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  using L = Layout<D>;
+  using L = Layout<DK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -134,10 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int e = a.order[rank];
   const int bi = e / a.nq;
   const int qt = e % a.nq;
-  const int h0 = kvh * a.g + kSlots<D> * pair;
-  const int nslots = min(kSlots<D>, a.g - kSlots<D> * pair);
-  constexpr int NSTD = kNst<D>;
-  static_assert(4 * BN + kSlots<D> * D <= 512, "TMEM columns");
+  const int h0 = kvh * a.g + kSlots<DK, DV> * pair;
+  const int nslots = min(kSlots<DK, DV>, a.g - kSlots<DK, DV> * pair);
+  constexpr int NSTD = kNst<DK, DV>;
+  static_assert(4 * BN + kSlots<DK, DV> * DV <= 512, "TMEM columns");
+  static_assert(Layout<DK, DV>::alloc <= 232448, "shared memory per block");
   const int2 rng = a.qrange[e];
   const int nt = 2 * a.qweight[e];  // 64-key tiles of the non-SKIP 128-key plan tiles
   const uint8_t* cls_row = a.cls + (size_t)e * a.nk;
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&bars->q_full, nslots * L::kTileBytes);
       for (int sl = 0; sl < nslots; ++sl)
-        for (int c = 0; c < L::kChunks; ++c)
+        for (int c = 0; c < L::kChunksK; ++c)
           tma_load_4d(smem_u32(smem + L::q_off + sl * L::kTileBytes + c * L::kChunk), &tm_q,
                       c * 64, h0 + sl, qt * BM, bi, &bars->q_full);
     }
@@ -203,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
           if (ok) {
-            mbar_arrive_expect_tx(&bars->kv_full[slot], L::kKVBytes);
-            for (int c = 0; c < L::kChunks; ++c)
+            mbar_arrive_expect_tx(&bars->kv_full[slot], kv == 0 ? L::kKBytes : L::kVBytes);
+            for (int c = 0; c < (kv == 0 ? L::kChunksK : L::kChunksV); ++c)
               tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kKVBytes + c * L::kChunkKV),
                           kv == 0 ? &tm_k : &tm_v, c * 64, kvh, j2 * BN, bi, &bars->kv_full[slot]);
             last_use[slot] = use;
@@ -230,13 +237,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sl = warp == 1 ? 0 : 1;
     if (lane == 0 && sl < nslots) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(BM, DV, false, true);
       // base descriptors: K-major Q / K tiles, MN-major V tiles (128B swizzle)
       const uint32_t da = sdesc_lo(smem_u32(smem + L::q_off + sl * L::kTileBytes), 16);
       const uint32_t kv_lo_k = sdesc_lo(smem_u32(smem + L::kv_off), 16);
       const uint32_t kv_lo_v = sdesc_lo(smem_u32(smem + L::kv_off), L::kChunkKV);
       const uint32_t d_s0 = tmem + 2 * sl * BN;  // buffer bb at d_s0 + bb * BN
-      const uint32_t d_o = tmem + 4 * BN + sl * D;
+      const uint32_t d_o = tmem + 4 * BN + sl * DV;
       bool ok = mbar_wait(&bars->q_full, 0, ctx);
       // Slot 1 starts once slot 0's first softmax is done, so the two softmax
       // warpgroups do not start in step.
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t db = kv_lo_k + ((slot_k * L::kKVBytes) >> 4);
           const uint32_t d_s = d_s0 + (m2 & 1) * BN;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < DK / 16; ++kk) {
             const uint32_t offa = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
             const uint32_t offb = ((kk / 4) * L::kChunkKV + (kk % 4) * 32) >> 4;
             mma_ss_lo(d_s, da + offa, db + offb, idesc_s, kk > 0 ? 1u : 0u);
@@ -332,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int iq = row_in ? a.q_ids[(int64_t)bi * a.s_q + grow] : 0;
       const int pq = row_in ? a.q_pos[(int64_t)bi * a.s_q + grow] : 0;
       const uint32_t t_s0 = tmem + ((uint32_t)(wq * 32) << 16) + 2 * sl * BN;  // + (n & 1) * BN
-      const uint32_t t_o = tmem + ((uint32_t)(wq * 32) << 16) + 4 * BN + sl * D;
+      const uint32_t t_o = tmem + ((uint32_t)(wq * 32) << 16) + 4 * BN + sl * DV;
       const float sl2 = a.scale_log2;
       float m = -INFINITY;  // running max (base-2 units)
       float l = 0.f;        // running denominator relative to m
@@ -423,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
+          for (int c = 0; c < DV; c += 32) {
             uint32_t o[32];
             tmem_ld32(t_o + c, o);
             tmem_wait_ld();
@@ -462,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           inv *= cb;
         }
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < DV; c += 32) {
           uint32_t o[32];
           if (n > 0) {
             tmem_ld32(t_o + c, o);
@@ -473,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!row_in) continue;
           if (a.merge) {
-            float* acc = static_cast<float*>(a.out) + orow * D + c;
+            float* acc = static_cast<float*>(a.out) + orow * DV + c;
             float v[32];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -485,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[4 * u + 3] = merge1(ca, 1.f, x.w, __uint_as_float(o[4 * u + 3]) * inv);
             }
             if (a.out_final) {
-              uint4* dst = reinterpret_cast<uint4*>(a.out_final + orow * D + c);
+              uint4* dst = reinterpret_cast<uint4*>(a.out_final + orow * DV + c);
 #pragma unroll
               for (int u = 0; u < 4; ++u)
                 dst[u] = make_uint4(pack_bf16(v[8 * u], v[8 * u + 1]), pack_bf16(v[8 * u + 2], v[8 * u + 3]),
@@ -500,14 +507,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
           }
           if (a.out_fp32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * D + c);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * DV + c);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
               dst[u] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
                                    __uint_as_float(o[4 * u + 2]) * inv,
                                    __uint_as_float(o[4 * u + 3]) * inv);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + c);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * DV + c);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               uint4 w;
@@ -532,14 +539,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int D>
+template <int DK, int DV>
 cudaError_t launch_fwd_d(const FwdArgs& a, const FwdLaunch& Lc, int64_t units, cudaStream_t st) {
-  const int smem = Layout<D>::alloc;
+  const int smem = Layout<DK, DV>::alloc;
   static std::atomic<int> smem_set[kMaxDevices];
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<D>), smem,
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_kernel<DK, DV>), smem,
                                     kLaunchRegs, smem_set);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<D><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
+  attn_fwd_kernel<DK, DV><<<(unsigned)units, kThreads, smem, st>>>(Lc.tm_q, Lc.tm_k, Lc.tm_v, a);
   return cudaGetLastError();
 }
 
@@ -566,7 +573,8 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   a.hq = (int)p.h_q;
   a.hkv = (int)p.h_kv;
   a.g = (int)(p.h_q / p.h_kv);
-  const int slots = p.d <= 128 ? 2 : 1;  // query heads per CTA
+  const int64_t dv = p.d_v > 0 ? p.d_v : p.d;
+  const int slots = dv <= 128 ? 2 : 1;  // query heads per CTA
   a.npairs = (a.g + slots - 1) / slots;
   a.nq = (int)Lc.nq;
   a.nk = (int)Lc.nk;
@@ -577,9 +585,10 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   a.scale_log2 = p.scale * 1.4426950408889634f;
   const int64_t units = p.b * Lc.nq * p.h_kv * a.npairs;
   if (units == 0) return cudaSuccess;
-  if (p.d == 128) return launch_fwd_d<128>(a, Lc, units, st);
-  if (p.d == 256) return launch_fwd_d<256>(a, Lc, units, st);
-  return launch_fwd_d<64>(a, Lc, units, st);
+  if (p.d == 128) return launch_fwd_d<128, 128>(a, Lc, units, st);
+  if (p.d == 256) return launch_fwd_d<256, 256>(a, Lc, units, st);
+  if (p.d == 192 && dv == 128) return launch_fwd_d<192, 128>(a, Lc, units, st);
+  return launch_fwd_d<64, 64>(a, Lc, units, st);
 }
 
 }  // namespace gb300

@@ -63,12 +63,20 @@ def _params(ga, **kw):
     (dict(merge_into_out=1, out_fp32=1, out_final=(1 << 20) + 4096), 1),  # overlaps out
     (dict(kv_token_stride=128), 1),                       # below h_kv * d = 256
     (dict(kv_token_stride=260), 1),                       # not a multiple of 8
+    (dict(d_v=-1), 1),                                    # negative value head dim
+    (dict(d_v=64), 2),                                    # only d = 192 with d_v = 128
+    (dict(d=192, d_v=128, kv_token_stride=640), 1),       # packed K/V needs d_v == d
 ])
 def test_fwd_rejects_invalid_arguments_on_host(ga, kw, code):
     p = _params(ga, **kw)
     assert ga.lib().attn_fwd_workspace_bytes(ctypes.byref(p)) == 0
     p.workspace_bytes = 1 << 30
     assert ga.lib().attn_fwd(ctypes.byref(p), None) == code
+
+
+def test_fwd_accepts_mla_head_dims(ga):
+    p = _params(ga, d=192, d_v=128)
+    assert ga.lib().attn_fwd_workspace_bytes(ctypes.byref(p)) > 0
 
 
 def test_fwd_workspace_checks(ga):
@@ -98,7 +106,9 @@ def test_bwd_rejects_invalid_arguments_on_host(ga):
     bp.fwd.d, bp.fwd.kv_token_stride = 256, 0
     bp.fwd.workspace_bytes = 1 << 30
     assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 2
-    bp.fwd.d = 80
+    bp.fwd.d, bp.fwd.d_v = 192, 128  # forward-only MLA shape
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 2
+    bp.fwd.d, bp.fwd.d_v = 80, 0
     assert ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp)) == 0
 
 

@@ -73,6 +73,28 @@ def test_fp32_output(ga, d):
     _full_check(ga, q, k, v, ids, pos, -1, 0.1, out_fp32=True)
 
 
+@pytest.mark.parametrize("b,s,hq,hkv,window,slots,seed", [
+    (2, 300, 4, 2, 70, None, 12),    # ragged tail, window
+    (1, 520, 3, 1, -1, None, 13),    # odd group size
+    (2, 1024, 8, 2, 200, 4, 14),     # padded slots (the tutorial's packing)
+])
+def test_mla_head_dims(ga, b, s, hq, hkv, window, slots, seed):
+    """d_qk = 192, d_v = 128 (MLA): out has V's head dim."""
+    q, k, v = workload.qkv(b, s, hq, hkv, 192, seed=seed, dv=128)
+    if slots is None:
+        ids, pos = workload.random_segments(b, s, seed=seed)
+    else:
+        ids, pos = workload.segments(b, s, slots)
+    out, _ = _full_check(ga, q, k, v, ids, pos, window, 192 ** -0.5)
+    assert out.shape == (b, s, hq, 128)
+
+
+def test_mla_fp32_output(ga):
+    q, k, v = workload.qkv(1, 256, 2, 1, 192, seed=15, dv=128)
+    ids, pos = workload.segments(1, 256, 2)
+    _full_check(ga, q, k, v, ids, pos, -1, 0.1, out_fp32=True)
+
+
 def test_d256_backward_is_rejected(ga):
     """The backward takes d = 64 and 128 only: a d = 256 call fails loudly
     before any launch."""
