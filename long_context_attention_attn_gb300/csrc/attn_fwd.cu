@@ -42,12 +42,15 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = kFwdKeyTile;  // keys per tile (half of the plan's 128-key tile)
 constexpr int NST = 8;   // K/V shared-memory slots (K and V tiles alternate), d <= 128
-// Query heads per CTA and K/V slots by head dims (DK of q / k, DV of v / out):
-// DV = 256 takes one head slot (its O accumulator fills TMEM columns
-// [256, 512)) and four 32 KB slots; DK = 192 (DV = 128) five 24 KB slots.
+// Query heads per CTA, K/V slots and ids ring entries by head dims (DK of
+// q / k, DV of v / out): DV = 256 takes one head slot (its O accumulator fills
+// TMEM columns [256, 512)), five 32 KB slots and two ring entries; DK = 192
+// (DV = 128) five 24 KB slots.  With five slots a tile's V load reuses a slot
+// freed a tile and a half earlier.
 template <int DK, int DV> constexpr int kSlots = DV <= 128 ? 2 : 1;
-template <int DK, int DV> constexpr int kNst = DK <= 128 ? NST : (DK == 192 ? 5 : 4);
+template <int DK, int DV> constexpr int kNst = DK <= 128 ? NST : 5;
 constexpr int NID = 4;   // ids/pos ring entries
+template <int DK, int DV> constexpr int kNid = DK == 256 ? 2 : NID;
 constexpr int kThreads = 384;
 // Registers per thread at launch (65536 / 384, rounded down to a multiple of 8).
 constexpr int kLaunchRegs = 168;
@@ -92,7 +95,7 @@ struct Layout {
   static constexpr int q_off = 0;                     // kSlots Q tiles
   static constexpr int kv_off = q_off + kSlots<DK, DV> * kTileBytes;
   static constexpr int id_off = kv_off + kNst<DK, DV> * kKVBytes;  // NID x kIdEntry ints
-  static constexpr int bar_off = id_off + NID * kIdEntry * 4;
+  static constexpr int bar_off = id_off + kNid<DK, DV> * kIdEntry * 4;
   static constexpr int bytes = bar_off + 512;
   // + slack for 1024-byte alignment; at least 150 KB so that one CTA (which
   // holds all 512 TMEM columns) is resident per SM.
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h0 = kvh * a.g + kSlots<DK, DV> * pair;
   const int nslots = min(kSlots<DK, DV>, a.g - kSlots<DK, DV> * pair);
   constexpr int NSTD = kNst<DK, DV>;
+  constexpr int NIDD = kNid<DK, DV>;
   static_assert(4 * BN + kSlots<DK, DV> * DV <= 512, "TMEM columns");
   static_assert(Layout<DK, DV>::alloc <= 232448, "shared memory per block");
   const int2 rng = a.qrange[e];
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 4 * nslots);  // one arrival per softmax warp
     }
-    for (int i = 0; i < NID; ++i) {
+    for (int i = 0; i < NIDD; ++i) {
       mbar_init(&bars->id_full[i], 1);
       mbar_init(&bars->id_empty[i], 128 * nslots);
     }
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t kind = cls_row[j2 >> 1];
       if (kind == kSkip) continue;
       const int j = j2;  // 64-key tile index
-      const int en = n % NID, use = n / NID;
+      const int en = n % NIDD, use = n / NIDD;
       const int64_t base = (int64_t)bi * a.s_kv;
       int vid[BN / 32], vpos[BN / 32];
 #pragma unroll
@@ -346,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n = 0;
       bool ok = true;
       for (; n < nt;) {
-        const int en = n % NID;
-        ok = mbar_wait(&bars->id_full[en], (n / NID) & 1, ctx);
+        const int en = n % NIDD;
+        ok = mbar_wait(&bars->id_full[en], (n / NIDD) & 1, ctx);
         ok = mbar_wait(&bars->s_full[sl][n & 1], (n >> 1) & 1, ctx) && ok;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
