@@ -386,6 +386,7 @@ def run_ours(args, rank, world, local_rank):
         s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event()
         h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        fwd_in_done = [ev(), ev()]  # q, k, v, ids, pos of the set have landed (dout may not)
         for e_ in comp_done + d2h_done:
             e_.record(stream)
 
@@ -393,18 +394,22 @@ def run_ours(args, rank, world, local_rank):
             sl = i % 2
             s_h2d.wait_event(comp_done[sl])  # step i-2 no longer reads this input set
             with torch.cuda.stream(s_h2d):
-                for n, t in h_in.items():
-                    d_in[sl][n].copy_(t, non_blocking=True)
+                # the forward's inputs first; dout (read by the backward only) last
+                for n in ("q", "k", "v", "ids", "pos", "dout"):
+                    d_in[sl][n].copy_(h_in[n], non_blocking=True)
+                    if n == "pos":
+                        fwd_in_done[sl].record(s_h2d)
             h2d_done[sl].record(s_h2d)
 
         def compute(i):
             sl = i % 2
-            stream.wait_event(h2d_done[sl])
+            stream.wait_event(fwd_in_done[sl])
             stream.wait_event(d2h_done[sl])  # step i-2's gradients have left this set
             x_ = d_in[sl]
             gq, gk, gv = d_out[sl]
             ga.attn_fwd(x_["q"], x_["k"], x_["v"], x_["ids"], x_["pos"],
                         window_left=w.window_left, scale=w.scale, out=out, lse=lse, workspace=ws)
+            stream.wait_event(h2d_done[sl])  # dout, for the backward
             ga.attn_bwd(x_["q"], x_["k"], x_["v"], out, lse, x_["dout"], x_["ids"], x_["pos"],
                         window_left=w.window_left, scale=w.scale, dq=gq, dk=gk, dv=gv,
                         workspace=ws)
@@ -445,7 +450,8 @@ def run_ours(args, rank, world, local_rank):
                "d2h_bytes_per_step": bo,
                "copies": "every step's inputs in and gradients out inside the timed region, "
                          "on two copy streams overlapping the neighbouring steps' compute "
-                         "(double-buffered device tensors)"}
+                         "(double-buffered device tensors); a step's forward starts once "
+                         "its own inputs have landed, its dout copy overlapping it"}
         del h_in, h_out, d_in, d_out
 
     if dist:
