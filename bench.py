@@ -228,7 +228,9 @@ def hbm_components(ga, dev, pk):
     """HBM-bound rows of the hot path at the ring workload's shapes (b=1,
     s=32768, 64 query heads, d=128): one merge of a full-sequence fp32 partial
     into an fp32 accumulator (12*d+12 bytes per row-head), and the dual-chunk
-    reorder of q (2 x 1 GiB).  CUDA events, median of 10 after 3 warm-ups."""
+    reorder of q (2 x 1 GiB).  CUDA events around 10 back-to-back calls after 3
+    warm-ups (so the host's per-call launch latency overlaps the previous call
+    instead of counting as kernel time), per call."""
     import torch
 
     b, s, h, d = 1, 32768, 64, 128
@@ -240,18 +242,17 @@ def hbm_components(ga, dev, pk):
     q = torch.randn(b, s, h, d, generator=g, device=dev).to(torch.bfloat16)
     qo = torch.empty_like(q)
 
-    def timed(fn):
+    def timed(fn, n=10):
         for _ in range(3):
             fn()
-        ts = []
-        for _ in range(10):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
             fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        return sorted(ts)[len(ts) // 2]
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
 
     merge_ms = timed(lambda: ga.attn_merge_partial(acc, la, blk, lb))
     merge_bytes = b * s * h * (12 * d + 12)

@@ -214,6 +214,7 @@ __device__ __forceinline__ int64_t perm_src(int64_t i, int64_t s, int strategy, 
 }
 
 // One warp per row; 16-byte vectors along the row.
+constexpr int kPermVecs = 16;  // 16-byte vectors in flight per lane
 __global__ void permute_vec16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
                                      int64_t rows, int64_t s, int64_t vpr, int strategy, int R,
                                      int stripe, int inverse) {
@@ -227,15 +228,16 @@ __global__ void permute_vec16_kernel(const uint4* __restrict__ in, uint4* __rest
     const int64_t dst = o * s + (inverse ? j : i);
     const uint4* a = in + src * vpr;
     uint4* bptr = out + dst * vpr;
-    int64_t w = lane;
-    for (; w + 96 < vpr; w += 128) {
-      const uint4 x0 = a[w], x1 = a[w + 32], x2 = a[w + 64], x3 = a[w + 96];
-      bptr[w] = x0;
-      bptr[w + 32] = x1;
-      bptr[w + 64] = x2;
-      bptr[w + 96] = x3;
+    // 16 loads in flight per lane (8 KB per warp) before the stores
+    for (int64_t w = lane; w < vpr; w += 32 * kPermVecs) {
+      uint4 x[kPermVecs];
+#pragma unroll
+      for (int u = 0; u < kPermVecs; ++u)
+        if (w + 32 * u < vpr) x[u] = a[w + 32 * u];
+#pragma unroll
+      for (int u = 0; u < kPermVecs; ++u)
+        if (w + 32 * u < vpr) bptr[w + 32 * u] = x[u];
     }
-    for (; w < vpr; w += 32) bptr[w] = a[w];
   }
 }
 
@@ -278,7 +280,7 @@ cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t s, 
                          (reinterpret_cast<uintptr_t>(out) % 16 == 0);
   if (inner_bytes % 16 == 0 && aligned16) {
     const int64_t need = (rows + 7) / 8;
-    const unsigned grid = (unsigned)std::min<int64_t>(need, (int64_t)sms * 8);
+    const unsigned grid = (unsigned)std::min<int64_t>(need, (int64_t)sms * 16);
     permute_vec16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(in),
                                                static_cast<uint4*>(out), rows, s, inner_bytes / 16,
                                                strategy, cp, stripe, inverse ? 1 : 0);
