@@ -7,7 +7,8 @@
 //
 // One CTA computes a 128-row query tile for TWO query heads of one GQA group
 // (both read the same kv head, so every K/V tile loaded into shared memory
-// feeds both), walking the keys in 64-key tiles.  Roles (384 threads):
+// feeds both; one head when d_v = 256), walking the keys in 64-key tiles.
+// Roles (384 threads):
 //   warp 0        TMA producer: Q tiles once, then K and V tiles into a ring
 //                 of shared-memory slots.
 //   warps 1, 3    MMA issuers, one thread per head slot: S_h = Q_h K^T and
@@ -19,7 +20,8 @@
 //   slot 0 S buffers [0,64) [64,128), slot 1 [128,192) [192,256),
 //   O0 [256,256+d_v)  O1 [256+d_v, 256+2d_v)
 // (head dims: q / k and v / out both 64, 128 or 256, or 192 / 128; at d_v = 256
-// a CTA takes one head slot, whose O fills columns [256, 512))
+// a CTA takes one head slot, whose O fills columns [256, 512), and warps 3 and
+// 8-11 stay idle)
 // Key tile n's scores go to buffer n & 1 of the slot, so S(n+1) is computed
 // while the softmax works on tile n.  P (bf16, 2 per column) overwrites the
 // first 32 columns of its S buffer and is the A operand of the P.V MMA
