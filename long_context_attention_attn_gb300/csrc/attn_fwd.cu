@@ -44,15 +44,15 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = kFwdKeyTile;  // keys per tile (half of the plan's 128-key tile)
 constexpr int NST = 8;   // K/V shared-memory slots (K and V tiles alternate), d <= 128
-// Query heads per CTA, K/V slots and ids ring entries by head dims (DK of
-// q / k, DV of v / out): DV = 256 takes one head slot (its O accumulator fills
-// TMEM columns [256, 512)), five 32 KB slots and two ring entries; DK = 192
-// (DV = 128) five 24 KB slots.  With five slots a tile's V load reuses a slot
-// freed a tile and a half earlier.
+// Query heads per CTA and K/V slots by head dims (DK of q / k, DV of v / out):
+// DV = 256 takes one head slot (its O accumulator fills TMEM columns
+// [256, 512)) and keeps the query tile in TMEM columns [128, 256) (the second
+// slot's S buffers), the A operand of S = Q K^T, so shared memory holds six
+// 32 KB K/V slots and no Q; DK = 192 (DV = 128) five 24 KB slots.
 template <int DK, int DV> constexpr int kSlots = DV <= 128 ? 2 : 1;
-template <int DK, int DV> constexpr int kNst = DK <= 128 ? NST : 5;
+template <int DK, int DV> constexpr bool kQInTmem = DK == 256;
+template <int DK, int DV> constexpr int kNst = DK <= 128 ? NST : (DK == 192 ? 5 : 6);
 constexpr int NID = 4;   // ids/pos ring entries
-template <int DK, int DV> constexpr int kNid = DK == 256 ? 2 : NID;
 constexpr int kThreads = 384;
 // Registers per thread at launch (65536 / 384, rounded down to a multiple of 8).
 constexpr int kLaunchRegs = 168;
@@ -64,6 +64,7 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct FwdArgs {
+  const __nv_bfloat16* q;  // read directly when the query tile is kept in TMEM
   const int* q_ids;
   const int* q_pos;
   const int* kv_ids;
@@ -94,10 +95,10 @@ struct Layout {
   static constexpr int kKBytes = BN * DK * 2;         // a K tile
   static constexpr int kVBytes = BN * DV * 2;         // a V tile
   static constexpr int kKVBytes = kKBytes > kVBytes ? kKBytes : kVBytes;  // a K / V slot
-  static constexpr int q_off = 0;                     // kSlots Q tiles
-  static constexpr int kv_off = q_off + kSlots<DK, DV> * kTileBytes;
+  static constexpr int q_off = 0;                     // kSlots Q tiles (none when in TMEM)
+  static constexpr int kv_off = q_off + (kQInTmem<DK, DV> ? 0 : kSlots<DK, DV> * kTileBytes);
   static constexpr int id_off = kv_off + kNst<DK, DV> * kKVBytes;  // NID x kIdEntry ints
-  static constexpr int bar_off = id_off + kNid<DK, DV> * kIdEntry * 4;
+  static constexpr int bar_off = id_off + NID * kIdEntry * 4;
   static constexpr int bytes = bar_off + 512;
   // + slack for 1024-byte alignment; at least 150 KB so that one CTA (which
   // holds all 512 TMEM columns) is resident per SM.
@@ -148,7 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h0 = kvh * a.g + kSlots<DK, DV> * pair;
   const int nslots = min(kSlots<DK, DV>, a.g - kSlots<DK, DV> * pair);
   constexpr int NSTD = kNst<DK, DV>;
-  constexpr int NIDD = kNid<DK, DV>;
+  constexpr int NIDD = NID;
+  constexpr bool QT = kQInTmem<DK, DV>;
+  constexpr uint32_t kColQ = 2 * BN;  // query tile in TMEM (QT only)
+  static_assert(!QT || (kSlots<DK, DV> == 1 && kColQ + DK / 2 <= 4 * BN), "TMEM columns");
   static_assert(4 * BN + kSlots<DK, DV> * DV <= 512, "TMEM columns");
   static_assert(Layout<DK, DV>::alloc <= 232448, "shared memory per block");
   const int2 rng = a.qrange[e];
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint8_t* cls_row = a.cls + (size_t)e * a.nk;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_full, QT ? 128 : 1);  // TMA, or the 128 threads storing Q into TMEM
     for (int i = 0; i < NSTD; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 4 * nslots);  // one arrival per softmax warp
@@ -197,11 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, nslots * L::kTileBytes);
-      for (int sl = 0; sl < nslots; ++sl)
-        for (int c = 0; c < L::kChunksK; ++c)
-          tma_load_4d(smem_u32(smem + L::q_off + sl * L::kTileBytes + c * L::kChunk), &tm_q,
-                      c * 64, h0 + sl, qt * BM, bi, &bars->q_full);
+      if (!QT) {
+        mbar_arrive_expect_tx(&bars->q_full, nslots * L::kTileBytes);
+        for (int sl = 0; sl < nslots; ++sl)
+          for (int c = 0; c < L::kChunksK; ++c)
+            tma_load_4d(smem_u32(smem + L::q_off + sl * L::kTileBytes + c * L::kChunk), &tm_q,
+                        c * 64, h0 + sl, qt * BM, bi, &bars->q_full);
+      }
     }
     int n = 0;
     int last_use[NSTD];
@@ -230,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Drain: every TMA copy this warp issued has landed before the CTA exits
     // (already true on the normal path; bounded after an abort).
     if (lane == 0) {
-      mbar_wait_drain(&bars->q_full, 0, a.status);
+      if (!QT) mbar_wait_drain(&bars->q_full, 0, a.status);
       for (int i = 0; i < NSTD; ++i)
         if (last_use[i] >= 0) mbar_wait_drain(&bars->kv_full[i], last_use[i] & 1, a.status);
     }
@@ -287,7 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < DK / 16; ++kk) {
             const uint32_t offa = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
             const uint32_t offb = ((kk / 4) * L::kChunkKV + (kk % 4) * 32) >> 4;
-            mma_ss_lo(d_s, da + offa, db + offb, idesc_s, kk > 0 ? 1u : 0u);
+            if constexpr (QT)
+              mma_ts_lo(d_s, tmem + kColQ + kk * 8, db + offb, idesc_s, kk > 0 ? 1u : 0u);
+            else
+              mma_ss_lo(d_s, da + offa, db + offb, idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full[sl][m2 & 1]);
         }
@@ -347,6 +356,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_s0 = tmem + ((uint32_t)(wq * 32) << 16) + 2 * sl * BN;  // + (n & 1) * BN
       const uint32_t t_o = tmem + ((uint32_t)(wq * 32) << 16) + 4 * BN + sl * DV;
       const float sl2 = a.scale_log2;
+      if constexpr (QT) {
+        // The query row into TMEM as bf16 pairs (column c holds elements 2c,
+        // 2c + 1: the row's own byte order), the A operand of S = Q K^T.
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + (((int64_t)bi * a.s_q + grow) * a.hq + h) * DK);
+#pragma unroll 1
+        for (int c = 0; c < DK / 2; c += 32) {
+          uint32_t w[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 v = row_in ? src[c / 4 + u] : make_uint4(0u, 0u, 0u, 0u);
+            w[4 * u] = v.x;
+            w[4 * u + 1] = v.y;
+            w[4 * u + 2] = v.z;
+            w[4 * u + 3] = v.w;
+          }
+          tmem_st32(tmem + ((uint32_t)(wq * 32) << 16) + kColQ + c, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->q_full);
+      }
       float m = -INFINITY;  // running max (base-2 units)
       float l = 0.f;        // running denominator relative to m
       int n = 0;
@@ -562,6 +593,7 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   const attn_fwd_params& p = *Lc.p;
   FwdArgs a;
   a.withhold_kv = Lc.withhold_kv ? 1 : 0;
+  a.q = static_cast<const __nv_bfloat16*>(p.q);
   a.q_ids = p.q_segment_ids;
   a.q_pos = p.q_segment_pos;
   a.kv_ids = p.kv_segment_ids;
