@@ -62,6 +62,44 @@ def test_random_packing(ga, b, s, hq, hkv, d, window, seed):
     _full_check(ga, x, window, d ** -0.5)
 
 
+
+@pytest.mark.parametrize("s_q,s_kv,q0,window,d,seed", [
+    (256, 384, 300, 200, 128, 11),   # queries late in the kv range, window crossing tiles
+    (200, 520, 100, -1, 64, 12),     # ragged on both sides, unlimited window
+    (384, 130, 0, 40, 128, 13),      # more queries than keys (rows past the keys see none)
+])
+def test_cross_descriptor_and_lengths(ga, s_q, s_kv, q0, window, d, seed):
+    """Queries of one shard against keys of another, of a different length
+    and with a padding hole in the keys (the per-block call of a ring step
+    with its own q and kv descriptors)."""
+    hq, hkv = 4, 2
+    q, _, _, dout = workload.qkv(1, s_q, hq, hkv, d, seed=seed, with_dout=True)
+    _, k, v = workload.qkv(1, s_kv, hq, hkv, d, seed=seed + 100)
+    ids = torch.ones(1, s_q, dtype=torch.int32)
+    pos = torch.arange(q0, q0 + s_q, dtype=torch.int32)[None]
+    kv_ids = torch.ones(1, s_kv, dtype=torch.int32)
+    kv_pos = torch.arange(0, s_kv, dtype=torch.int32)[None]
+    kv_ids[0, s_kv // 3:s_kv // 3 + 30] = 0
+    scale = d ** -0.5
+    g = {n: t.to(DEV) for n, t in dict(q=q, k=k, v=v, dout=dout, ids=ids, pos=pos,
+                                       kv_ids=kv_ids, kv_pos=kv_pos).items()}
+    out, lse = ga.attn_fwd(g["q"], g["k"], g["v"], g["ids"], g["pos"], g["kv_ids"], g["kv_pos"],
+                           window_left=window, scale=scale)
+    dq, dk, dv = ga.attn_bwd(g["q"], g["k"], g["v"], out, lse, g["dout"], g["ids"], g["pos"],
+                             g["kv_ids"], g["kv_pos"], window_left=window, scale=scale)
+    torch.cuda.synchronize()
+    rq, rk, rv = A.attn_bwd(q, k, v, dout, ids, pos, kv_ids, kv_pos, window, scale)
+    check_grad(dq.cpu(), rq, "dq")
+    check_grad(dk.cpu(), rk, "dk")
+    check_grad(dv.cpu(), rv, "dv")
+    # keys no query can see (padding, or outside every query's window) get exactly 0
+    ro, _ = A.attn_fwd(q, k, v, ids, pos, kv_ids, kv_pos, window, scale)
+    unseen = torch.from_numpy(np.abs(rk).sum(axis=(2, 3)) == 0)
+    assert torch.all(dk.cpu()[unseen] == 0) and torch.all(dv.cpu()[unseen] == 0)
+    # query rows that see no key get dQ = 0 exactly
+    blind = torch.from_numpy(np.abs(ro).sum(axis=(2, 3)) == 0)
+    assert torch.all(dq.cpu()[blind] == 0)
+
 def _sampled(ga, name, dq_samples, key_samples):
     w = workload.WORKLOADS[name]
     x = workload.make(w, device=DEV, with_dout=True)
