@@ -28,6 +28,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOP/s on valid pairs, % of GB300 dense BF16 peak (1 GPU)"
+METRIC_FWD = "attention fwd TFLOP/s on valid pairs, % of GB300 dense BF16 peak (1 GPU)"
 WORKLOAD = "full_swa_64k"
 # TE tutorial, section 5: single-GPU fused attention fwd+bwd on this exact
 # workload, 126.687 ms on one GB200 (context, another machine).
@@ -314,16 +315,22 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = workload.WORKLOADS[args.workload]
+    fwd_only = w.fwd_only  # head dims the backward does not take: the step is attn_fwd
     pairs = valid_pairs(w)
-    fwd_flop = 4 * w.d * w.hq * pairs
-    bwd_flop = 10 * w.d * w.hq * pairs
-    x = workload.make(w, device=dev, with_dout=True, seed=workload.SEED + rank)
-    q, k, v, dout, ids, pos = x["q"], x["k"], x["v"], x["dout"], x["ids"], x["pos"]
-    out = torch.empty_like(q)
+    fwd_flop = 2 * (w.d + w.dv) * w.hq * pairs
+    bwd_flop = 0 if fwd_only else 10 * w.d * w.hq * pairs
+    x = workload.make(w, device=dev, with_dout=not fwd_only, seed=workload.SEED + rank)
+    q, k, v, ids, pos = x["q"], x["k"], x["v"], x["ids"], x["pos"]
+    dout = x.get("dout")
+    out = torch.empty(w.b, w.s, w.hq, w.dv, dtype=q.dtype, device=dev)
     lse = torch.empty(w.b, w.hq, w.s, dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left), dtype=torch.uint8,
-                     device=dev)
+    if fwd_only:
+        ws = torch.empty(ga.workspace_bytes_fwd(q, k, ids, pos, window_left=w.window_left, v=v),
+                         dtype=torch.uint8, device=dev)
+    else:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left),
+                         dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
@@ -333,8 +340,9 @@ def run_ours(args, rank, world, local_rank):
                     lse=lse, workspace=ws)
         if ev:
             ev[1].record(stream)
-        ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=w.window_left, scale=w.scale,
-                    dq=dq, dk=dk, dv=dv, workspace=ws)
+        if not fwd_only:
+            ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=w.window_left,
+                        scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
         if ev:
             ev[2].record(stream)
 
@@ -374,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
     # copies run on their own streams into double-buffered device tensors, so
     # step i+1's inputs and step i-1's gradients move while step i computes.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not fwd_only:
         h_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v),
                                                          ("dout", dout), ("ids", ids),
                                                          ("pos", pos))}
@@ -461,9 +469,13 @@ def run_ours(args, rank, world, local_rank):
         return
     pk = peaks()
     hbm = hbm_components(ga, dev, pk)
-    bwd_tflops = bwd_flop / (bwd_avg * 1e-3) / 1e12
+    bwd_tflops = None if fwd_only else bwd_flop / (bwd_avg * 1e-3) / 1e12
     fwd_tflops = fwd_flop / (fwd_avg * 1e-3) / 1e12
     per_gpu = value / world
+    if fwd_only:
+        print(json.dumps(fwd_only_line(args, w, world, pairs, value, ms_per_step, fwd_avg,
+                                       fwd_tflops, pk, clocks)), flush=True)
+        return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         val, info = oracle_sample(w)
@@ -505,6 +517,35 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
+
+
+def fwd_only_line(args, w, world, pairs, value, ms_per_step, fwd_avg, fwd_tflops, pk, clocks):
+    """Result line of a forward-only workload (head dims the backward does not
+    take): the step is one attn_fwd call; no end-to-end or oracle leg."""
+    per_gpu = value / world
+    return {
+        "metric": METRIC_FWD, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "b": w.b, "s": w.s, "slots": w.slots, "hq": w.hq,
+                   "hkv": w.hkv, "d": w.d, "d_v": w.dv, "window": [w.window_left, 0],
+                   "step": "attn_fwd", "valid_pairs_per_head": pairs,
+                   "flop_per_pair_head": {"fwd": 2 * (w.d + w.dv)},
+                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+        "pct_of_peak": {"burst": 100 * per_gpu / pk["bf16_burst"],
+                        "sustained": 100 * per_gpu / pk["bf16_sustained"],
+                        "source": pk["source"]},
+        "components": {"fwd_ms": fwd_avg, "fwd_tflops": fwd_tflops},
+        "roofline": {"kernel": "attn_fwd (fused forward + its tile plan; timed per call)",
+                     "bound": "tensor", "achieved": fwd_tflops, "peak": pk["bf16_sustained"],
+                     "unit": "TFLOP/s", "frac": fwd_tflops / pk["bf16_sustained"],
+                     "peak_kind": f"bf16 sustained, {pk['source']}", "traffic": None},
+        "cpu_baseline": None,
+        "e2e": None,
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks.summary(),
+    }
 
 
 def main():

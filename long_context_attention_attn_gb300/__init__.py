@@ -164,10 +164,13 @@ def _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, 
 
 
 def workspace_bytes_fwd(q, k, q_ids, q_pos, kv_ids=None, kv_pos=None, window_left=-1,
-                        scale=None) -> int:
+                        scale=None, v=None) -> int:
+    """Workspace bytes attn_fwd needs for these shapes (0 if it rejects them);
+    pass ``v`` when its head dim differs from k's."""
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
-    p = _fwd_params(q, k, k, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, q, q, False)
+    v = k if v is None else v
+    p = _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, q, q, False)
     return int(lib().attn_fwd_workspace_bytes(ctypes.byref(p)))
 
 

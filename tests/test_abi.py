@@ -79,6 +79,18 @@ def test_fwd_accepts_mla_head_dims(ga):
     assert ga.lib().attn_fwd_workspace_bytes(ctypes.byref(p)) > 0
 
 
+def test_binding_workspace_query_takes_v_width(ga):
+    """The binding's size query for MLA shapes needs v (its head dim differs
+    from k's); without it the shapes read as an unsupported d = 192."""
+    import workload
+    q, k, v = workload.qkv(1, 256, 4, 2, 192, dv=128)
+    ids, pos = workload.segments(1, 256, None)
+    assert ga.workspace_bytes_fwd(q, k, ids, pos, v=v) > 0
+    assert ga.workspace_bytes_fwd(q, k, ids, pos) == 0
+    q, k, v = workload.qkv(1, 256, 4, 2, 128)
+    assert ga.workspace_bytes_fwd(q, k, ids, pos, v=v) == ga.workspace_bytes_fwd(q, k, ids, pos)
+
+
 def test_fwd_workspace_checks(ga):
     p = _params(ga)
     need = ga.lib().attn_fwd_workspace_bytes(ctypes.byref(p))

@@ -38,13 +38,20 @@ class Workload:
     bwd: bool = False
     cp_size: int = 0          # >0: ring emulation over cp_size logical shards
     note: str = ""
+    d_v: int = 0              # head dim of v / out when it differs from q / k's (0: d)
+    fwd_only: bool = False    # head dims the backward does not take: measured forward only
 
     @property
     def scale(self) -> float:
         return self.d ** -0.5
 
+    @property
+    def dv(self) -> int:
+        return self.d_v or self.d
 
-# The five workloads the hot path is measured and checked on.
+
+# The five workloads the hot path is measured and checked on, then the other
+# head dims' forward-only shapes.
 WORKLOADS = {
     "tiny": Workload("tiny", 1, 256, 4, 2, 64, None, -1,
                      note="one segment, causal, no window"),
@@ -56,6 +63,16 @@ WORKLOADS = {
                          note="one segment, causal, ring emulation over 4 shards"),
     "full_swa_64k": Workload("full_swa_64k", 2, 65536, 128, 8, 128, 4, 8192, bwd=True,
                              note="4 slots of 16384 (12288 valid), causal, window (8192,0)"),
+    # Other head dims (TE tutorial, "next steps": MLA head dims), forward only,
+    # on the packed_swa packing and on one causal 32k segment.
+    "packed_swa_d256": Workload("packed_swa_d256", 2, 16384, 32, 8, 256, 4, 1024,
+                                fwd_only=True, note="packed_swa's packing at d = 256"),
+    "packed_swa_mla": Workload("packed_swa_mla", 2, 16384, 32, 8, 192, 4, 1024, d_v=128,
+                               fwd_only=True, note="packed_swa's packing, d_qk 192, d_v 128"),
+    "causal_32k_d256": Workload("causal_32k_d256", 1, 32768, 32, 8, 256, None, -1,
+                                fwd_only=True, note="one causal segment of 32768, d = 256"),
+    "causal_32k_mla": Workload("causal_32k_mla", 1, 32768, 32, 8, 192, None, -1, d_v=128,
+                               fwd_only=True, note="one causal segment, d_qk 192, d_v 128"),
 }
 
 
@@ -110,7 +127,8 @@ def qkv(b: int, s: int, hq: int, hkv: int, d: int, *, seed: int = SEED,
 def make(w: Workload, *, device="cpu", seed: int = SEED, with_dout: Optional[bool] = None):
     """All inputs of a workload: dict of q, k, v, [dout], ids, pos."""
     with_dout = w.bwd if with_dout is None else with_dout
-    tensors = qkv(w.b, w.s, w.hq, w.hkv, w.d, seed=seed, with_dout=with_dout, device=device)
+    tensors = qkv(w.b, w.s, w.hq, w.hkv, w.d, seed=seed, with_dout=with_dout, device=device,
+                  dv=w.dv)
     ids, pos = segments(w.b, w.s, w.slots)
     out = dict(q=tensors[0], k=tensors[1], v=tensors[2],
                ids=ids.to(device), pos=pos.to(device))
