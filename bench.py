@@ -468,14 +468,14 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     pk = peaks()
-    hbm = hbm_components(ga, dev, pk)
-    bwd_tflops = None if fwd_only else bwd_flop / (bwd_avg * 1e-3) / 1e12
     fwd_tflops = fwd_flop / (fwd_avg * 1e-3) / 1e12
-    per_gpu = value / world
     if fwd_only:
         print(json.dumps(fwd_only_line(args, w, world, pairs, value, ms_per_step, fwd_avg,
                                        fwd_tflops, pk, clocks)), flush=True)
         return
+    hbm = hbm_components(ga, dev, pk)
+    bwd_tflops = bwd_flop / (bwd_avg * 1e-3) / 1e12
+    per_gpu = value / world
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         val, info = oracle_sample(w)
