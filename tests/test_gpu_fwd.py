@@ -190,6 +190,17 @@ def test_full_swa_64k_sampled(ga):
     ])
 
 
+@pytest.mark.parametrize("name,samples", [
+    ("packed_swa_d256", [(0, 0, 0, 128), (1, 31, 4096 + 2900, 300), (0, 12, 16384 - 200, 200)]),
+    ("packed_swa_mla", [(0, 3, 1000, 128), (1, 30, 2 * 4096 + 3000, 200)]),
+    ("causal_32k_d256", [(0, 0, 0, 128), (0, 31, 32768 - 100, 100), (0, 9, 20000, 64)]),
+    ("causal_32k_mla", [(0, 5, 127, 130), (0, 26, 32768 - 64, 64)]),
+])
+def test_other_head_dims_sampled(ga, name, samples):
+    """The forward-only head-dim workloads at the sizes the bench times them."""
+    _sampled_check(ga, name, samples)
+
+
 def test_fwd_bit_identical_across_repeats(ga):
     """The forward has a fixed reduction order, so repeated calls must agree bit
     for bit; a read of O before the last P.V groups land (or any other race
