@@ -11,7 +11,9 @@
 // TMEM while it walks over every (query tile, query head of the GQA group)
 // that can see the tile (a "step").  Per step it recomputes S^T = K Q^T and
 // dP^T = V dO^T on tcgen05 (keys on TMEM lanes), forms P^T and dS^T in
-// registers (one thread per key row), writes them back to TMEM as bf16 (the A
+// registers (one thread per key row; one extra K = 16 MMA step subtracts the
+// per-query LSE / scale from S^T and D from dP^T, so that no per-column vector
+// is read from shared memory), writes them back to TMEM as bf16 (the A
 // operands of dV += P^T dO and dK += dS^T Q), stages dS in shared memory for
 // dQ = dS K, and adds the dQ tile into an fp32 accumulator in global memory
 // with TMA tiled reduce-adds staged through the (then free) dS buffer.
@@ -44,14 +46,35 @@ constexpr int BM = 128;  // query rows per step
 constexpr int BN = 128;  // key rows per CTA
 constexpr int NQ = 2;    // Q tile stages
 constexpr int NV = 4;    // per-step vector ring entries
-// vector entry: lse2, D, ids, pos (128 each), then the step's tile class
-constexpr int kVecEntry = 4 * 128 + 32;
+// vector entry: query ids, pos (128 each), then the step's tile class
+constexpr int kVecEntry = 2 * 128 + 32;
+// Per-step augment tile (no-swizzle K-major, 128 query rows x 16 bf16): row q
+// holds -c split into three bf16 (c = LSE / scale, so that scale * (S - c) is
+// the exponent of P in the base-2 domain) and -D split likewise, then zeros.
+// With the constant "ones" tiles E_S (ones in columns 0-2) and E_D (ones in
+// columns 3-5) as A, one extra K = 16 MMA step makes the tensor core deliver
+// S^T - c and dP^T - D, so no per-column vector is read in the element-wise
+// phases.
+constexpr int kAugTile = 128 * 16 * 2;
+constexpr float kAugNoKeys = 18446744073709551616.0f;  // 2^64: c of a row without keys
 constexpr int kThreads = 384;
 // Registers per thread at launch (65536 / 384, rounded down to a multiple of 8).
 constexpr int kLaunchRegs = 168;
 static_assert(128 * kRegsControl + 256 * kRegsCompute <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr float kLog2e = 1.4426950408889634f;
+
+// x as three bf16 (round to nearest even each) whose fp32 sum is x to about
+// 24 bits: the high part, then the rounded residuals.
+__device__ __forceinline__ void split_bf16x3(float x, uint32_t out[3]) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(h);
+  const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+  out[0] = __bfloat16_as_ushort(h);
+  out[1] = __bfloat16_as_ushort(m);
+  out[2] = __bfloat16_as_ushort(l);
+}
 
 struct BwdArgs {
   const int* q_ids;
@@ -86,7 +109,9 @@ struct BLayout {
   static constexpr int q_off = v_off + kTile;          // NQ stages
   static constexpr int do_off = q_off + NQ * kTile;    // 1 stage
   static constexpr int ds_off = do_off + kTile;        // dS: 128 q x 128 keys bf16, MN-major
-  static constexpr int vec_off = ds_off + 2 * kChunk;  // NV x kVecEntry words
+  static constexpr int e_off = ds_off + 2 * kChunk;    // E_S, E_D ones tiles
+  static constexpr int aug_off = e_off + 2 * kAugTile; // NV augment tiles
+  static constexpr int vec_off = aug_off + NV * kAugTile;  // NV x kVecEntry words
   static constexpr int bar_off = vec_off + NV * kVecEntry * 4;
   static constexpr int bytes = bar_off + 256;
   static constexpr int alloc = (bytes + 1024) > 150 * 1024 ? (bytes + 1024) : 150 * 1024;
@@ -202,6 +227,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
+  if (warp == 2) {
+    // E_S / E_D (ones in columns 0-2 / 3-5 of each key row) and zeroed
+    // augment tiles (their second K half stays zero)
+    uint4* e = reinterpret_cast<uint4*>(smem + L::e_off);
+    constexpr int kE16 = kAugTile / 16;  // 16-byte units per tile
+    const uint32_t one = 0x3F80u;        // bf16 1.0
+    for (int i = lane; i < 2 * kE16 + NV * kE16; i += 32) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      const bool first_half = ((i % kE16) % 16) < 8;  // K columns 0-7 of its row
+      if (i < kE16 && first_half) v = make_uint4(one | (one << 16), one, 0u, 0u);
+      if (i >= kE16 && i < 2 * kE16 && first_half) v = make_uint4(0u, one << 16, one | (one << 16), 0u);
+      e[i] = v;
+    }
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -284,22 +324,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_mn = sdesc_lo(smem_u32(smem + L::q_off), L::kChunk);
       const uint32_t do_mn = sdesc_lo(smem_u32(smem + L::do_off), L::kChunk);
       const uint32_t ds_mn = sdesc_lo(smem_u32(smem + L::ds_off), L::kChunk);
+      const uint32_t e_s = sdesc_lo_nosw(smem_u32(smem + L::e_off));
+      const uint32_t e_d = sdesc_lo_nosw(smem_u32(smem + L::e_off + kAugTile));
+      const uint32_t aug0 = sdesc_lo_nosw(smem_u32(smem + L::aug_off));
       const uint32_t t_s = tmem + kColS, t_dp = tmem + kColDP, t_dq = tmem + kColDQ;
       bool ok = mbar_wait(&bars->kv_full, 0, ctx);
       for (int t = 0; t < nsteps_total && ok; ++t) {
         const int qs = t % NQ;
         const uint32_t qstage = (qs * L::kTile) >> 4;
         ok = mbar_wait(&bars->q_full[qs], (t / NQ) & 1, ctx);
+        // the step's augment tile (-c, -D)
+        if (ok) ok = mbar_wait(&bars->vec_full[t % NV], (t / NV) & 1, ctx);
         // S^T overwrites P^T / dS^T of the previous step: dV and dK must be done
         if (ok && t > 0) ok = mbar_wait(&bars->dk_done, (t - 1) & 1, ctx);
         if (!ok) break;
         tc_fence_after();
-        // S^T = K Q^T  (M = keys, N = queries, K = d)
+        const uint32_t aug = aug0 + (((t % NV) * kAugTile) >> 4);
+        // S^T - c = K Q^T + E_S Aug^T  (M = keys, N = queries, K = d, then 16)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
           mma_ss_lo(t_s, k_km + off, q_km + qstage + off, id_kk, kk > 0 ? 1u : 0u);
         }
+        mma_ss_nosw(t_s, e_s, aug, id_kk, 1u);
         mma_commit(&bars->s_full);
         // dP^T = V dO^T
         ok = mbar_wait(&bars->do_full, t & 1, ctx);
@@ -312,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = ((kk / 4) * L::kChunk + (kk % 4) * 32) >> 4;
           mma_ss_lo(t_dp, v_km + off, do_km + off, id_kk, kk > 0 ? 1u : 0u);
         }
+        mma_ss_nosw(t_dp, e_d, aug, id_kk, 1u);  // dP^T - D
         mma_commit(&bars->dp_full);
         // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major)
         ok = mbar_wait(&bars->p_full, t & 1, ctx);
@@ -377,9 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ======================================================== vector loader
-    // Per step: LSE (base 2; +inf for rows without keys, so P = 0), D, query
-    // ids / pos, and the step's tile class, into the ring read
-    // by the element-wise warpgroups (off the TMA producer's path).
+    // Per step: the augment tile (-LSE / scale and -D, each split into three
+    // bf16; a row without keys takes 2^64, so P = 0), read by the S^T and dP^T
+    // MMAs, and the query ids / pos and the step's tile class, read by the
+    // element-wise warpgroups (off the TMA producer's path).
     int t = 0;
     bool ok = true;
     for (StepIter it = it0; it.valid() && ok; it.next(), ++t) {
@@ -403,19 +452,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ok = mbar_wait(&bars->vec_empty[en], (use & 1) ^ 1, ctx);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      float* v = vec + en * kVecEntry;
-      int* vi = reinterpret_cast<int*>(v);
+      int* vi = reinterpret_cast<int*>(vec + en * kVecEntry);
+      uint8_t* aug = smem + L::aug_off + en * kAugTile;
+      const float inv_scale = 1.f / a.scale;
 #pragma unroll
       for (int u = 0; u < BM / 32; ++u) {
         const int r = u * 32 + lane;
-        v[r] = (vl[u] == -INFINITY) ? INFINITY : vl[u] * kLog2e;
-        v[BM + r] = vd[u];
-        vi[2 * BM + r] = vid[u];
-        vi[3 * BM + r] = vps[u];
+        vi[r] = vid[u];
+        vi[BM + r] = vps[u];
+        // -c and -D, each as three bf16 whose sum is the fp32 value
+        const float c = (vl[u] == -INFINITY) ? kAugNoKeys : vl[u] * inv_scale;
+        uint32_t cs[3], ds[3];
+        split_bf16x3(-c, cs);
+        split_bf16x3(-vd[u], ds);
+        *reinterpret_cast<uint4*>(aug + (r / 8) * 256 + (r % 8) * 16) =
+            make_uint4(cs[0] | (cs[1] << 16), cs[2] | (ds[0] << 16), ds[1] | (ds[2] << 16), 0u);
       }
       if (lane == 0) {
-        vi[4 * BM] = kind;
+        vi[2 * BM] = kind;
       }
+      fence_proxy_async_smem();  // the augment tile is read by the MMAs
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->vec_full[en]);
     }
@@ -445,27 +501,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* ventry = vec + en * kVecEntry;
-      const int* vmeta = reinterpret_cast<const int*>(ventry) + 4 * BM;
-      const bool partial = vmeta[0] == kPartial;
-      const float* lse2 = ventry + 64 * w;
-      const float* dvec = ventry + BM + 64 * w;
-      const int* qid = reinterpret_cast<const int*>(ventry + 2 * BM) + 64 * w;
-      const int* qpos = reinterpret_cast<const int*>(ventry + 3 * BM) + 64 * w;
+      const int* ventry = reinterpret_cast<const int*>(vec + en * kVecEntry);
+      const bool partial = ventry[2 * BM] == kPartial;
+      const int* qid = ventry + 64 * w;
+      const int* qpos = ventry + BM + 64 * w;
       uint32_t r[64];
       tmem_ld32(tmem + lane_off + kColS + 64 * w, &r[0]);
       tmem_ld32(tmem + lane_off + kColS + 64 * w + 32, &r[32]);
       tmem_wait_ld();
-      // per-column vectors are read from shared memory 16 bytes at a time
-      const float4* lse4 = reinterpret_cast<const float4*>(lse2);
+      // the tensor core already subtracted c = LSE / scale: P = 2^(scale log2(e) (S - c))
       float p[64];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 l = lse4[c];
-        const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) p[4 * c + u] = ex2(fmaf(__uint_as_float(r[4 * c + u]), sl2, -lv[u]));
-      }
+      for (int u = 0; u < 64; ++u) p[u] = ex2(__uint_as_float(r[u]) * sl2);
       if (partial) {
         const int4* id4 = reinterpret_cast<const int4*>(qid);
         const int4* ps4 = reinterpret_cast<const int4*>(qpos);
@@ -498,15 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_off + kColDP + 64 * w, &r[0]);
       tmem_ld32(tmem + lane_off + kColDP + 64 * w + 32, &r[32]);
       tmem_wait_ld();
-      const float4* d4 = reinterpret_cast<const float4*>(dvec);
+      // dP^T - D came from the tensor core
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 dv4 = d4[c];
-        pk2[2 * c] = pack_bf16(p[4 * c] * (__uint_as_float(r[4 * c]) - dv4.x),
-                               p[4 * c + 1] * (__uint_as_float(r[4 * c + 1]) - dv4.y));
-        pk2[2 * c + 1] = pack_bf16(p[4 * c + 2] * (__uint_as_float(r[4 * c + 2]) - dv4.z),
-                                   p[4 * c + 3] * (__uint_as_float(r[4 * c + 3]) - dv4.w));
-      }
+      for (int c = 0; c < 32; ++c)
+        pk2[c] = pack_bf16(p[2 * c] * __uint_as_float(r[2 * c]),
+                           p[2 * c + 1] * __uint_as_float(r[2 * c + 1]));
       tmem_st32(tmem + lane_off + kColS + 64 * w + 32, pk2);
       // The dS buffer doubles as the dQ staging area of the previous step: wait
       // until the TMA has read it.

@@ -215,6 +215,28 @@ __device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32
       : "memory");
 }
 
+// No-swizzle K-major operand of K = 16 (two 8 x 16-byte core matrices per
+// 8-row group): core matrix (row group g, K half h) at g * 256 + h * 128 bytes,
+// its 8 rows 16 bytes apart; lbo = 128 (next K half), sbo = 256 (next 8 rows),
+// swizzle mode 0.
+constexpr uint32_t kSdescHiNoSwizzle = ((256u >> 4) & 0x3FFFu) | (1u << 14);
+__device__ __forceinline__ uint32_t sdesc_lo_nosw(uint32_t saddr) {
+  return ((saddr & 0x3FFFFu) >> 4) | ((128u >> 4) << 16);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, both operands no-swizzle K-major
+__device__ __forceinline__ void mma_ss_nosw(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %5};\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSdescHiNoSwizzle)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem] with a split B descriptor
 __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                           uint32_t idesc, uint32_t accumulate) {
