@@ -49,8 +49,9 @@ constexpr int NV = 4;    // per-step vector ring entries
 // vector entry: query ids, pos (128 each), then the step's tile class
 constexpr int kVecEntry = 2 * 128 + 32;
 // Per-step augment tile (no-swizzle K-major, 128 query rows x 16 bf16): row q
-// holds -c split into three bf16 (c = LSE / scale, so that scale * (S - c) is
-// the exponent of P in the base-2 domain) and -D split likewise, then zeros.
+// holds -c split into three bf16 (c = (LSE - ln scale) / scale, so that
+// 2^(scale log2(e) (S - c)) = scale * P: P and dS carry the factor that dK and
+// dQ need, and dV divides it back out) and -D split likewise, then zeros.
 // With the constant "ones" tiles E_S (ones in columns 0-2) and E_D (ones in
 // columns 3-5) as A, one extra K = 16 MMA step makes the tensor core deliver
 // S^T - c and dP^T - D, so no per-column vector is read in the element-wise
@@ -97,6 +98,7 @@ struct BwdArgs {
   int64_t kv_stride;  // elements between consecutive tokens of dk / dv
   float scale;
   float scale_log2;
+  float c_shift;  // -ln(scale) / scale: added to c so that the exponent gives scale * P
 };
 
 template <int D>
@@ -461,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         vi[r] = vid[u];
         vi[BM + r] = vps[u];
         // -c and -D, each as three bf16 whose sum is the fp32 value
-        const float c = (vl[u] == -INFINITY) ? kAugNoKeys : vl[u] * inv_scale;
+        const float c = (vl[u] == -INFINITY) ? kAugNoKeys : vl[u] * inv_scale + a.c_shift;
         uint32_t cs[3], ds[3];
         split_bf16x3(-c, cs);
         split_bf16x3(-vd[u], ds);
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_off + kColS + 64 * w, &r[0]);
       tmem_ld32(tmem + lane_off + kColS + 64 * w + 32, &r[32]);
       tmem_wait_ld();
-      // the tensor core already subtracted c = LSE / scale: P = 2^(scale log2(e) (S - c))
+      // the tensor core already subtracted c: p = 2^(scale log2(e) (S - c)) = scale * P
       float p[64];
 #pragma unroll
       for (int u = 0; u < 64; ++u) p[u] = ex2(__uint_as_float(r[u]) * sl2);
@@ -581,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
-      // dQ (x scale) into the fp32 accumulator.  Half 0 stages its columns in
+      // dQ (scaled already: dS carries the factor) into the fp32 accumulator.  Half 0 stages its columns in
       // the dS buffer (free: the dQ MMA has read it), half 1 in the Q stage of
       // this step (free once dK, its last reader, is done), as 32-column boxes
       // of 128 rows x 128 B (128B-swizzled); warp 3 issues the reduce-adds.
@@ -592,16 +594,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       {
         uint8_t* stage = (w == 0) ? smem + L::ds_off : smem + L::q_off + (t % NQ) * L::kTile;
-        const float sc = a.scale;
 #pragma unroll
         for (int k = 0; k < kRounds; ++k) {
           uint8_t* box = stage + k * L::kChunk + kr * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const float4 v4 = make_float4(__uint_as_float(q[32 * k + 4 * u]) * sc,
-                                          __uint_as_float(q[32 * k + 4 * u + 1]) * sc,
-                                          __uint_as_float(q[32 * k + 4 * u + 2]) * sc,
-                                          __uint_as_float(q[32 * k + 4 * u + 3]) * sc);
+            const float4 v4 = make_float4(__uint_as_float(q[32 * k + 4 * u]),
+                                          __uint_as_float(q[32 * k + 4 * u + 1]),
+                                          __uint_as_float(q[32 * k + 4 * u + 2]),
+                                          __uint_as_float(q[32 * k + 4 * u + 3]));
             *reinterpret_cast<float4*>(box + ((u ^ (kr & 7)) * 16)) = v4;
           }
         }
@@ -618,7 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     if (ok) {
-      const float sc = (w == 0) ? 1.f : a.scale;
+      // P was formed as scale * P (so dS too): dK and dQ carry their factor
+      // already, dV takes it back out
+      const float sc = (w == 0) ? 1.f / a.scale : 1.f;
       const int64_t row0 = ((int64_t)bi * a.s_kv + key) * a.kv_stride + (int64_t)kvh * D;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
@@ -700,6 +703,7 @@ cudaError_t launch_attn_bwd(const BwdLaunch& Lc, cudaStream_t st) {
   a.kv_stride = f.kv_token_stride > 0 ? f.kv_token_stride : f.h_kv * f.d;
   a.scale = f.scale;
   a.scale_log2 = f.scale * kLog2e;
+  a.c_shift = -logf(f.scale) / f.scale;
   const int64_t units = f.b * Lc.nk * f.h_kv;
   if (units == 0) return cudaSuccess;
   if (f.d == 128) {
