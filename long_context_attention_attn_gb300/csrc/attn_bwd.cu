@@ -514,7 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the tensor core already subtracted c: p = 2^(scale log2(e) (S - c)) = scale * P
       float p[64];
 #pragma unroll
-      for (int u = 0; u < 64; ++u) p[u] = ex2(__uint_as_float(r[u]) * sl2);
+      for (int u = 0; u < 64; u += 2) {
+        float x0, x1;
+        mul_f32x2(x0, x1, __uint_as_float(r[u]), __uint_as_float(r[u + 1]), sl2, sl2);
+        p[u] = ex2(x0);
+        p[u + 1] = ex2(x1);
+      }
       if (partial) {
         const int4* id4 = reinterpret_cast<const int4*>(qid);
         const int4* ps4 = reinterpret_cast<const int4*>(qpos);
@@ -549,9 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       // dP^T - D came from the tensor core
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        pk2[c] = pack_bf16(p[2 * c] * __uint_as_float(r[2 * c]),
-                           p[2 * c + 1] * __uint_as_float(r[2 * c + 1]));
+      for (int c = 0; c < 32; ++c) {
+        float d0, d1;
+        mul_f32x2(d0, d1, p[2 * c], p[2 * c + 1], __uint_as_float(r[2 * c]),
+                  __uint_as_float(r[2 * c + 1]));
+        pk2[c] = pack_bf16(d0, d1);
+      }
       tmem_st32(tmem + lane_off + kColS + 64 * w + 32, pk2);
       // The dS buffer doubles as the dQ staging area of the previous step: wait
       // until the TMA has read it.

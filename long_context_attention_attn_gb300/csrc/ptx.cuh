@@ -237,6 +237,19 @@ __device__ __forceinline__ void mma_ss_nosw(uint32_t d_tmem, uint32_t a_lo, uint
       : "memory");
 }
 
+// Two fp32 products in one packed instruction: (d0, d1) = (a0 * b0, a1 * b1),
+// each rounded to nearest even.
+__device__ __forceinline__ void mul_f32x2(float& d0, float& d1, float a0, float a1, float b0,
+                                          float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // D[tmem] (+)= A[tmem] * B[smem] with a split B descriptor
 __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                           uint32_t idesc, uint32_t accumulate) {
