@@ -446,14 +446,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // packed bf16 P overwrites the front of the score registers
 #pragma unroll
         for (int c = 0; c < BN; c += 4) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, -msub));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -msub));
-          const float p2 = ex2(fmaf(__uint_as_float(sr[c + 2]), sl2, -msub));
-          const float p3 = ex2(fmaf(__uint_as_float(sr[c + 3]), sl2, -msub));
-          s0 += p0;
-          s1 += p1;
-          s2 += p2;
-          s3 += p3;
+          float p0, p1, p2, p3;
+          if constexpr (kSlots<DK, DV> == 2) {
+            // two softmax warps per SM sub-partition: issue slots are the limit,
+            // so exponent arguments and running sums go two lanes per instruction
+            float x0, x1, x2, x3;
+            fma_f32x2(x0, x1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2,
+                      -msub, -msub);
+            fma_f32x2(x2, x3, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]), sl2, sl2,
+                      -msub, -msub);
+            p0 = ex2(x0);
+            p1 = ex2(x1);
+            p2 = ex2(x2);
+            p3 = ex2(x3);
+            add_f32x2(s0, s1, s0, s1, p0, p1);
+            add_f32x2(s2, s3, s2, s3, p2, p3);
+          } else {
+            // one softmax warp per sub-partition: latency is the limit
+            p0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, -msub));
+            p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -msub));
+            p2 = ex2(fmaf(__uint_as_float(sr[c + 2]), sl2, -msub));
+            p3 = ex2(fmaf(__uint_as_float(sr[c + 3]), sl2, -msub));
+            s0 += p0;
+            s1 += p1;
+            s2 += p2;
+            s3 += p3;
+          }
           sr[c / 2] = pack_bf16(p0, p1);
           sr[c / 2 + 1] = pack_bf16(p2, p3);
         }

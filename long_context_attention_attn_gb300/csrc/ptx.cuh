@@ -250,6 +250,31 @@ __device__ __forceinline__ void mul_f32x2(float& d0, float& d1, float a0, float 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) in one packed instruction
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0,
+                                          float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// (d0, d1) = (a0 + b0, a1 + b1) in one packed instruction
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1, float b0,
+                                          float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // D[tmem] (+)= A[tmem] * B[smem] with a split B descriptor
 __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                           uint32_t idesc, uint32_t accumulate) {
