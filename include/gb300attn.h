@@ -164,7 +164,9 @@ GB300ATTN_API int attn_fwd(const attn_fwd_params* p, attn_stream_t stream);
 /* Backward attention: D = rowsum(dO*O), fused dQ/dK/dV kernel, dQ finalise.
  * d must be 64 or 128: at d = 256 a 128-key tile's dK and dV alone would fill
  * the 512 TMEM columns of a CTA, so d = 256 returns ATTN_ERR_UNSUPPORTED
- * before any launch. */
+ * before any launch.  scale must be at least 1e-30 (ATTN_ERR_UNSUPPORTED
+ * otherwise): the kernel subtracts (LSE - ln scale) / scale from S on the
+ * tensor core, which must stay within the fp32 range. */
 GB300ATTN_API int attn_bwd(const attn_bwd_params* p, attn_stream_t stream);
 
 /* Online-softmax merge of a partial result into an accumulator, per row-head.

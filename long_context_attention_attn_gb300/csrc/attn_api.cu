@@ -189,6 +189,8 @@ size_t attn_bwd_workspace_bytes(const attn_bwd_params* p) {
   return L.end + d_bytes + dq_bytes;
 }
 
+constexpr float kBwdMinScale = 1e-30f;
+
 int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   if (!p) return ATTN_ERR_INVALID_ARG;
   int rc = check_fwd(&p->fwd);
@@ -196,6 +198,9 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   if (p->fwd.out_fp32 || p->fwd.merge_into_out || p->fwd.out_final) return ATTN_ERR_INVALID_ARG;
   // d = 256: dK and dV of a 128-key tile alone would fill the 512 TMEM columns
   if (p->fwd.d > 128 || fwd_dv(&p->fwd) != p->fwd.d) return ATTN_ERR_UNSUPPORTED;
+  // The kernel feeds (LSE - ln scale) / scale to the tensor core as bf16
+  // parts; below 1e-30 that value could leave the fp32 range.
+  if (p->fwd.scale < kBwdMinScale) return ATTN_ERR_UNSUPPORTED;
   if (!p->dout || !p->dq || !p->dk || !p->dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned(p->dout, 16) || !aligned(p->dq, 16) || !aligned(p->dk, 16) || !aligned(p->dv, 16))
     return ATTN_ERR_INVALID_ARG;

@@ -122,6 +122,11 @@ def test_bwd_rejects_invalid_arguments_on_host(ga):
     assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 2
     bp.fwd.d, bp.fwd.d_v = 80, 0
     assert ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp)) == 0
+    # a scale the forward takes but the backward does not: (LSE - ln scale) /
+    # scale would leave the fp32 range
+    bp.fwd.d = 128
+    bp.fwd.scale = 1e-35
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 2
 
 
 @pytest.mark.parametrize("args,code", [
