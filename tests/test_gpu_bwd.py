@@ -100,6 +100,20 @@ def test_cross_descriptor_and_lengths(ga, s_q, s_kv, q0, window, d, seed):
     blind = torch.from_numpy(np.abs(ro).sum(axis=(2, 3)) == 0)
     assert torch.all(dq.cpu()[blind] == 0)
 
+
+@pytest.mark.parametrize("scale", [1.0, 2.5, 0.01])
+def test_scale_other_than_inverse_sqrt_d(ga, scale):
+    """The backward carries the softmax scale on P (its exponent is shifted by
+    ln(scale)); scales at and above 1 and far below 1/sqrt(d) exercise both
+    signs of that shift."""
+    b, s, hq, hkv, d, window, seed = 1, 300, 4, 2, 128, 90, 21
+    q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=seed, with_dout=True)
+    if scale >= 1:  # keep the scores in the range a trained model produces
+        q, k = (q.float() * 0.3).to(torch.bfloat16), (k.float() * 0.3).to(torch.bfloat16)
+    ids, pos = workload.random_segments(b, s, seed=seed)
+    x = dict(q=q, k=k, v=v, dout=dout, ids=ids, pos=pos)
+    _full_check(ga, x, window, scale)
+
 def _sampled(ga, name, dq_samples, key_samples):
     w = workload.WORKLOADS[name]
     x = workload.make(w, device=DEV, with_dout=True)
