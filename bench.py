@@ -43,10 +43,18 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload fwd / bwd, ring and all-gather timings")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload name (the headline number is full_swa_64k; smaller ones "
                          "serve profiling)")
     return ap.parse_args()
+
+
+def median(xs):
+    xs = sorted(xs)
+    n = len(xs)
+    return xs[n // 2] if n % 2 else 0.5 * (xs[n // 2 - 1] + xs[n // 2])
 
 
 def max_over_ranks(value, dist=None, device="cpu"):
@@ -270,6 +278,91 @@ def hbm_components(ga, dev, pk):
     return out
 
 
+def _timed_calls(fn, iters=10, warmup=3):
+    """Median CUDA-event time (ms) of single calls of fn on the current stream."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return median(times)
+
+
+def per_config(ga, dev, pk, big=None):
+    """fwd / bwd TFLOP/s (valid pairs; medians of 10 single calls after 3
+    warm-ups) on every workload of the pages' set, the ring workload as one
+    call, as R = 4 logical ring shards (fused and separate merge, forward and
+    backward), and the all-gather strategy at the tutorial's 64k shape with
+    stripe 512 (``big`` = the resident full_swa_64k inputs, if any)."""
+    import torch
+
+    import workload
+    from long_context_attention_attn_gb300 import ring
+
+    res = {}
+    for name in ("tiny", "packed_thd", "packed_swa", "ring_cp4"):
+        w = workload.WORKLOADS[name]
+        pairs = valid_pairs(w)
+        x = workload.make(w, device=dev, with_dout=True)
+        q, k, v, ids, pos, dout = x["q"], x["k"], x["v"], x["ids"], x["pos"], x["dout"]
+        ws = torch.empty(ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(w.b, w.hq, w.s, dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        fwd = lambda: ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale,
+                                  out=out, lse=lse, workspace=ws)
+        bwd = lambda: ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=w.window_left,
+                                  scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        f_ms = _timed_calls(fwd)
+        b_ms = _timed_calls(bwd)
+        if ga.read_device_status(ws) != 0:
+            raise RuntimeError(f"{name}: device status {ga.read_device_status(ws)}")
+        ff, bf = 4 * w.d * w.hq * pairs, 10 * w.d * w.hq * pairs
+        res[name] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "fwd_tflops": ff / f_ms / 1e9,
+                     "bwd_tflops": bf / b_ms / 1e9, "step_tflops": (ff + bf) / (f_ms + b_ms) / 1e9,
+                     "valid_pairs_per_head": pairs}
+        if name == "ring_cp4":
+            R = w.cp_size
+            kw = dict(window_left=w.window_left, scale=w.scale, check_status=False)
+            rf = lambda: ring.ring_attn_fwd(q, k, v, ids, pos, R, fused_merge=True, **kw)
+            rs = lambda: ring.ring_attn_fwd(q, k, v, ids, pos, R, fused_merge=False, **kw)
+            rb = lambda: ring.ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, R, **kw)
+            fused_ms, sep_ms, rb_ms = _timed_calls(rf), _timed_calls(rs), _timed_calls(rb)
+            res["ring_cp4_shards"] = {
+                "what": f"{R} logical dual-chunk ring shards: reorder, {R}x{R} block attn_fwd "
+                        "calls with the merge folded into the epilogue (fused) or as a separate "
+                        "attn_merge_partial pass, inverse reorder; backward: per-block attn_bwd "
+                        "in fp32 accumulate mode with the final LSE",
+                "fwd_fused_ms": fused_ms, "fwd_separate_ms": sep_ms, "bwd_ms": rb_ms,
+                "fwd_fused_tflops": ff / fused_ms / 1e9, "fwd_separate_tflops": ff / sep_ms / 1e9,
+                "bwd_tflops": bf / rb_ms / 1e9}
+        del x, q, k, v, ids, pos, dout, ws, out, lse, dq, dk, dv
+        torch.cuda.empty_cache()
+    if big is not None:
+        w = workload.WORKLOADS["full_swa_64k"]
+        pairs = valid_pairs(w)
+        ag = lambda: ring.allgather_attn_fwd(big["q"], big["k"], big["v"], big["ids"], big["pos"],
+                                             4, window_left=w.window_left, scale=w.scale,
+                                             stripe_size=512, check_status=False)
+        ag_ms = _timed_calls(ag, iters=5)
+        ff = 4 * w.d * w.hq * pairs
+        res["allgather_64k"] = {
+            "what": "full_swa_64k as 4 logical all-gather shards (striped reorder, stripe 512; "
+                    "each shard's queries against the whole reordered K/V in one attn_fwd; "
+                    "inverse reorder)",
+            "fwd_ms": ag_ms, "fwd_tflops": ff / ag_ms / 1e9}
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_reference(args, rank):
     import workload
     w = workload.WORKLOADS[args.workload]
@@ -369,10 +462,9 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    fwd_ms = sorted(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = sorted(e[1].elapsed_time(e[2]) for e in evs)
-    fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    bwd_avg = sum(bwd_ms) / len(bwd_ms)
+    # per-call figures: medians over the timed steps
+    fwd_avg = median([e[0].elapsed_time(e[1]) for e in evs])
+    bwd_avg = median([e[1].elapsed_time(e[2]) for e in evs])
     ms_per_step = max_over_ranks(total_ms / args.steps, dist, dev)
     value = whole_job_tflops(world, fwd_flop + bwd_flop, ms_per_step)
 
@@ -474,6 +566,9 @@ def run_ours(args, rank, world, local_rank):
                                        fwd_tflops, pk, clocks)), flush=True)
         return
     hbm = hbm_components(ga, dev, pk)
+    per_cfg = None
+    if not args.no_per_config:
+        per_cfg = per_config(ga, dev, pk, big=x)
     bwd_tflops = bwd_flop / (bwd_avg * 1e-3) / 1e12
     per_gpu = value / world
     cpu = None
@@ -503,7 +598,8 @@ def run_ours(args, rank, world, local_rank):
                        "bwd_tflops": bwd_tflops,
                        "fwd_pct_of_burst_peak": 100 * fwd_tflops / pk["bf16_burst"],
                        "bwd_pct_of_burst_peak": 100 * bwd_tflops / pk["bf16_burst"],
-                       "hbm_rows": hbm},
+                       "timing": "medians of the timed steps' per-call CUDA events",
+                       "hbm_rows": hbm, "per_config": per_cfg},
         "roofline": {"kernel": "attn_bwd (fused backward + its D pre-pass, plan and dQ "
                                "finalise; timed per call)",
                      "bound": "tensor", "achieved": bwd_tflops, "peak": pk["bf16_sustained"],

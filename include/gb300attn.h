@@ -266,14 +266,26 @@ GB300ATTN_API int attn_read_device_status(const void* workspace, attn_stream_t s
  *    the process exits.  Problems whose attn_fwd_workspace_bytes() exceeds
  *    4 MiB are rejected with ATTN_ERR_UNSUPPORTED (about b * ceil(s_q/128) *
  *    ceil(s_kv/128) <= 3.5M tiles, e.g. b=2 with s=160k).
- *  - No cudaMalloc / cudaFree or other allocating call is made.  The first
- *    call on a device looks up the array's device address (cudaGetSymbolAddress
- *    with that device current); make that first call before any stream capture.
+ *  - No cudaMalloc / cudaFree or other allocating call is made.  Every call
+ *    looks up the array's device address (cudaGetSymbolAddress, with the
+ *    caller's device current); the first call on a device also loads the
+ *    library's module there, so make that first call before any stream
+ *    capture.
  *  - All calls share the one array and it keeps the last call's contents (the
  *    status word is cleared at the start of every call): calls that overlap on
  *    the GPU (different streams, or different host threads) race on it.
+ *  - A device-side timeout (see ATTN_ERR_TIMEOUT) is recorded in that array's
+ *    status word, not returned: read it with attn_fwd_noalloc_status.
  */
 GB300ATTN_API int attn_fwd_noalloc(const attn_fwd_params* p, attn_stream_t stream);
+
+/* Synchronises `stream`, then returns the status word of attn_fwd_noalloc's
+ * scratch on the current device (the counterpart of attn_read_device_status
+ * for that entry point): ATTN_OK, or ATTN_ERR_TIMEOUT if a bounded wait of
+ * the last attn_fwd_noalloc on this device gave up, its outputs then being
+ * undefined.  ATTN_ERR_CUDA if the stream or the copy fails.  The pages have
+ * no counterpart to this call either. */
+GB300ATTN_API int attn_fwd_noalloc_status(attn_stream_t stream);
 
 /* Static description of a status code. */
 GB300ATTN_API const char* attn_status_string(int status);

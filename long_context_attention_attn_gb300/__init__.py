@@ -25,7 +25,7 @@ EXPORTS = (
     "attn_fwd_workspace_bytes", "attn_bwd_workspace_bytes", "attn_fwd", "attn_bwd",
     "attn_merge_partial", "reorder_causal_lb", "inverse_reorder_causal_lb", "attn_tile_plan",
     "attn_read_device_status", "attn_status_string", "attn_fwd_noalloc",
-    "attn_fwd_test_timeout", "attn_segments_from_seqlens",
+    "attn_fwd_test_timeout", "attn_segments_from_seqlens", "attn_fwd_noalloc_status",
 )
 
 
@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
         h.attn_fwd_test_timeout.restype = c_int
         h.attn_fwd_noalloc.argtypes = [ctypes.POINTER(FwdParams), vp]
         h.attn_fwd_noalloc.restype = c_int
+        h.attn_fwd_noalloc_status.argtypes = [vp]
+        h.attn_fwd_noalloc_status.restype = c_int
         h.attn_segments_from_seqlens.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
         h.attn_segments_from_seqlens.restype = c_int
         h.attn_status_string.argtypes = [c_int]
@@ -181,7 +183,7 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: int = -1,
              scale: Optional[float] = None, out=None, lse=None, out_fp32: bool = False,
              merge_into_out: bool = False, out_final=None,
-             workspace: Optional[torch.Tensor] = None):
+             workspace: Optional[torch.Tensor] = None, check_status: bool = False):
     """Forward attention.  Returns (out [b,s_q,Hq,d_v], lse fp32 [b,Hq,s_q]).
 
     q bf16 [b,s_q,Hq,d]; k bf16 [b,s_kv,Hkv,d]; v bf16 [b,s_kv,Hkv,d_v] (d_v = d,
@@ -190,7 +192,36 @@ def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: in
     With ``merge_into_out`` the given fp32 ``out`` / ``lse`` hold a finished
     partial over other key blocks and this call's result is merged into them
     (into bf16 ``out_final`` instead of ``out`` when given).
+    ``check_status`` synchronises the stream after the launch and raises
+    :class:`AttnError` (``ATTN_ERR_TIMEOUT``) if a bounded device-side wait gave
+    up, in which case the outputs are undefined; otherwise the call stays
+    asynchronous and the status can be read later from ``workspace`` with
+    :func:`read_device_status`.
     """
+    return _attn_fwd_call("attn_fwd", q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale,
+                          out, lse, out_fp32, merge_into_out, out_final, workspace, check_status)
+
+
+def attn_fwd_test_timeout(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
+                          window_left: int = -1, scale: Optional[float] = None,
+                          workspace: Optional[torch.Tensor] = None, check_status: bool = True):
+    """Test hook: attn_fwd with every key / value load withheld, so the
+    device-side waits run out (about a second) and the launch records
+    ``ATTN_ERR_TIMEOUT``; with ``check_status`` (the default) that raises
+    :class:`AttnError` here.  Not for production use."""
+    return _attn_fwd_call("attn_fwd_test_timeout", q, k, v, q_ids, q_pos, kv_ids, kv_pos,
+                          window_left, scale, None, None, False, False, None, workspace,
+                          check_status)
+
+
+def _raise_on_device_status(workspace: torch.Tensor, what: str):
+    code = read_device_status(workspace)
+    if code != ATTN_OK:
+        raise AttnError(code, what)
+
+
+def _attn_fwd_call(entry, q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse,
+                   out_fp32, merge_into_out, out_final, workspace, check_status):
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
     _need_cuda(q, q_ids, q_pos, kv_ids, kv_pos, out, lse, workspace, out_final)
@@ -218,15 +249,19 @@ def attn_fwd(q, k, v, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: in
     if workspace is None:
         workspace = _workspace(need, q.device)
     p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
-    _check(lib().attn_fwd(ctypes.byref(p), _stream(q.device)), "attn_fwd")
+    _check(getattr(lib(), entry)(ctypes.byref(p), _stream(q.device)), entry)
+    if check_status:
+        _raise_on_device_status(workspace, entry)
     return out, lse
 
 
 def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
              window_left: int = -1, scale: Optional[float] = None, dq=None, dk=None, dv=None,
-             accumulate_fp32: bool = False, workspace: Optional[torch.Tensor] = None):
+             accumulate_fp32: bool = False, workspace: Optional[torch.Tensor] = None,
+             check_status: bool = False):
     """Backward attention.  Returns (dq, dk, dv): bf16, or with
-    ``accumulate_fp32`` the given fp32 tensors with this call's gradients added."""
+    ``accumulate_fp32`` the given fp32 tensors with this call's gradients added.
+    ``check_status`` as in :func:`attn_fwd`."""
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
     _need_cuda(q, out, lse, dout, q_ids, q_pos, kv_ids, kv_pos, workspace, dq)
@@ -256,6 +291,8 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
         workspace = _workspace(need, q.device)
     p.fwd.workspace, p.fwd.workspace_bytes = workspace.data_ptr(), workspace.numel()
     _check(lib().attn_bwd(ctypes.byref(p), _stream(q.device)), "attn_bwd")
+    if check_status:
+        _raise_on_device_status(workspace, "attn_bwd")
     return dq, dk, dv
 
 
@@ -356,3 +393,10 @@ def attn_tile_plan(q, k, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left:
 def read_device_status(workspace: torch.Tensor) -> int:
     """Synchronise the current stream and read the device status word."""
     return int(lib().attn_read_device_status(_ptr(workspace), _stream(workspace.device)))
+
+
+def noalloc_status() -> int:
+    """Synchronise the current stream and read the status word of
+    attn_fwd_noalloc's built-in scratch on the current device."""
+    dev = torch.cuda.current_device()
+    return int(lib().attn_fwd_noalloc_status(_stream(dev)))

@@ -13,32 +13,23 @@
 // The array is a file-scope __device__ variable: every GPU that loads this
 // library holds its kAttnNoAllocScratchBytes until the process exits.  In
 // host code the array's name is only a host-side stand-in, so its device
-// address is looked up once per device with cudaGetSymbolAddress (with that
-// device current) and cached.
-#include <mutex>
-
+// address is looked up with cudaGetSymbolAddress, with the caller's device
+// current, on every call.  Once the library's module is loaded on a device
+// that lookup allocates nothing; repeating it instead of caching the pointer
+// keeps the address right after a cudaDeviceReset or a primary-context
+// teardown, which load the module again at a new address.
 #include "internal.h"
 
 namespace {
 
 constexpr size_t kAttnNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) uint8_t g_fwd_scratch[kAttnNoAllocScratchBytes];
 
-// Device address of g_fwd_scratch on the current device (set up on first use).
+// Device address of g_fwd_scratch on the current device, or null.
 void* scratch_on_current_device() {
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 }  // namespace
@@ -59,4 +50,13 @@ extern "C" GB300ATTN_API int attn_fwd_noalloc(const attn_fwd_params* p, attn_str
   q.workspace = ws;
   q.workspace_bytes = kAttnNoAllocScratchBytes;
   return attn_fwd(&q, stream);
+}
+
+// The status word of the scratch above on the current device: ATTN_OK, or
+// ATTN_ERR_TIMEOUT when a bounded device-side wait of the last
+// attn_fwd_noalloc on this device gave up (its outputs are then undefined).
+extern "C" GB300ATTN_API int attn_fwd_noalloc_status(attn_stream_t stream) {
+  void* ws = scratch_on_current_device();
+  if (!ws) return ATTN_ERR_CUDA;
+  return attn_read_device_status(ws, stream);
 }

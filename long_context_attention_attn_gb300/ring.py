@@ -22,20 +22,44 @@ from typing import Optional
 
 import torch
 
-from . import (DUAL_CHUNK, STRIPED, attn_bwd, attn_fwd, attn_merge_partial,
+from . import (ATTN_OK, DUAL_CHUNK, STRIPED, AttnError, attn_bwd, attn_fwd, attn_merge_partial,
                inverse_reorder_causal_lb, reorder_causal_lb, workspace_bytes_bwd,
                workspace_bytes_fwd)
 
 
+class _StatusLog:
+    """The device status word of every attention call of a driver run.
+
+    Each call clears its workspace's status word when it starts, so the word
+    is copied aside (a 4-byte device-to-device copy, no kernel) after every
+    call and all copies are read once, with one synchronisation, at the end."""
+
+    def __init__(self, n: int, device):
+        self.words = torch.zeros(max(n, 1), dtype=torch.int32, device=device)
+        self.n = 0
+
+    def record(self, ws: torch.Tensor):
+        self.words[self.n:self.n + 1].copy_(ws[:4].view(torch.int32))
+        self.n += 1
+
+    def check(self, what: str):
+        worst = int(self.words[:self.n].max().item()) if self.n else ATTN_OK
+        if worst != ATTN_OK:
+            raise AttnError(worst, what)
+
+
 def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
                   scale: Optional[float] = None, strategy: int = DUAL_CHUNK, stripe_size: int = 1,
-                  fused_merge: bool = True):
+                  fused_merge: bool = True, check_status: bool = True):
     """Forward attention computed as cp_size ring steps per logical shard.
 
     q bf16 [b,s,Hq,d]; k, v bf16 [b,s,Hkv,d]; ids/pos int32 [b,s] (natural
     order).  Returns (out bf16 [b,s,Hq,d], lse fp32 [b,Hq,s]) in natural order.
     ``fused_merge`` folds each step's partial into the running result in the
     attention kernel's epilogue; otherwise a separate merge pass runs per step.
+    ``check_status`` reads every call's device status word once at the end
+    (one synchronisation) and raises :class:`AttnError` if a bounded
+    device-side wait gave up, rather than returning undefined output.
     """
     b, s, hq, d = q.shape
     R = int(cp_size)
@@ -55,6 +79,7 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
     ws = torch.empty(workspace_bytes_fwd(qr[:1, :n], kr[:1, :n], idr[:1, :n], posr[:1, :n],
                                          window_left=window_left),
                      dtype=torch.uint8, device=dev)
+    log = _StatusLog(b * R * R, dev) if check_status else None
     for bi in range(b):
         for r in range(R):
             rows = slice(r * n, (r + 1) * n)
@@ -80,6 +105,8 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
                              scale=scale, out=blk, lse=blk_lse, out_fp32=True, workspace=ws)
                     attn_merge_partial(acc, lacc, blk, blk_lse,
                                        out_final=out_r[:, rows] if t == R - 1 else None)
+                if log is not None:
+                    log.record(ws)
         # [R, Hq, n] -> [Hq, R*n]: a block transpose, done as a striped permutation
         # of R*Hq stripes of n values over Hq logical shards.
         lse_t = reorder_causal_lb(lse_sh.view(1, R * hq * n), STRIPED, hq, n, seq_dim=1)
@@ -87,12 +114,14 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
                                   out=lse[bi])
         inverse_reorder_causal_lb(out_r, strategy, R, stripe_size, seq_dim=1,
                                   out=out[bi:bi + 1])
+    if log is not None:
+        log.check("ring_attn_fwd")
     return out, lse
 
 
 def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
                        scale: Optional[float] = None, strategy: int = STRIPED,
-                       stripe_size: int = 512):
+                       stripe_size: int = 512, check_status: bool = True):
     """All-gather context parallelism on one GPU (TE tutorial section 5,
     "AllGather" with a striped reorder, stripe_size 512; "Context parallelism
     and ring attention", section "Communication choices").
@@ -102,7 +131,7 @@ def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1
     reordered K/V (what an all-gather of K/V would give every device).  The
     mask uses the reordered segment positions, so the result equals full
     attention.  Returns (out bf16 [b,s,Hq,d], lse fp32 [b,Hq,s]) in natural
-    token order.
+    token order.  ``check_status`` as in :func:`ring_attn_fwd`.
     """
     b, s, hq, d = q.shape
     R = int(cp_size)
@@ -119,6 +148,7 @@ def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1
     ws = torch.empty(workspace_bytes_fwd(qr[:1, :n], kr[:1], idr[:1, :n], posr[:1, :n],
                                          idr[:1], posr[:1], window_left=window_left),
                      dtype=torch.uint8, device=dev)
+    log = _StatusLog(b * R, dev) if check_status else None
     for bi in range(b):
         kv = (kr[bi:bi + 1], vr[bi:bi + 1], idr[bi:bi + 1], posr[bi:bi + 1])
         for r in range(R):
@@ -126,17 +156,21 @@ def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1
             attn_fwd(qr[bi:bi + 1, rows], kv[0], kv[1], idr[bi:bi + 1, rows],
                      posr[bi:bi + 1, rows], kv[2], kv[3], window_left=window_left, scale=scale,
                      out=out_r[:, rows], lse=lse_sh[r:r + 1], workspace=ws)
+            if log is not None:
+                log.record(ws)
         lse_t = reorder_causal_lb(lse_sh.view(1, R * hq * n), STRIPED, hq, n, seq_dim=1)
         inverse_reorder_causal_lb(lse_t.view(hq, s), strategy, R, stripe_size, seq_dim=1,
                                   out=lse[bi])
         inverse_reorder_causal_lb(out_r, strategy, R, stripe_size, seq_dim=1,
                                   out=out[bi:bi + 1])
+    if log is not None:
+        log.check("allgather_attn_fwd")
     return out, lse
 
 
 def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_left: int = -1,
                   scale: Optional[float] = None, strategy: int = DUAL_CHUNK,
-                  stripe_size: int = 1):
+                  stripe_size: int = 1, check_status: bool = True):
     """Backward of ring attention, emulated on one GPU.
 
     Shard r keeps its query rows, final output O_r, LSE_r and dO_r; at step t
@@ -150,6 +184,7 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
 
     out / lse: the forward results in natural order (e.g. from ring_attn_fwd).
     Returns fp32 (dq [b,s,Hq,d], dk, dv [b,s,Hkv,d]) in natural order.
+    ``check_status`` as in :func:`ring_attn_fwd`.
     """
     b, s, hq, d = q.shape
     hkv = k.shape[2]
@@ -168,6 +203,7 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
     ws = torch.empty(workspace_bytes_bwd(qr[:1, :n], kr[:1, :n], idr[:1, :n], posr[:1, :n],
                                          window_left),
                      dtype=torch.uint8, device=dev)
+    log = _StatusLog(b * R * R, dev) if check_status else None
     for bi in range(b):
         # this row's LSE in reordered order, then [Hq, R*n] -> [R, Hq, n] so that
         # every shard's LSE is contiguous (the inverse of a striped block transpose)
@@ -185,5 +221,9 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
                          posr[bi:bi + 1, rk], window_left=window_left, scale=scale,
                          dq=dq[bi:bi + 1, rq], dk=dk[bi:bi + 1, rk], dv=dv[bi:bi + 1, rk],
                          accumulate_fp32=True, workspace=ws)
+                if log is not None:
+                    log.record(ws)
+    if log is not None:
+        log.check("ring_attn_bwd")
     inv = lambda x: inverse_reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
     return inv(dq), inv(dk), inv(dv)

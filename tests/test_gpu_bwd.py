@@ -191,3 +191,42 @@ def test_packed_kv_layout_fwd_bwd():
     check_grad(dq.cpu(), gq, "dq")
     check_grad(dk.cpu(), gk, "dk")
     check_grad(dv.cpu(), gv, "dv")
+
+
+def test_full_swa_64k_whole_slot_of_one_group(ga):
+    """The 64k workload in the benchmark's launch configuration, checked on one
+    whole slot (batch row 1, tokens 16384-32767: segment 2 and its padding) of
+    one kv group (kv head 5, query heads 80-95): every element of out, lse, dQ,
+    dK and dV there.  Segments see only themselves, so the oracle run on the
+    slot's tokens alone gives exactly these rows, and dK / dV of the slot's keys
+    are complete (every query row that sees them is in the slot)."""
+    import os
+    w = workload.WORKLOADS["full_swa_64k"]
+    x = workload.make(w, device=DEV, with_dout=True)
+    out, lse = ga.attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"], window_left=w.window_left,
+                           scale=w.scale)
+    dq, dk, dv = ga.attn_bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], x["ids"], x["pos"],
+                             window_left=w.window_left, scale=w.scale)
+    torch.cuda.synchronize()
+    bi, kvh, t0, t1 = 1, 5, 16384, 32768
+    g = w.hq // w.hkv
+    hs = slice(kvh * g, kvh * g + g)
+    cut = lambda t, h: t[bi:bi + 1, t0:t1, h].cpu()
+    q, k, v, do = cut(x["q"], hs), cut(x["k"], slice(kvh, kvh + 1)), \
+        cut(x["v"], slice(kvh, kvh + 1)), cut(x["dout"], hs)
+    ids, pos = x["ids"][bi:bi + 1, t0:t1].cpu(), x["pos"][bi:bi + 1, t0:t1].cpu()
+    got = dict(out=cut(out, hs), lse=lse[bi:bi + 1, hs, t0:t1].cpu(), dq=cut(dq, hs),
+               dk=cut(dk, slice(kvh, kvh + 1)), dv=cut(dv, slice(kvh, kvh + 1)))
+    del x, out, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+    torch.set_num_threads(os.cpu_count() or 1)
+    ro, rl = A.attn_fwd(q, k, v, ids, pos, ids, pos, w.window_left, w.scale)
+    check_out(got["out"], ro)
+    check_lse(got["lse"], rl)
+    rq, rk, rv = A.attn_bwd(q, k, v, do, ids, pos, ids, pos, w.window_left, w.scale, out=ro)
+    check_grad(got["dq"], rq, "dq")
+    check_grad(got["dk"], rk, "dk")
+    check_grad(got["dv"], rv, "dv")
+    pad = ids[0] == 0
+    assert torch.all(got["out"][0, pad] == 0) and torch.all(got["dq"][0, pad] == 0)
+    assert torch.all(got["dk"][0, pad] == 0) and torch.all(got["dv"][0, pad] == 0)

@@ -152,7 +152,10 @@ def test_segments_from_seqlens_tutorial_row():
 def test_concurrent_calls_from_host_threads():
     """The library keeps no per-call state: four host threads, each with its own
     stream and inputs, calling attn_fwd / attn_bwd at once get bit-identical
-    results to the same calls made one after another."""
+    out, lse, dk and dv to the same calls made one after another.  dq is
+    compared within the gradient tolerance only: its fp32 sum over key tiles
+    is formed by reduce-adds whose order the hardware schedules, so the
+    rounding of the last bits may differ from run to run."""
     import threading
     import long_context_attention_attn_gb300 as ga
     cases = []
@@ -185,6 +188,10 @@ def test_concurrent_calls_from_host_threads():
     for t in threads:
         t.join()
     torch.cuda.synchronize()
+    from tests.parity import check_grad
     for got, want in zip(results, serial):
-        for g, w in zip(got, want):
-            assert torch.equal(g, w)
+        out, lse, dq, dk, dv = got
+        for name, g, w in (("out", out, want[0]), ("lse", lse, want[1]), ("dk", dk, want[3]),
+                           ("dv", dv, want[4])):
+            assert torch.equal(g, w), name
+        check_grad(dq.cpu(), want[2].cpu(), "dq")

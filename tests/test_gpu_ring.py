@@ -158,3 +158,44 @@ def test_fwd_merge_mode_matches_oracle_merge(final):
     torch.cuda.synchronize()
     check_out((fin if final else acc).float().cpu(), want_o)
     check_lse(lacc.cpu(), want_l)
+
+
+def test_ring_backward_at_ring_workload(ring):
+    """The 32k ring workload's backward as R = 4 dual-chunk ring shards
+    (per-block attn_bwd, fp32 accumulation with the final LSE): equal to the
+    single-call backward on every element (both within the gradient
+    tolerance of each other) and to the oracle on sampled query rows (dQ) and
+    key tiles (dK, dV, complete: every row that sees those keys is included)."""
+    import long_context_attention_attn_gb300 as ga
+    from tests.parity import check_grad
+    w = workload.WORKLOADS["ring_cp4"]
+    x = workload.make(w, device=DEV, with_dout=True)
+    q, k, v, ids, pos, dout = x["q"], x["k"], x["v"], x["ids"], x["pos"], x["dout"]
+    out, lse = ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale)
+    dq, dk, dv = ring.ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, w.cp_size,
+                                    window_left=w.window_left, scale=w.scale)
+    fq, fk, fv = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=w.window_left,
+                             scale=w.scale)
+    torch.cuda.synchronize()
+    for name, a_, b_ in (("dq", dq, fq), ("dk", dk, fk), ("dv", dv, fv)):
+        num = (a_.float() - b_.float()).norm().item()
+        den = b_.float().norm().item()
+        assert num <= 1e-2 * den, f"ring vs single-call {name}: rel-L2 {num / den:.3e}"
+    g = w.hq // w.hkv
+    idc, psc = ids.cpu(), pos.cpu()
+    for kvh, r0, nr in ((0, 0, 128), (4, 20000, 64), (7, 32768 - 96, 96)):
+        hs = slice(kvh * g, kvh * g + g)
+        rows = np.arange(r0, r0 + nr)
+        rq, _, _ = A.attn_bwd(q[:, :, hs].cpu(), k[:, :, kvh:kvh + 1].cpu(),
+                              v[:, :, kvh:kvh + 1].cpu(), dout[:, :, hs].cpu(), idc, psc, idc,
+                              psc, w.window_left, w.scale, rows=rows)
+        check_grad(dq[0, r0:r0 + nr, hs].cpu(), rq[0, rows], f"dq kvh{kvh} r{r0}")
+    for kvh, k0, nk in ((2, 32768 - 128, 128), (6, 32768 - 200, 72)):
+        keys = np.arange(k0, k0 + nk)
+        rows = A.rows_seeing_keys(idc[0], psc[0], idc[0], psc[0], w.window_left, keys)
+        hs = slice(kvh * g, kvh * g + g)
+        _, rk, rv = A.attn_bwd(q[:, :, hs].cpu(), k[:, :, kvh:kvh + 1].cpu(),
+                               v[:, :, kvh:kvh + 1].cpu(), dout[:, :, hs].cpu(), idc, psc, idc,
+                               psc, w.window_left, w.scale, rows=rows)
+        check_grad(dk[0, k0:k0 + nk, kvh].cpu(), rk[0, keys, 0], f"dk kvh{kvh} k{k0}")
+        check_grad(dv[0, k0:k0 + nk, kvh].cpu(), rv[0, keys, 0], f"dv kvh{kvh} k{k0}")

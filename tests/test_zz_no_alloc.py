@@ -41,6 +41,8 @@ def test_noalloc_matches_attn_fwd_twice(name):
         lse = torch.full_like(ref_l, float("nan"))
         p = _params(ga, x, w, out, lse)
         assert ga.lib().attn_fwd_noalloc(ctypes.byref(p), stream) == ga.ATTN_OK
+        # the scratch's status word: every bounded device-side wait completed
+        assert ga.lib().attn_fwd_noalloc_status(stream) == ga.ATTN_OK
         torch.cuda.synchronize()
         check_out(out.cpu(), ref_o.float().cpu())
         check_lse(lse.cpu(), ref_l.cpu())
