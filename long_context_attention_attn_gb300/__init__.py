@@ -265,7 +265,15 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
     _need_cuda(q, out, lse, dout, q_ids, q_pos, kv_ids, kv_pos, workspace, dq)
-    kv_stride = _kv_token_stride(k, v)
+    mla = v.shape[3] != k.shape[3]
+    if mla:
+        # V narrower than Q / K (d_qk 192, d_v 128): separate, contiguous tensors
+        _need_cuda(k, v, dk, dv)
+        if v.shape[:3] != k.shape[:3]:
+            raise ValueError("k / v of different head dims must share [b, s, h]")
+        kv_stride = 0
+    else:
+        kv_stride = _kv_token_stride(k, v)
     if kv_stride and (dk is None or dv is None):
         if kv_stride != 2 * k.shape[2] * k.shape[3]:
             raise ValueError("strided k / v: pass dk and dv in the same layout")
@@ -280,7 +288,11 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _kv_token_stride(k, v, dk, dv)  # dk / dv must have the layout of k / v
+    if mla:
+        if dk.shape != k.shape or dv.shape != v.shape:
+            raise ValueError("dk / dv must have the shapes of k / v")
+    else:
+        _kv_token_stride(k, v, dk, dv)  # dk / dv must have the layout of k / v
     p = BwdParams()
     p.fwd = _fwd_params(q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, scale, out, lse, False)
     p.fwd.kv_token_stride = kv_stride
@@ -296,9 +308,12 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     return dq, dk, dv
 
 
-def workspace_bytes_bwd(q, k, q_ids, q_pos, window_left=-1) -> int:
+def workspace_bytes_bwd(q, k, q_ids, q_pos, window_left=-1, v=None) -> int:
+    """Workspace bytes attn_bwd needs for these shapes (0 if it rejects them);
+    pass ``v`` when its head dim differs from k's."""
     p = BwdParams()
-    p.fwd = _fwd_params(q, k, k, q_ids, q_pos, q_ids, q_pos, window_left, None, q, q, False)
+    p.fwd = _fwd_params(q, k, k if v is None else v, q_ids, q_pos, q_ids, q_pos, window_left,
+                        None, q, q, False)
     return int(lib().attn_bwd_workspace_bytes(ctypes.byref(p)))
 
 

@@ -2,6 +2,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "internal.h"
@@ -182,10 +183,22 @@ int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,
   return cuda_status(e);
 }
 
+// Which backward runs: the fused kernel (dQ summed through an fp32
+// accumulator in global memory) or the dK / dV kernel plus the dQ kernel.
+// The head dims whose dK and dV do not fit the fused kernel's TMEM (256, and
+// 192 / 128) take the split pair.
+static bool use_split_bwd(const attn_fwd_params* f) {
+  const int64_t dv = fwd_dv(f);
+  if (f->d == 256 || (f->d == 192 && dv == 128)) return true;
+  const char* e = getenv("GB300ATTN_BWD");
+  return e && e[0] == 's';
+}
+
 size_t attn_bwd_workspace_bytes(const attn_bwd_params* p) {
   if (!p || check_fwd(&p->fwd) != ATTN_OK) return 0;
   const PlanLayout L = fwd_layout(&p->fwd);
   const size_t d_bytes = align_up((size_t)(p->fwd.b * p->fwd.h_q * p->fwd.s_q) * 4, 256);
+  if (use_split_bwd(&p->fwd)) return L.end + d_bytes;
   const size_t dq_bytes = align_up((size_t)(p->fwd.b * p->fwd.s_q * p->fwd.h_q * p->fwd.d) * 4, 256);
   return L.end + d_bytes + dq_bytes;
 }
@@ -197,8 +210,6 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   int rc = check_fwd(&p->fwd);
   if (rc != ATTN_OK) return rc;
   if (p->fwd.out_fp32 || p->fwd.merge_into_out || p->fwd.out_final) return ATTN_ERR_INVALID_ARG;
-  // d = 256: dK and dV of a 128-key tile alone would fill the 512 TMEM columns
-  if (p->fwd.d > 128 || fwd_dv(&p->fwd) != p->fwd.d) return ATTN_ERR_UNSUPPORTED;
   // The kernel feeds (LSE - ln scale) / scale to the tensor core as bf16
   // parts; below 1e-30 that value could leave the fp32 range.
   if (p->fwd.scale < kBwdMinScale) return ATTN_ERR_UNSUPPORTED;
@@ -211,6 +222,33 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   rc = check_workspace(f, need);
   if (rc != ATTN_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t dv = fwd_dv(f);
+  if (use_split_bwd(f)) {
+    SplitLaunch sl;
+    sl.p = p;
+    sl.plan = plan_ptrs(f->workspace, L);
+    sl.nq = cdiv(f->s_q, kTile);
+    sl.nk = cdiv(f->s_kv, kTile);
+    sl.D = reinterpret_cast<float*>(static_cast<char*>(f->workspace) + L.end);
+    const int bm = split_bwd_query_rows(f->d, dv), bn = split_bwd_key_rows(f->d, dv);
+    if (!encode_qkv_map(&sl.tm_q, f->q, f->b, f->s_q, f->h_q, f->d, 0) ||
+        !encode_qkv_map(&sl.tm_do, p->dout, f->b, f->s_q, f->h_q, dv, 0) ||
+        !encode_qkv_map(&sl.tm_q_a, f->q, f->b, f->s_q, f->h_q, f->d, 0, bm) ||
+        !encode_qkv_map(&sl.tm_do_a, p->dout, f->b, f->s_q, f->h_q, dv, 0, bm) ||
+        !encode_qkv_map(&sl.tm_k, f->k, f->b, f->s_kv, f->h_kv, f->d, f->kv_token_stride) ||
+        !encode_qkv_map(&sl.tm_v, f->v, f->b, f->s_kv, f->h_kv, dv, f->kv_token_stride) ||
+        !encode_qkv_map(&sl.tm_kb, f->k, f->b, f->s_kv, f->h_kv, f->d, f->kv_token_stride, bn) ||
+        !encode_qkv_map(&sl.tm_vb, f->v, f->b, f->s_kv, f->h_kv, dv, f->kv_token_stride, bn))
+      return ATTN_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(sl.plan.status, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = launch_tile_plan(*f, sl.plan, sl.nq, sl.nk, true, st);
+    if (e == cudaSuccess)
+      e = launch_bwd_preprocess(f->out, p->dout, sl.D, nullptr, f->b, f->s_q, f->h_q, dv, st);
+    if (e == cudaSuccess) e = launch_attn_bwd_split(sl, st);
+    if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+    return cuda_status(e);
+  }
+  if (dv != f->d) return ATTN_ERR_UNSUPPORTED;
   BwdLaunch bl;
   bl.p = p;
   bl.plan = plan_ptrs(f->workspace, L);

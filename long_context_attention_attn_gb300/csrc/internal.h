@@ -153,6 +153,22 @@ struct BwdLaunch {
 };
 cudaError_t launch_attn_bwd(const BwdLaunch& L, cudaStream_t st);
 
+// ---- attn_bwd_split.cu
+// Backward as a dK / dV kernel plus a dQ kernel (no fp32 dQ accumulator).
+struct SplitLaunch {
+  const attn_bwd_params* p;
+  PlanPtrs plan;
+  int64_t nq, nk;
+  float* D;                      // [b, hq, s_q]
+  CUtensorMap tm_q, tm_do;       // 128-row boxes (dQ kernel)
+  CUtensorMap tm_q_a, tm_do_a;   // split_bwd_query_rows()-row boxes (dK / dV kernel)
+  CUtensorMap tm_k, tm_v;        // 128-row boxes (dK / dV kernel)
+  CUtensorMap tm_kb, tm_vb;      // split_bwd_key_rows()-row boxes (dQ kernel)
+};
+int split_bwd_query_rows(int64_t d, int64_t dv);
+int split_bwd_key_rows(int64_t d, int64_t dv);
+cudaError_t launch_attn_bwd_split(const SplitLaunch& L, cudaStream_t st);
+
 // ---- attn_api.cu
 bool encode_qkv_map(CUtensorMap* m, const void* base, int64_t b, int64_t s, int64_t h, int64_t d,
                     int64_t token_stride, int box_rows = kTile);

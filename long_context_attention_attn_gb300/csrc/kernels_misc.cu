@@ -500,10 +500,14 @@ __global__ void bwd_preprocess_kernel(const uint4* __restrict__ out, const uint4
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, float* zero_acc,
                                   int64_t b, int64_t s, int64_t h, int64_t d, cudaStream_t st) {
   const int64_t rows = b * s * h;
-  const int rows_per_cta = 8 * (d == 128 ? 2 : 4);
+  const int rows_per_cta = 8 * (d == 256 ? 1 : d == 128 ? 2 : 4);
   const unsigned grid =
       (unsigned)std::min<int64_t>((rows + rows_per_cta - 1) / rows_per_cta, (int64_t)sm_count() * 16);
-  if (d == 128)
+  if (d == 256)
+    bwd_preprocess_kernel<256><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
+                                                     static_cast<const uint4*>(dout), D,
+                                                     reinterpret_cast<float4*>(zero_acc), b, s, h);
+  else if (d == 128)
     bwd_preprocess_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
                                                      static_cast<const uint4*>(dout), D,
                                                      reinterpret_cast<float4*>(zero_acc), b, s, h);

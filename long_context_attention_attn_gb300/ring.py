@@ -62,6 +62,7 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
     device-side wait gave up, rather than returning undefined output.
     """
     b, s, hq, d = q.shape
+    dv = v.shape[3]  # the output takes V's head dim
     R = int(cp_size)
     if s % R:
         raise ValueError("sequence length must be divisible by cp_size")
@@ -69,15 +70,15 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
     dev = q.device
     re = lambda x: reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
     qr, kr, vr, idr, posr = re(q), re(k), re(v), re(ids), re(pos)
-    out = torch.empty_like(q)
+    out = torch.empty(b, s, hq, dv, dtype=q.dtype, device=dev)
     lse = torch.empty(b, hq, s, dtype=torch.float32, device=dev)
-    acc = torch.empty(1, n, hq, d, dtype=torch.float32, device=dev)
-    blk = torch.empty(1, n, hq, d, dtype=torch.float32, device=dev)
+    acc = torch.empty(1, n, hq, dv, dtype=torch.float32, device=dev)
+    blk = torch.empty(1, n, hq, dv, dtype=torch.float32, device=dev)
     blk_lse = torch.empty(1, hq, n, dtype=torch.float32, device=dev)
     lse_sh = torch.empty(R, hq, n, dtype=torch.float32, device=dev)
-    out_r = torch.empty(1, s, hq, d, dtype=q.dtype, device=dev)
+    out_r = torch.empty(1, s, hq, dv, dtype=q.dtype, device=dev)
     ws = torch.empty(workspace_bytes_fwd(qr[:1, :n], kr[:1, :n], idr[:1, :n], posr[:1, :n],
-                                         window_left=window_left),
+                                         window_left=window_left, v=vr[:1, :n]),
                      dtype=torch.uint8, device=dev)
     log = _StatusLog(b * R * R, dev) if check_status else None
     for bi in range(b):
@@ -134,6 +135,7 @@ def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1
     token order.  ``check_status`` as in :func:`ring_attn_fwd`.
     """
     b, s, hq, d = q.shape
+    dv = v.shape[3]
     R = int(cp_size)
     if s % R:
         raise ValueError("sequence length must be divisible by cp_size")
@@ -141,12 +143,12 @@ def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1
     dev = q.device
     re = lambda x: reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
     qr, kr, vr, idr, posr = re(q), re(k), re(v), re(ids), re(pos)
-    out = torch.empty_like(q)
+    out = torch.empty(b, s, hq, dv, dtype=q.dtype, device=dev)
     lse = torch.empty(b, hq, s, dtype=torch.float32, device=dev)
-    out_r = torch.empty(1, s, hq, d, dtype=q.dtype, device=dev)
+    out_r = torch.empty(1, s, hq, dv, dtype=q.dtype, device=dev)
     lse_sh = torch.empty(R, hq, n, dtype=torch.float32, device=dev)
     ws = torch.empty(workspace_bytes_fwd(qr[:1, :n], kr[:1], idr[:1, :n], posr[:1, :n],
-                                         idr[:1], posr[:1], window_left=window_left),
+                                         idr[:1], posr[:1], window_left=window_left, v=vr[:1]),
                      dtype=torch.uint8, device=dev)
     log = _StatusLog(b * R, dev) if check_status else None
     for bi in range(b):
@@ -198,10 +200,10 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
     idr, posr = re(ids), re(pos)
     dq = torch.zeros(b, s, hq, d, dtype=torch.float32, device=dev)
     dk = torch.zeros(b, s, hkv, d, dtype=torch.float32, device=dev)
-    dv = torch.zeros(b, s, hkv, d, dtype=torch.float32, device=dev)
+    dv = torch.zeros(b, s, hkv, v.shape[3], dtype=torch.float32, device=dev)
     lse_sh = torch.empty(R, hq, n, dtype=torch.float32, device=dev)
     ws = torch.empty(workspace_bytes_bwd(qr[:1, :n], kr[:1, :n], idr[:1, :n], posr[:1, :n],
-                                         window_left),
+                                         window_left, v=vr[:1, :n]),
                      dtype=torch.uint8, device=dev)
     log = _StatusLog(b * R * R, dev) if check_status else None
     for bi in range(b):

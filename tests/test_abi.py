@@ -113,13 +113,16 @@ def test_bwd_rejects_invalid_arguments_on_host(ga):
     bp.fwd.merge_into_out = 1
     assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
     bp.fwd.merge_into_out = 0
-    # the forward takes d = 256, the backward does not (its dK and dV alone
-    # would fill the tensor memory of a CTA)
+    # d = 256 and the MLA shape (192, 128) are taken (by the dK / dV + dQ kernel
+    # pair); only the size query runs here, nothing is launched on the fake
+    # pointers.  Their workspace holds no fp32 dQ accumulator.
     bp.fwd.d, bp.fwd.kv_token_stride = 256, 0
-    bp.fwd.workspace_bytes = 1 << 30
-    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 2
-    bp.fwd.d, bp.fwd.d_v = 192, 128  # forward-only MLA shape
-    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 2
+    n256 = ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp))
+    assert 0 < n256 < 2 * 4096 * 16 * 256 * 4
+    bp.fwd.d, bp.fwd.d_v = 192, 128
+    assert ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp)) > 0
+    bp.fwd.d_v = 0  # 192 / 192 is no supported shape
+    assert ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp)) == 0
     bp.fwd.d, bp.fwd.d_v = 80, 0
     assert ga.lib().attn_bwd_workspace_bytes(ctypes.byref(bp)) == 0
     # a scale the forward takes but the backward does not: (LSE - ln scale) /

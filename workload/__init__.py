@@ -73,11 +73,12 @@ WORKLOADS = {
                                 fwd_only=True, note="one causal segment of 32768, d = 256"),
     "causal_32k_mla": Workload("causal_32k_mla", 1, 32768, 32, 8, 192, None, -1, d_v=128,
                                fwd_only=True, note="one causal segment, d_qk 192, d_v 128"),
-    # Profiling case: one causal segment of 16384 with a 16-head GQA group, so a
-    # query tile meets ~64 key tiles on average as at the 64k workload, but the
-    # whole problem holds a few hundred MB (kernel counters are captured here).
-    "causal_16k_g16": Workload("causal_16k_g16", 1, 16384, 16, 1, 128, None, -1, bwd=True,
-                               note="profiling: one causal segment, Hq 16, Hkv 1"),
+    # Profiling case: one segment of 32768 with the 64k workload's window and
+    # GQA group size, so a query tile meets ~65 key tiles as there, in a
+    # problem of a few hundred MB with several waves of CTAs (kernel counters
+    # are captured here).
+    "swa_32k_g16": Workload("swa_32k_g16", 1, 32768, 32, 2, 128, None, 8192, bwd=True,
+                            note="profiling: one segment, window (8192,0), Hq 32, Hkv 2"),
 }
 
 
