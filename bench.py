@@ -349,6 +349,27 @@ def per_config(ga, dev, pk, big=None):
     if big is not None:
         w = workload.WORKLOADS["full_swa_64k"]
         pairs = valid_pairs(w)
+        # the deterministic backward (dK / dV kernel + dQ kernel) on the same inputs
+        q, k, v, ids, pos = big["q"], big["k"], big["v"], big["ids"], big["pos"]
+        out = torch.empty_like(q)
+        lse = torch.empty(w.b, w.hq, w.s, dtype=torch.float32, device=dev)
+        ws = torch.empty(ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left, deterministic=True),
+                         dtype=torch.uint8, device=dev)
+        ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale, out=out,
+                    lse=lse, workspace=ws)
+        grads = [torch.empty_like(t) for t in (q, k, v)]
+        det = lambda: ga.attn_bwd(q, k, v, out, lse, big["dout"], ids, pos,
+                                  window_left=w.window_left, scale=w.scale, dq=grads[0],
+                                  dk=grads[1], dv=grads[2], workspace=ws, deterministic=True)
+        det_ms = _timed_calls(det, iters=5)
+        if ga.read_device_status(ws) != 0:
+            raise RuntimeError("deterministic backward: device status")
+        res["full_swa_64k_deterministic_bwd"] = {
+            "what": "attn_bwd(deterministic=True): dK / dV kernel + dQ kernel, dQ summed on "
+                    "chip in a fixed order (bit-identical run to run)",
+            "bwd_ms": det_ms, "bwd_tflops": 10 * w.d * w.hq * pairs / det_ms / 1e9}
+        del out, lse, ws, grads
+        torch.cuda.empty_cache()
         ag = lambda: ring.allgather_attn_fwd(big["q"], big["k"], big["v"], big["ids"], big["pos"],
                                              4, window_left=w.window_left, scale=w.scale,
                                              stripe_size=512, check_status=False)

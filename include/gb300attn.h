@@ -66,7 +66,7 @@ enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
  *  q_segment_ids, q_segment_pos    int32 [b, s_q]
  *  kv_segment_ids, kv_segment_pos  int32 [b, s_kv]  (may alias the q ones)
  *  b, s_q, s_kv, h_q, h_kv, d      sizes; h_q % h_kv == 0; d in {64, 128, 256}
- *                                  (attn_bwd: d in {64, 128}); d is the head
+ *                                  (forward and backward); d is the head
  *                                  dim of q and k, and of v unless d_v says
  *                                  otherwise;
  *                                  s_q, s_kv >= 1 (ragged lengths allowed)
@@ -100,8 +100,8 @@ enum { ATTN_REORDER_DUAL_CHUNK = 0, ATTN_REORDER_STRIPED = 1 };
  *                 Must be 0 when d_v differs from d.
  *  d_v            head dim of v and out; 0 = d.  Other than d, only d = 192
  *                 with d_v = 128 (the MLA shape the TE tutorial's closing
- *                 section points to), forward only: v is then bf16
- *                 [b, s_kv, h_kv, 128], contiguous.  attn_bwd requires 0 or d.
+ *                 section points to), forward and backward: v is then bf16
+ *                 [b, s_kv, h_kv, 128], contiguous.
  */
 typedef struct attn_fwd_params {
   const void* q;
@@ -134,16 +134,26 @@ typedef struct attn_fwd_params {
  *  dout     bf16 [b, s_q, h_q, d]
  *  (merge_into_out must be 0 and out_final NULL in the embedded fwd fields)
  *  dq       bf16 [b, s_q, h_q, d]     (written)
- *  dk, dv   bf16 [b, s_kv, h_kv, d]   (written; summed over the GQA group),
- *           tokens fwd.kv_token_stride elements apart like k and v
- *  workspace  >= attn_bwd_workspace_bytes() bytes, 256-byte aligned; holds the
- *             fp32 dQ accumulator, D = rowsum(dO * O) and the tile plan.
+ *  dk       bf16 [b, s_kv, h_kv, d]   (written; summed over the GQA group),
+ *  dv       bf16 [b, s_kv, h_kv, d_v] tokens fwd.kv_token_stride elements apart
+ *           like k and v
+ *  workspace  >= attn_bwd_workspace_bytes() bytes, 256-byte aligned; holds
+ *             D = rowsum(dO * O), the tile plan and (fused path) the fp32 dQ
+ *             accumulator.
  *  accumulate_fp32  0: dq/dk/dv are bf16 and are overwritten.
  *                   1: dq/dk/dv are fp32 and this call's gradients are ADDED to
  *                   their contents (ring context parallelism sums per-block
  *                   contributions; "Context parallelism and ring attention",
  *                   section "Ring attention").  out / lse must then be the final
  *                   forward output and LSE of the query rows (D and P use them).
+ *  deterministic    0: at d = 64 / 128 one fused kernel computes dQ, dK and dV and
+ *                   sums dQ over key tiles with fp32 reduce-adds into a global
+ *                   accumulator, in an order the hardware schedules (the last
+ *                   bits of dq may differ from run to run).
+ *                   1: a dK / dV kernel and a dQ kernel; dQ of each query tile is
+ *                   summed in a fixed order on chip and written once, so every
+ *                   output is bit-identical from run to run (slower at d <= 128).
+ *                   d = 256 and (192, 128) always take this pair.
  */
 typedef struct attn_bwd_params {
   attn_fwd_params fwd;
@@ -152,6 +162,7 @@ typedef struct attn_bwd_params {
   void* dk;
   void* dv;
   int32_t accumulate_fp32;
+  int32_t deterministic;
 } attn_bwd_params;
 
 /* Scratch sizes (bytes) for the given problem; 0 on invalid sizes. */
@@ -161,12 +172,13 @@ GB300ATTN_API size_t attn_bwd_workspace_bytes(const attn_bwd_params* p);
 /* Forward attention (tile plan + fused tcgen05 kernel).  See attn_fwd_params. */
 GB300ATTN_API int attn_fwd(const attn_fwd_params* p, attn_stream_t stream);
 
-/* Backward attention: D = rowsum(dO*O), fused dQ/dK/dV kernel, dQ finalise.
- * d must be 64 or 128: at d = 256 a 128-key tile's dK and dV alone would fill
- * the 512 TMEM columns of a CTA, so d = 256 returns ATTN_ERR_UNSUPPORTED
- * before any launch.  scale must be at least 1e-30 (ATTN_ERR_UNSUPPORTED
- * otherwise): the kernel subtracts (LSE - ln scale) / scale from S on the
- * tensor core, which must stay within the fp32 range. */
+/* Backward attention: D = rowsum(dO*O), then either the fused dQ/dK/dV kernel
+ * and the dQ finalise (d = 64 / 128, deterministic = 0), or the dK / dV kernel
+ * and the dQ kernel (deterministic = 1, and always at d = 256 and d = 192 with
+ * d_v = 128, where a 128-key tile's dK and dV would not fit the fused
+ * kernel's 512 TMEM columns).  scale must be at least 1e-30
+ * (ATTN_ERR_UNSUPPORTED otherwise): the kernels subtract (LSE - ln scale) /
+ * scale from S on the tensor core, which must stay within the fp32 range. */
 GB300ATTN_API int attn_bwd(const attn_bwd_params* p, attn_stream_t stream);
 
 /* Online-softmax merge of a partial result into an accumulator, per row-head.

@@ -55,6 +55,7 @@ class BwdParams(ctypes.Structure):
     _fields_ = [
         ("fwd", FwdParams), ("dout", ctypes.c_void_p), ("dq", ctypes.c_void_p),
         ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p), ("accumulate_fp32", ctypes.c_int32),
+        ("deterministic", ctypes.c_int32),
     ]
 
 
@@ -258,9 +259,12 @@ def _attn_fwd_call(entry, q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, sc
 def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
              window_left: int = -1, scale: Optional[float] = None, dq=None, dk=None, dv=None,
              accumulate_fp32: bool = False, workspace: Optional[torch.Tensor] = None,
-             check_status: bool = False):
+             check_status: bool = False, deterministic: bool = False):
     """Backward attention.  Returns (dq, dk, dv): bf16, or with
     ``accumulate_fp32`` the given fp32 tensors with this call's gradients added.
+    ``deterministic`` takes the dK / dV + dQ kernel pair, whose results are
+    bit-identical from run to run (the default fused kernel sums dQ with
+    reduce-adds in hardware order); head dims 256 and (192, 128) always take it.
     ``check_status`` as in :func:`attn_fwd`."""
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
@@ -298,6 +302,7 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     p.fwd.kv_token_stride = kv_stride
     p.dout, p.dq, p.dk, p.dv = dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
     p.accumulate_fp32 = 1 if accumulate_fp32 else 0
+    p.deterministic = 1 if deterministic else 0
     need = lib().attn_bwd_workspace_bytes(ctypes.byref(p))
     if workspace is None:
         workspace = _workspace(need, q.device)
@@ -308,12 +313,14 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     return dq, dk, dv
 
 
-def workspace_bytes_bwd(q, k, q_ids, q_pos, window_left=-1, v=None) -> int:
+def workspace_bytes_bwd(q, k, q_ids, q_pos, window_left=-1, v=None,
+                        deterministic: bool = False) -> int:
     """Workspace bytes attn_bwd needs for these shapes (0 if it rejects them);
     pass ``v`` when its head dim differs from k's."""
     p = BwdParams()
     p.fwd = _fwd_params(q, k, k if v is None else v, q_ids, q_pos, q_ids, q_pos, window_left,
                         None, q, q, False)
+    p.deterministic = 1 if deterministic else 0
     return int(lib().attn_bwd_workspace_bytes(ctypes.byref(p)))
 
 

@@ -2,7 +2,6 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 
 #include "internal.h"
@@ -184,21 +183,21 @@ int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,
 }
 
 // Which backward runs: the fused kernel (dQ summed through an fp32
-// accumulator in global memory) or the dK / dV kernel plus the dQ kernel.
-// The head dims whose dK and dV do not fit the fused kernel's TMEM (256, and
-// 192 / 128) take the split pair.
-static bool use_split_bwd(const attn_fwd_params* f) {
+// accumulator in global memory) or the dK / dV kernel plus the dQ kernel
+// (dQ summed on chip in a fixed order: deterministic).  The head dims whose
+// dK and dV do not fit the fused kernel's TMEM (256, and 192 / 128) always
+// take the pair.
+static bool use_split_bwd(const attn_bwd_params* p) {
+  const attn_fwd_params* f = &p->fwd;
   const int64_t dv = fwd_dv(f);
-  if (f->d == 256 || (f->d == 192 && dv == 128)) return true;
-  const char* e = getenv("GB300ATTN_BWD");
-  return e && e[0] == 's';
+  return f->d == 256 || (f->d == 192 && dv == 128) || p->deterministic != 0;
 }
 
 size_t attn_bwd_workspace_bytes(const attn_bwd_params* p) {
   if (!p || check_fwd(&p->fwd) != ATTN_OK) return 0;
   const PlanLayout L = fwd_layout(&p->fwd);
   const size_t d_bytes = align_up((size_t)(p->fwd.b * p->fwd.h_q * p->fwd.s_q) * 4, 256);
-  if (use_split_bwd(&p->fwd)) return L.end + d_bytes;
+  if (use_split_bwd(p)) return L.end + d_bytes;
   const size_t dq_bytes = align_up((size_t)(p->fwd.b * p->fwd.s_q * p->fwd.h_q * p->fwd.d) * 4, 256);
   return L.end + d_bytes + dq_bytes;
 }
@@ -223,7 +222,8 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   if (rc != ATTN_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t dv = fwd_dv(f);
-  if (use_split_bwd(f)) {
+  if (p->deterministic != 0 && p->deterministic != 1) return ATTN_ERR_INVALID_ARG;
+  if (use_split_bwd(p)) {
     SplitLaunch sl;
     sl.p = p;
     sl.plan = plan_ptrs(f->workspace, L);

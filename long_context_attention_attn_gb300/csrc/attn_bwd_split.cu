@@ -116,8 +116,9 @@ struct ALayout {
   static constexpr int bar_off = vec_off + NV * kVec * 4;
   static constexpr int bytes = bar_off + 256;
   static constexpr int alloc = (bytes + 1024) > 150 * 1024 ? (bytes + 1024) : 150 * 1024;
-  // TMEM columns: S^T, dP^T (BM each), then the dV and dK slices
-  static constexpr uint32_t kColS = 0, kColDP = BM, kColDV = 2 * BM, kColDK = 2 * BM + DVS;
+  // TMEM columns: two BM-wide regions that S^T and dP^T take in turn (step t:
+  // S^T in region t & 1, dP^T in the other), then the dV and dK slices
+  static constexpr uint32_t kColR = 0, kColDV = 2 * BM, kColDK = 2 * BM + DVS;
   static_assert(2 * BM + DVS + DKS <= 512, "TMEM columns");
   static_assert(alloc <= 232448, "shared memory per block");
   static_assert(DKS % 64 == 0 || DKS == 64 || DKS % 32 == 0, "dK slice");
@@ -323,51 +324,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t e_s = sdesc_lo_nosw(smem_u32(smem + L::e_off));
         const uint32_t e_d = sdesc_lo_nosw(smem_u32(smem + L::e_off + L::kE));
         const uint32_t aug0 = sdesc_lo_nosw(smem_u32(smem + L::aug_off));
-        const uint32_t t_s = tmem + L::kColS, t_dp = tmem + L::kColDP;
         // this CTA's slice: d columns [ks * DKS, ...) of dK, [ks * DVS, ...) of dV
         const uint32_t q_slice = (uint32_t)((ks * L::DKS / 64) * L::kQChunk) >> 4;
         const uint32_t do_slice = (uint32_t)((ks * L::DVS / 64) * L::kQChunk) >> 4;
         constexpr int kHB = BM / 2;  // query columns of one element-wise half
-        bool ok = mbar_wait(&bars->kv_full, 0, ctx);
-        for (int t = 0; t < nsteps_total && ok; ++t) {
-          const int qs = t % NQ, os = t % NO;
-          const uint32_t qstage = (uint32_t)(qs * L::kQTile) >> 4;
-          const uint32_t ostage = (uint32_t)(os * L::kOTile) >> 4;
-          ok = mbar_wait(&bars->q_full[qs], (t / NQ) & 1, ctx);
-          if (ok) ok = mbar_wait(&bars->vec_full[t % NV], (t / NV) & 1, ctx);
-          // S^T overwrites P^T / dS^T of the previous step: dV and dK must be done
-          if (ok && t > 0) ok = mbar_wait(&bars->dk_done, (t - 1) & 1, ctx);
-          if (!ok) break;
+        auto region = [&](int r) { return tmem + L::kColR + (uint32_t)((r & 1) * BM); };
+        // S^T(t) - c = K Q^T + E_S Aug^T into region t  (M = keys, N = BM queries)
+        auto issue_s = [&](int t) -> bool {
+          const int qs = t % NQ;
+          bool w_ok = mbar_wait(&bars->q_full[qs], (t / NQ) & 1, ctx);
+          if (w_ok) w_ok = mbar_wait(&bars->vec_full[t % NV], (t / NV) & 1, ctx);
+          if (!w_ok) return false;
           tc_fence_after();
+          const uint32_t qstage = (uint32_t)(qs * L::kQTile) >> 4;
           const uint32_t aug = aug0 + (uint32_t)(((t % NV) * L::kAug) >> 4);
-          // S^T - c = K Q^T + E_S Aug^T  (M = keys, N = BM queries, K = DK, then 16)
 #pragma unroll
           for (int kk = 0; kk < DK / 16; ++kk) {
             const uint32_t offk = (uint32_t)((kk / 4) * L::kKChunk + (kk % 4) * 32) >> 4;
             const uint32_t offq = (uint32_t)((kk / 4) * L::kQChunk + (kk % 4) * 32) >> 4;
-            mma_ss_lo(t_s, k_km + offk, q_km + qstage + offq, id_st, kk > 0 ? 1u : 0u);
+            mma_ss_lo(region(t), k_km + offk, q_km + qstage + offq, id_st, kk > 0 ? 1u : 0u);
           }
-          mma_ss_nosw(t_s, e_s, aug, id_st, 1u);
+          mma_ss_nosw(region(t), e_s, aug, id_st, 1u);
           mma_commit(&bars->s_full);
-          // dP^T - D = V dO^T + E_D Aug^T: dP^T's columns are free once the
-          // element-wise warps have read the previous step's
-          ok = mbar_wait(&bars->do_full[os], (t / NO) & 1, ctx);
-          if (ok && t > 0) ok = mbar_wait(&bars->dp_free, (t - 1) & 1, ctx);
-          if (!ok) break;
+          return true;
+        };
+        // dP^T(t) - D = V dO^T + E_D Aug^T into the other region
+        auto issue_dp = [&](int t) -> bool {
+          const int os = t % NO;
+          if (!mbar_wait(&bars->do_full[os], (t / NO) & 1, ctx)) return false;
           tc_fence_after();
+          const uint32_t ostage = (uint32_t)(os * L::kOTile) >> 4;
+          const uint32_t aug = aug0 + (uint32_t)(((t % NV) * L::kAug) >> 4);
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk) {
             const uint32_t offv = (uint32_t)((kk / 4) * L::kKChunk + (kk % 4) * 32) >> 4;
             const uint32_t offo = (uint32_t)((kk / 4) * L::kQChunk + (kk % 4) * 32) >> 4;
-            mma_ss_lo(t_dp, v_km + offv, do_km + ostage + offo, id_st, kk > 0 ? 1u : 0u);
+            mma_ss_lo(region(t + 1), v_km + offv, do_km + ostage + offo, id_st, kk > 0 ? 1u : 0u);
           }
-          mma_ss_nosw(t_dp, e_d, aug, id_st, 1u);
+          mma_ss_nosw(region(t + 1), e_d, aug, id_st, 1u);
           mma_commit(&bars->dp_full);
+          return true;
+        };
+        // Order: S^T(0), dP^T(0); per step t: dV(t) (once P^T(t) is in TMEM),
+        // S^T(t+1) (into the region dP^T(t) leaves once the element-wise warps
+        // have read it), dK(t) (once dS^T(t) is in TMEM), dP^T(t+1) (into the
+        // region P^T / dS^T(t) leave once dV(t) and dK(t) are done).
+        bool ok = mbar_wait(&bars->kv_full, 0, ctx);
+        if (ok && nsteps_total > 0) ok = issue_s(0) && issue_dp(0);
+        for (int t = 0; t < nsteps_total && ok; ++t) {
+          const int qs = t % NQ, os = t % NO;
+          const uint32_t qstage = (uint32_t)(qs * L::kQTile) >> 4;
+          const uint32_t ostage = (uint32_t)(os * L::kOTile) >> 4;
+          const uint32_t t_s = region(t);
+          const uint32_t acc0 = t > 0 ? 1u : 0u;
           // dV += P^T dO  (A = P^T in TMEM: K-step kk reads half kk / (kHB / 16))
           ok = mbar_wait(&bars->p_full, t & 1, ctx);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk) {
             const uint32_t col = (kk / (kHB / 16)) * kHB + (kk % (kHB / 16)) * 8;
@@ -376,6 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kk > 0 ? 1u : acc0);
           }
           mma_commit(&bars->do_empty[os]);
+          // With two Q stages S^T(t+1) goes ahead of dK(t); with one, Q(t+1)
+          // can only arrive once dK(t) has released the stage.
+          if constexpr (NQ > 1) {
+            if (t + 1 < nsteps_total) {
+              ok = mbar_wait(&bars->dp_free, t & 1, ctx) && issue_s(t + 1);
+              if (!ok) break;
+            }
+          }
           // dK += dS^T Q  (A = dS^T in TMEM: the second half of each half's columns)
           ok = mbar_wait(&bars->ds_full, t & 1, ctx);
           if (!ok) break;
@@ -389,6 +410,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bars->dk_done);
           mma_commit(&bars->q_empty[qs]);
+          if constexpr (NQ == 1) {
+            if (t + 1 < nsteps_total) {
+              ok = mbar_wait(&bars->dp_free, t & 1, ctx) && issue_s(t + 1);
+              if (!ok) break;
+            }
+          }
+          if (t + 1 < nsteps_total) {
+            ok = mbar_wait(&bars->dk_done, t & 1, ctx) && issue_dp(t + 1);
+            if (!ok) break;
+          }
         }
         mma_commit(&bars->drain);
         mbar_wait_drain(&bars->drain, 0, a.status);
@@ -456,12 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ik = key_in ? a.kv_ids[(int64_t)bi * a.s_kv + key] : 0;
     const int pk = key_in ? a.kv_pos[(int64_t)bi * a.s_kv + key] : 0;
     const float sl2 = a.scale_log2;
-    const uint32_t t_sh = tmem + lane_off + L::kColS + kHB * w;   // this half's S^T columns
-    const uint32_t t_dph = tmem + lane_off + L::kColDP + kHB * w;
     int t = 0;
     bool ok = true;
     for (; t < nsteps_total; ++t) {
       const int en = t % NV;
+      // this half's S^T columns (region t & 1) and dP^T columns (the other region)
+      const uint32_t t_sh = tmem + lane_off + L::kColR + (uint32_t)((t & 1) * BM) + kHB * w;
+      const uint32_t t_dph = tmem + lane_off + L::kColR + (uint32_t)(((t + 1) & 1) * BM) + kHB * w;
       ok = mbar_wait(&bars->vec_full[en], (t / NV) & 1, ctx);
       ok = mbar_wait(&bars->s_full, t & 1, ctx) && ok;
       ok = __all_sync(0xffffffffu, ok);

@@ -172,7 +172,8 @@ def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1
 
 def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_left: int = -1,
                   scale: Optional[float] = None, strategy: int = DUAL_CHUNK,
-                  stripe_size: int = 1, check_status: bool = True):
+                  stripe_size: int = 1, check_status: bool = True,
+                  deterministic: bool = False):
     """Backward of ring attention, emulated on one GPU.
 
     Shard r keeps its query rows, final output O_r, LSE_r and dO_r; at step t
@@ -186,7 +187,9 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
 
     out / lse: the forward results in natural order (e.g. from ring_attn_fwd).
     Returns fp32 (dq [b,s,Hq,d], dk, dv [b,s,Hkv,d]) in natural order.
-    ``check_status`` as in :func:`ring_attn_fwd`.
+    ``check_status`` as in :func:`ring_attn_fwd`; ``deterministic`` as in
+    :func:`attn_bwd` (the block calls then add fixed-order sums, so the
+    result is bit-identical from run to run).
     """
     b, s, hq, d = q.shape
     hkv = k.shape[2]
@@ -203,7 +206,8 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
     dv = torch.zeros(b, s, hkv, v.shape[3], dtype=torch.float32, device=dev)
     lse_sh = torch.empty(R, hq, n, dtype=torch.float32, device=dev)
     ws = torch.empty(workspace_bytes_bwd(qr[:1, :n], kr[:1, :n], idr[:1, :n], posr[:1, :n],
-                                         window_left, v=vr[:1, :n]),
+                                         window_left, v=vr[:1, :n],
+                                         deterministic=deterministic),
                      dtype=torch.uint8, device=dev)
     log = _StatusLog(b * R * R, dev) if check_status else None
     for bi in range(b):
@@ -222,7 +226,7 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
                          idr[bi:bi + 1, rq], posr[bi:bi + 1, rq], idr[bi:bi + 1, rk],
                          posr[bi:bi + 1, rk], window_left=window_left, scale=scale,
                          dq=dq[bi:bi + 1, rq], dk=dk[bi:bi + 1, rk], dv=dv[bi:bi + 1, rk],
-                         accumulate_fp32=True, workspace=ws)
+                         accumulate_fp32=True, workspace=ws, deterministic=deterministic)
                 if log is not None:
                     log.record(ws)
     if log is not None:

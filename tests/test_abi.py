@@ -113,6 +113,10 @@ def test_bwd_rejects_invalid_arguments_on_host(ga):
     bp.fwd.merge_into_out = 1
     assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
     bp.fwd.merge_into_out = 0
+    bp.fwd.workspace_bytes = 1 << 30
+    bp.deterministic = 2  # the flag is 0 or 1
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
+    bp.deterministic = 0
     # d = 256 and the MLA shape (192, 128) are taken (by the dK / dV + dQ kernel
     # pair); only the size query runs here, nothing is launched on the fake
     # pointers.  Their workspace holds no fp32 dQ accumulator.

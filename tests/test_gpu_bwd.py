@@ -23,18 +23,19 @@ def ga():
     return pkg
 
 
-def _gpu_grads(ga, x, window, scale):
+def _gpu_grads(ga, x, window, scale, det=False):
     g = {k: v.to(DEV) for k, v in x.items()}
     out, lse = ga.attn_fwd(g["q"], g["k"], g["v"], g["ids"], g["pos"], window_left=window,
                            scale=scale)
     dq, dk, dv = ga.attn_bwd(g["q"], g["k"], g["v"], out, lse, g["dout"], g["ids"], g["pos"],
-                             window_left=window, scale=scale)
+                             window_left=window, scale=scale, deterministic=det,
+                             check_status=True)
     torch.cuda.synchronize()
     return dq.cpu(), dk.cpu(), dv.cpu()
 
 
-def _full_check(ga, x, window, scale):
-    dq, dk, dv = _gpu_grads(ga, x, window, scale)
+def _full_check(ga, x, window, scale, det=False):
+    dq, dk, dv = _gpu_grads(ga, x, window, scale, det)
     rq, rk, rv = A.attn_bwd(x["q"], x["k"], x["v"], x["dout"], x["ids"], x["pos"], x["ids"],
                             x["pos"], window, scale)
     check_grad(dq, rq, "dq")
@@ -44,31 +45,51 @@ def _full_check(ga, x, window, scale):
     assert torch.all(dq[pad] == 0) and torch.all(dk[pad] == 0) and torch.all(dv[pad] == 0)
 
 
-def test_tiny_workload(ga):
+@pytest.mark.parametrize("det", [False, True])
+def test_tiny_workload(ga, det):
     w = workload.WORKLOADS["tiny"]
-    _full_check(ga, workload.make(w, with_dout=True), w.window_left, w.scale)
+    _full_check(ga, workload.make(w, with_dout=True), w.window_left, w.scale, det)
 
 
+@pytest.mark.parametrize("det", [False, True])
 @pytest.mark.parametrize("b,s,hq,hkv,d,window,seed", [
     (2, 300, 4, 1, 128, 70, 1),   # ragged tail, g = 4
     (1, 200, 3, 1, 64, -1, 2),    # odd group
     (1, 384, 2, 2, 128, -1, 3),   # g = 1
     (1, 640, 4, 2, 128, 0, 4),    # window 0
 ])
-def test_random_packing(ga, b, s, hq, hkv, d, window, seed):
+def test_random_packing(ga, b, s, hq, hkv, d, window, seed, det):
     q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=seed, with_dout=True)
     ids, pos = workload.random_segments(b, s, seed=seed)
     x = dict(q=q, k=k, v=v, dout=dout, ids=ids, pos=pos)
-    _full_check(ga, x, window, d ** -0.5)
+    _full_check(ga, x, window, d ** -0.5, det)
+
+
+@pytest.mark.parametrize("name", ["packed_swa", "tiny"])
+def test_deterministic_mode_is_bit_identical(ga, name):
+    """deterministic=True: dQ is summed on chip in a fixed order, so three
+    backward calls on the same inputs give the same bits in dq, dk and dv."""
+    w = workload.WORKLOADS[name]
+    x = workload.make(w, device=DEV, with_dout=True)
+    out, lse = ga.attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"], window_left=w.window_left,
+                           scale=w.scale)
+    runs = [ga.attn_bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], x["ids"], x["pos"],
+                        window_left=w.window_left, scale=w.scale, deterministic=True)
+            for _ in range(3)]
+    torch.cuda.synchronize()
+    for r in runs[1:]:
+        for a_, b_ in zip(r, runs[0]):
+            assert torch.equal(a_, b_)
 
 
 
+@pytest.mark.parametrize("det", [False, True])
 @pytest.mark.parametrize("s_q,s_kv,q0,window,d,seed", [
     (256, 384, 300, 200, 128, 11),   # queries late in the kv range, window crossing tiles
     (200, 520, 100, -1, 64, 12),     # ragged on both sides, unlimited window
     (384, 130, 0, 40, 128, 13),      # more queries than keys (rows past the keys see none)
 ])
-def test_cross_descriptor_and_lengths(ga, s_q, s_kv, q0, window, d, seed):
+def test_cross_descriptor_and_lengths(ga, s_q, s_kv, q0, window, d, seed, det):
     """Queries of one shard against keys of another, of a different length
     and with a padding hole in the keys (the per-block call of a ring step
     with its own q and kv descriptors)."""
@@ -86,7 +107,8 @@ def test_cross_descriptor_and_lengths(ga, s_q, s_kv, q0, window, d, seed):
     out, lse = ga.attn_fwd(g["q"], g["k"], g["v"], g["ids"], g["pos"], g["kv_ids"], g["kv_pos"],
                            window_left=window, scale=scale)
     dq, dk, dv = ga.attn_bwd(g["q"], g["k"], g["v"], out, lse, g["dout"], g["ids"], g["pos"],
-                             g["kv_ids"], g["kv_pos"], window_left=window, scale=scale)
+                             g["kv_ids"], g["kv_pos"], window_left=window, scale=scale,
+                             deterministic=det)
     torch.cuda.synchronize()
     rq, rk, rv = A.attn_bwd(q, k, v, dout, ids, pos, kv_ids, kv_pos, window, scale)
     check_grad(dq.cpu(), rq, "dq")
@@ -114,13 +136,14 @@ def test_scale_other_than_inverse_sqrt_d(ga, scale):
     x = dict(q=q, k=k, v=v, dout=dout, ids=ids, pos=pos)
     _full_check(ga, x, window, scale)
 
-def _sampled(ga, name, dq_samples, key_samples):
+def _sampled(ga, name, dq_samples, key_samples, det=False):
     w = workload.WORKLOADS[name]
     x = workload.make(w, device=DEV, with_dout=True)
     out, lse = ga.attn_fwd(x["q"], x["k"], x["v"], x["ids"], x["pos"], window_left=w.window_left,
                            scale=w.scale)
     dq, dk, dv = ga.attn_bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], x["ids"], x["pos"],
-                             window_left=w.window_left, scale=w.scale)
+                             window_left=w.window_left, scale=w.scale, deterministic=det,
+                             check_status=True)
     torch.cuda.synchronize()
     del out, lse
     ids, pos = x["ids"].cpu(), x["pos"].cpu()
@@ -159,11 +182,13 @@ def test_packed_swa_sampled(ga):
              key_samples=[(0, 2, 1900, 128), (1, 5, 4096 + 3000, 72), (0, 0, 0, 64)])
 
 
-def test_full_swa_64k_sampled(ga):
-    """The 64k packed GQA-SWA workload in the benchmark's launch configuration."""
+@pytest.mark.parametrize("det", [False, True])
+def test_full_swa_64k_sampled(ga, det):
+    """The 64k packed GQA-SWA workload in the benchmark's launch configuration
+    (and in deterministic mode)."""
     _sampled(ga, "full_swa_64k",
              dq_samples=[(0, 0, 9000, 64), (1, 7, 16384 + 12200, 120)],
-             key_samples=[(0, 3, 12160, 128), (1, 6, 2 * 16384 + 12220, 68)])
+             key_samples=[(0, 3, 12160, 128), (1, 6, 2 * 16384 + 12220, 68)], det=det)
 
 
 def test_packed_kv_layout_fwd_bwd():

@@ -95,16 +95,19 @@ def test_mla_fp32_output(ga):
     _full_check(ga, q, k, v, ids, pos, -1, 0.1, out_fp32=True)
 
 
-def test_d256_backward_is_rejected(ga):
-    """The backward takes d = 64 and 128 only: a d = 256 call fails loudly
-    before any launch."""
-    q, k, v, dout = workload.qkv(1, 256, 2, 1, 256, seed=10, with_dout=True)
+def test_unsupported_head_dim_is_rejected_before_launch(ga):
+    """A head dim outside {64, 128, 256, (192, 128)} fails loudly before any
+    launch, in the forward and in the backward."""
+    q, k, v, dout = workload.qkv(1, 256, 2, 1, 96, seed=10, with_dout=True)
     ids, pos = workload.segments(1, 256, 1)
     g = {n: t.to(DEV) for n, t in dict(q=q, k=k, v=v, dout=dout, ids=ids, pos=pos).items()}
-    out, lse = ga.attn_fwd(g["q"], g["k"], g["v"], g["ids"], g["pos"], scale=256 ** -0.5)
+    with pytest.raises(RuntimeError):
+        ga.attn_fwd(g["q"], g["k"], g["v"], g["ids"], g["pos"], scale=96 ** -0.5)
+    out = torch.zeros_like(g["q"])
+    lse = torch.zeros(1, 2, 256, device=DEV)
     with pytest.raises(RuntimeError):
         ga.attn_bwd(g["q"], g["k"], g["v"], out, lse, g["dout"], g["ids"], g["pos"],
-                    scale=256 ** -0.5)
+                    scale=96 ** -0.5)
 
 
 def test_cross_descriptor_and_lengths(ga):

@@ -149,13 +149,15 @@ def test_segments_from_seqlens_tutorial_row():
     assert torch.equal(ids.cpu(), wi) and torch.equal(pos.cpu(), wp)
 
 
-def test_concurrent_calls_from_host_threads():
+@pytest.mark.parametrize("det", [False, True])
+def test_concurrent_calls_from_host_threads(det):
     """The library keeps no per-call state: four host threads, each with its own
     stream and inputs, calling attn_fwd / attn_bwd at once get bit-identical
     out, lse, dk and dv to the same calls made one after another.  dq is
     compared within the gradient tolerance only: its fp32 sum over key tiles
     is formed by reduce-adds whose order the hardware schedules, so the
-    rounding of the last bits may differ from run to run."""
+    rounding of the last bits may differ from run to run; in deterministic
+    mode it is bit-identical too."""
     import threading
     import long_context_attention_attn_gb300 as ga
     cases = []
@@ -168,7 +170,8 @@ def test_concurrent_calls_from_host_threads():
     def run(c):
         q, k, v, dout, ids, pos = c
         out, lse = ga.attn_fwd(q, k, v, ids, pos, window_left=200, scale=0.1)
-        dq, dk, dv = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=200, scale=0.1)
+        dq, dk, dv = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=200, scale=0.1,
+                                 deterministic=det)
         return out, lse, dq, dk, dv
 
     serial = [run(c) for c in cases]
@@ -195,3 +198,5 @@ def test_concurrent_calls_from_host_threads():
                            ("dv", dv, want[4])):
             assert torch.equal(g, w), name
         check_grad(dq.cpu(), want[2].cpu(), "dq")
+        if det:
+            assert torch.equal(dq, want[2])
