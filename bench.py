@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-workload fwd / bwd, ring and all-gather timings")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time attn_bwd(deterministic=True): the dK / dV + dQ kernel pair")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload name (the headline number is full_swa_64k; smaller ones "
                          "serve profiling)")
@@ -211,7 +213,8 @@ def oracle_sample(w, budget_s=12.0, max_blocks=48):
     ids, pos = workload.segments(1, w.s, w.slots)
     ids, pos = ids[:, :n_tok].numpy(), pos[:, :n_tok].numpy()
     q, k, v, dout = (t[:, :n_tok].to(torch.float64).numpy() for t in
-                     workload.qkv(1, w.s, g, 1, w.d, seed=workload.SEED, with_dout=True))
+                     workload.qkv(1, w.s, g, 1, w.d, seed=workload.SEED, with_dout=True,
+                                  dv=w.dv))
     flops = 0.0
     t0 = time.perf_counter()
     blocks = 0
@@ -222,7 +225,7 @@ def oracle_sample(w, budget_s=12.0, max_blocks=48):
         A.attn_bwd(q, k, v, dout, ids, pos, ids, pos, w.window_left, w.scale, rows=rows)
         W = w.window_left
         pairs = sum((int(p) if W < 0 else min(int(p), W)) + 1 for p in pos[0, rows])
-        flops += pairs * g * 14 * w.d
+        flops += pairs * g * (8 * w.d + 6 * w.dv)  # fwd 2 (d + d_v) + bwd 2 (3 d + 2 d_v)
         blocks += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -397,7 +400,7 @@ def run_reference(args, rank):
             vals.append(val)
     value = sum(vals) / len(vals)
     pairs = valid_pairs(w)
-    flops = pairs * w.hq * 14 * w.d
+    flops = pairs * w.hq * (8 * w.d + 6 * w.dv)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
@@ -429,10 +432,11 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = workload.WORKLOADS[args.workload]
-    fwd_only = w.fwd_only  # head dims the backward does not take: the step is attn_fwd
+    fwd_only = w.fwd_only  # a forward-only workload: the step is attn_fwd
     pairs = valid_pairs(w)
     fwd_flop = 2 * (w.d + w.dv) * w.hq * pairs
-    bwd_flop = 0 if fwd_only else 10 * w.d * w.hq * pairs
+    # backward per pair and head: S and dK, dQ over d_qk; dP and dV over d_v
+    bwd_flop = 0 if fwd_only else 2 * (3 * w.d + 2 * w.dv) * w.hq * pairs
     x = workload.make(w, device=dev, with_dout=not fwd_only, seed=workload.SEED + rank)
     q, k, v, ids, pos = x["q"], x["k"], x["v"], x["ids"], x["pos"]
     dout = x.get("dout")
@@ -443,7 +447,8 @@ def run_ours(args, rank, world, local_rank):
                          dtype=torch.uint8, device=dev)
     else:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws = torch.empty(ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left),
+        ws = torch.empty(ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left, v=v,
+                                                deterministic=args.deterministic),
                          dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -456,7 +461,8 @@ def run_ours(args, rank, world, local_rank):
             ev[1].record(stream)
         if not fwd_only:
             ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=w.window_left,
-                        scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+                        scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                        deterministic=args.deterministic)
         if ev:
             ev[2].record(stream)
 
@@ -534,7 +540,7 @@ def run_ours(args, rank, world, local_rank):
             stream.wait_event(h2d_done[sl])  # dout, for the backward
             ga.attn_bwd(x_["q"], x_["k"], x_["v"], out, lse, x_["dout"], x_["ids"], x_["pos"],
                         window_left=w.window_left, scale=w.scale, dq=gq, dk=gk, dv=gv,
-                        workspace=ws)
+                        workspace=ws, deterministic=args.deterministic)
             comp_done[sl].record(stream)
 
         def d2h(i):
@@ -589,7 +595,7 @@ def run_ours(args, rank, world, local_rank):
     hbm = hbm_components(ga, dev, pk)
     per_cfg = None
     if not args.no_per_config:
-        per_cfg = per_config(ga, dev, pk, big=x)
+        per_cfg = per_config(ga, dev, pk, big=x if w.name == WORKLOAD else None)
     bwd_tflops = bwd_flop / (bwd_avg * 1e-3) / 1e12
     per_gpu = value / world
     cpu = None
@@ -597,7 +603,11 @@ def run_ours(args, rank, world, local_rank):
         val, info = oracle_sample(w)
         cpu = {"value": val, "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
                "sample": info["sample"]}
-    launches_per_step = 5 + 9  # fwd: 4 plan + 1 fused; bwd: 6 plan + D + fused + dQ finalise
+    # fwd: plan (2 summaries, classes, 4-kernel order sort) + 1 fused kernel;
+    # bwd: plan (+ kv ranges and the kv-side sort) + D pre-pass + fused kernel +
+    # dQ finalise, or + dK / dV kernel + dQ kernel
+    split_bwd = args.deterministic or w.d == 256 or w.dv != w.d
+    launches_per_step = 8 + 15
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
@@ -605,9 +615,12 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": value / world / ((fwd_flop + bwd_flop) / (PAGE_GB200_MS * 1e-3) / 1e12),
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "b": w.b, "s": w.s, "slots": w.slots, "hq": w.hq,
-                   "hkv": w.hkv, "d": w.d, "window": [w.window_left, 0],
-                   "step": "attn_fwd + attn_bwd", "valid_pairs_per_head": pairs,
-                   "flop_per_pair_head": {"fwd": 4 * w.d, "bwd": 10 * w.d},
+                   "hkv": w.hkv, "d": w.d, "d_v": w.dv, "window": [w.window_left, 0],
+                   "step": "attn_fwd + attn_bwd" + (" (deterministic)" if args.deterministic
+                                                      else ""),
+                   "valid_pairs_per_head": pairs,
+                   "flop_per_pair_head": {"fwd": 2 * (w.d + w.dv),
+                                          "bwd": 2 * (3 * w.d + 2 * w.dv)},
                    "l2": "inputs larger than L2 (q, dout 4 GiB each); no flush",
                    "vs_baseline_ref": "TE tutorial single-GB200 fwd+bwd 126.687 ms on this "
                                       "workload, converted with the same FLOP count",
@@ -621,12 +634,14 @@ def run_ours(args, rank, world, local_rank):
                        "bwd_pct_of_burst_peak": 100 * bwd_tflops / pk["bf16_burst"],
                        "timing": "medians of the timed steps' per-call CUDA events",
                        "hbm_rows": hbm, "per_config": per_cfg},
-        "roofline": {"kernel": "attn_bwd (fused backward + its D pre-pass, plan and dQ "
-                               "finalise; timed per call)",
+        "roofline": {"kernel": ("attn_bwd (dK / dV kernel + dQ kernel + D pre-pass and plan; "
+                                "timed per call)" if split_bwd else
+                                "attn_bwd (fused backward + its D pre-pass, plan and dQ "
+                                "finalise; timed per call)"),
                      "bound": "tensor", "achieved": bwd_tflops, "peak": pk["bf16_sustained"],
                      "unit": "TFLOP/s", "frac": bwd_tflops / pk["bf16_sustained"],
                      "peak_kind": f"bf16 sustained, {pk['source']}",
-                     "traffic": bwd_traffic() if w.name == WORKLOAD else None,
+                     "traffic": bwd_traffic() if (w.name == WORKLOAD and not split_bwd) else None,
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read+write)"},
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -251,6 +251,18 @@ GB300ATTN_API int attn_segments_from_seqlens(const int32_t* seqlens, const int32
 GB300ATTN_API int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,
                    attn_stream_t stream);
 
+/* Debug hook: the order in which the kernels take their work units, heaviest
+ * first (the units with the most non-SKIP tiles of the other side), equal
+ * weights in index order (a stable sort).
+ *  q_order   int32 [b * ceil(s_q/128)]:  (b, query tile) indices b * nq + tile
+ *            (forward and dQ kernels)
+ *  kv_order  int32 [b * ceil(s_kv/128)]: (b, key tile) indices b * nk + tile
+ *            (dK / dV and fused backward kernels)
+ * Uses p->workspace like attn_fwd.  Not part of any computation's result:
+ * the order only decides which CTAs run first. */
+GB300ATTN_API int attn_tile_order(const attn_fwd_params* p, int32_t* q_order, int32_t* kv_order,
+                                  attn_stream_t stream);
+
 /* Test hook for the device-side timeout path: runs attn_fwd with every key /
  * value tile load withheld, so the bounded waits of the launch run out (about
  * one second) instead of completing.  The kernel then stops early, leaves its

@@ -26,6 +26,7 @@ EXPORTS = (
     "attn_merge_partial", "reorder_causal_lb", "inverse_reorder_causal_lb", "attn_tile_plan",
     "attn_read_device_status", "attn_status_string", "attn_fwd_noalloc",
     "attn_fwd_test_timeout", "attn_segments_from_seqlens", "attn_fwd_noalloc_status",
+    "attn_tile_order",
 )
 
 
@@ -88,6 +89,8 @@ def lib() -> ctypes.CDLL:
             f.restype = c_int
         h.attn_tile_plan.argtypes = [ctypes.POINTER(FwdParams), vp, vp, vp]
         h.attn_tile_plan.restype = c_int
+        h.attn_tile_order.argtypes = [ctypes.POINTER(FwdParams), vp, vp, vp]
+        h.attn_tile_order.restype = c_int
         h.attn_read_device_status.argtypes = [vp, vp]
         h.attn_read_device_status.restype = c_int
         h.attn_fwd_test_timeout.argtypes = [ctypes.POINTER(FwdParams), vp]
@@ -410,6 +413,27 @@ def attn_tile_plan(q, k, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left:
     _check(lib().attn_tile_plan(ctypes.byref(p), _ptr(cls), _ptr(rng), _stream(q.device)),
            "attn_tile_plan")
     return cls, rng
+
+
+def attn_tile_order(q, k, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: int = -1,
+                    workspace=None):
+    """The kernels' work order (debug hook): (q_order int32 [b*nq], kv_order
+    int32 [b*nk]), each a stable heaviest-first permutation of the units."""
+    kv_ids = q_ids if kv_ids is None else kv_ids
+    kv_pos = q_pos if kv_pos is None else kv_pos
+    _need_cuda(q, k, q_ids, q_pos, kv_ids, kv_pos)
+    b, s_q = q.shape[:2]
+    s_kv = k.shape[1]
+    nq, nk = -(-s_q // TILE), -(-s_kv // TILE)
+    p = _fwd_params(q, k, k, q_ids, q_pos, kv_ids, kv_pos, window_left, None, q, q, False)
+    need = lib().attn_fwd_workspace_bytes(ctypes.byref(p))
+    workspace = _workspace(need, q.device) if workspace is None else workspace
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    qo = torch.empty(b * nq, dtype=torch.int32, device=q.device)
+    ko = torch.empty(b * nk, dtype=torch.int32, device=q.device)
+    _check(lib().attn_tile_order(ctypes.byref(p), _ptr(qo), _ptr(ko), _stream(q.device)),
+           "attn_tile_order")
+    return qo, ko
 
 
 def read_device_status(workspace: torch.Tensor) -> int:

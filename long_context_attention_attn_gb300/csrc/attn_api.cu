@@ -193,6 +193,27 @@ static bool use_split_bwd(const attn_bwd_params* p) {
   return f->d == 256 || (f->d == 192 && dv == 128) || p->deterministic != 0;
 }
 
+int attn_tile_order(const attn_fwd_params* p, int32_t* q_order, int32_t* kv_order,
+                    attn_stream_t stream) {
+  int rc = check_fwd(p);
+  if (rc != ATTN_OK) return rc;
+  if (!q_order || !kv_order || !aligned(q_order, 4) || !aligned(kv_order, 4))
+    return ATTN_ERR_INVALID_ARG;
+  const PlanLayout L = fwd_layout(p);
+  rc = check_workspace(p, L.end);
+  if (rc != ATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t nq = cdiv(p->s_q, kTile), nk = cdiv(p->s_kv, kTile);
+  const PlanPtrs pp = plan_ptrs(p->workspace, L);
+  cudaError_t e = launch_tile_plan(*p, pp, nq, nk, true, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(q_order, pp.q_order, (size_t)(p->b * nq) * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(kv_order, pp.kv_order, (size_t)(p->b * nk) * 4, cudaMemcpyDeviceToDevice,
+                        st);
+  return cuda_status(e);
+}
+
 size_t attn_bwd_workspace_bytes(const attn_bwd_params* p) {
   if (!p || check_fwd(&p->fwd) != ATTN_OK) return 0;
   const PlanLayout L = fwd_layout(&p->fwd);

@@ -39,6 +39,8 @@ inline cudaError_t ensure_smem_limit(const void* kernel, int bytes, int launch_r
 constexpr int kTile = 128;  // query / key tile edge used by the plan and the kernels
 constexpr int kFwdKeyTile = 64;  // keys per tile inside the forward kernel (half a plan tile)
 
+constexpr int kSortChunk = 1024;  // rows per CTA of the heavy-first sort
+
 // Per-128-token tile summary of a segment descriptor (32 bytes).
 struct TileSummary {
   int any_valid;  // some token has id != 0
@@ -65,6 +67,10 @@ struct PlanLayout {
   size_t q_order;     // int  [b, nq]  (b, q tile) heavy first
   size_t kv_order;    // int  [b, nk]  (b, kv tile) heavy first
   size_t classes;     // uint8 [b, nq, nk]
+  size_t sort_hist;   // int [chunks, buckets]  heavy-first sort: per-chunk weight counts
+  size_t sort_rank;   // int [max(b*nq, b*nk)]   rank among equal weights in the chunk
+  size_t sort_start;  // int [buckets]           first position of each weight
+  int64_t sort_buckets;  // max(nq, nk) + 1: weights are tile counts of the other side
   size_t end;
 };
 
@@ -83,6 +89,12 @@ inline PlanLayout plan_layout(int64_t b, int64_t nq, int64_t nk, size_t base = 0
   L.q_order = o;   o = align_up(o + (size_t)(b * nq) * 4, 256);
   L.kv_order = o;  o = align_up(o + (size_t)(b * nk) * 4, 256);
   L.classes = o;   o = align_up(o + (size_t)(b * nq * nk), 256);
+  const int64_t nmax = b * (nq > nk ? nq : nk);
+  L.sort_buckets = (nq > nk ? nq : nk) + 1;
+  const int64_t chunks = (nmax + kSortChunk - 1) / kSortChunk;
+  L.sort_hist = o;  o = align_up(o + (size_t)(chunks * L.sort_buckets) * 4, 256);
+  L.sort_rank = o;  o = align_up(o + (size_t)nmax * 4, 256);
+  L.sort_start = o; o = align_up(o + (size_t)L.sort_buckets * 4, 256);
   L.end = o;
   return L;
 }
@@ -98,6 +110,10 @@ struct PlanPtrs {
   int* q_order;
   int* kv_order;
   uint8_t* classes;
+  int* sort_hist;
+  int* sort_rank;
+  int* sort_start;
+  int64_t sort_buckets;
 };
 
 inline PlanPtrs plan_ptrs(void* ws, const PlanLayout& L) {
@@ -111,7 +127,11 @@ inline PlanPtrs plan_ptrs(void* ws, const PlanLayout& L) {
                   reinterpret_cast<int*>(c + L.kv_weight),
                   reinterpret_cast<int*>(c + L.q_order),
                   reinterpret_cast<int*>(c + L.kv_order),
-                  reinterpret_cast<uint8_t*>(c + L.classes)};
+                  reinterpret_cast<uint8_t*>(c + L.classes),
+                  reinterpret_cast<int*>(c + L.sort_hist),
+                  reinterpret_cast<int*>(c + L.sort_rank),
+                  reinterpret_cast<int*>(c + L.sort_start),
+                  L.sort_buckets};
 }
 
 // ---- kernels_misc.cu

@@ -109,74 +109,215 @@ __global__ void tile_class_kernel(const TileSummary* __restrict__ qs,
   }
 }
 
-// One CTA per (kv tile, b): the range of q tiles that see it (backward side).
-__global__ void kv_range_kernel(const uint8_t* __restrict__ cls, int64_t nq, int64_t nk,
-                                int2* __restrict__ krange, int* __restrict__ kweight) {
-  const int64_t c = blockIdx.x, bi = blockIdx.y;
-  __shared__ int s_first, s_last, s_count;
-  if (threadIdx.x == 0) {
-    s_first = INT_MAX;
-    s_last = -1;
-    s_count = 0;
-  }
-  __syncthreads();
+// The range of q tiles that see each kv tile (backward side).  A CTA takes 32
+// neighbouring kv tiles of one batch row (lane = kv tile, so a warp reads 32
+// consecutive class bytes of a row: one sector), its 32 warps split the rows,
+// and each warp keeps eight independent loads in flight.
+__global__ void __launch_bounds__(1024)
+    kv_range_kernel(const uint8_t* __restrict__ cls, int64_t nq, int64_t nk,
+                    int2* __restrict__ krange, int* __restrict__ kweight) {
+  __shared__ int s_first[32][33], s_last[32][33], s_count[32][33];
+  const int64_t bi = blockIdx.y;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 32 + lane;
   int first = INT_MAX, last = -1, count = 0;
-  for (int64_t a = threadIdx.x; a < nq; a += blockDim.x) {
-    if (cls[(bi * nq + a) * nk + c] != kSkip) {
-      first = min(first, (int)a);
-      last = max(last, (int)a);
-      ++count;
+  if (c < nk) {
+    const uint8_t* col = cls + bi * nq * nk + c;
+    for (int64_t a0 = (int64_t)wid * 8; a0 < nq; a0 += 32 * 8) {
+      uint8_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = (a0 + u < nq) ? col[(a0 + u) * nk] : (uint8_t)kSkip;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (v[u] != kSkip) {
+          first = min(first, (int)(a0 + u));
+          last = max(last, (int)(a0 + u));
+          ++count;
+        }
+      }
     }
   }
-  atomicMin(&s_first, first);
-  atomicMax(&s_last, last);
-  atomicAdd(&s_count, count);
+  s_first[wid][lane] = first;
+  s_last[wid][lane] = last;
+  s_count[wid][lane] = count;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    krange[bi * nk + c] = s_last < 0 ? make_int2(0, -1) : make_int2(s_first, s_last);
-    kweight[bi * nk + c] = s_count;
+  if (wid == 0 && c < nk) {
+    for (int w = 1; w < 32; ++w) {
+      first = min(first, s_first[w][lane]);
+      last = max(last, s_last[w][lane]);
+      count += s_count[w][lane];
+    }
+    krange[bi * nk + c] = last < 0 ? make_int2(0, -1) : make_int2(first, last);
+    kweight[bi * nk + c] = count;
   }
 }
 
-// Stable counting sort of n work rows by weight, heaviest first (single CTA):
-// rows of equal weight keep their index order, so neighbouring tiles stay
-// neighbours in the launch order (their K/V, Q and dQ tiles are then shared
-// through L2 by the CTAs running at the same time).  Weights above
-// kBuckets - 1 share the top bucket.
-constexpr int kBuckets = 2048;
-constexpr int kSortChunk = 1024;
-__global__ void heavy_first_kernel(const int* __restrict__ weight, int n, int* __restrict__ order) {
-  __shared__ int hist[kBuckets];
-  __shared__ int start[kBuckets];
-  __shared__ int chunk_w[kSortChunk];
-  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) hist[i] = 0;
+// Stable counting sort of n work rows by weight, heaviest first: rows of equal
+// weight keep their index order, so neighbouring tiles stay neighbours in the
+// launch order (their K/V, Q and dQ tiles are then shared through L2 by the
+// CTAs running at the same time).  Row i goes to
+//   (rows with a larger weight) + (rows of its weight in earlier chunks)
+//   + (rows of its weight earlier in its own chunk of kSortChunk rows).
+// order_chunk_kernel: per chunk, the weight counts (a [chunks, buckets]
+// table in global memory) and each row's rank within the chunk among the
+// rows of its weight (a bitonic sort of (weight, index) pairs in shared
+// memory, then the distance to the first pair of the same weight).
+// order_colscan_kernel / order_bucketscan_kernel: the table's prefix down the
+// chunks of each weight, and the first position of each weight (a suffix sum
+// over the weights).
+// order_scatter_kernel: order[position] = row.
+__device__ __forceinline__ int clamp_weight(int w, int buckets) {
+  return w < 0 ? 0 : (w >= buckets ? buckets - 1 : w);
+}
+
+__global__ void __launch_bounds__(kSortChunk)
+    order_chunk_kernel(const int* __restrict__ weight, int n, int buckets, int* __restrict__ hist,
+                       int* __restrict__ rank) {
+  __shared__ uint64_t keys[kSortChunk];
+  __shared__ int warp_max[kSortChunk / 32];
+  const int t = threadIdx.x;
+  const int64_t i = (int64_t)blockIdx.x * kSortChunk + t;
+  uint64_t key = ~0ull;  // rows past n sort last
+  if (i < n) {
+    const int w = clamp_weight(weight[i], buckets);
+    atomicAdd(&hist[(int64_t)blockIdx.x * buckets + w], 1);
+    key = ((uint64_t)w << 32) | (uint32_t)t;
+  }
+  keys[t] = key;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    atomicAdd(&hist[min(weight[i], kBuckets - 1)], 1);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int w = kBuckets - 1; w >= 0; --w) {
-      start[w] = acc;
-      acc += hist[w];
+  for (int k = 2; k <= kSortChunk; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int p = t ^ j;
+      if (p > t) {
+        const uint64_t x = keys[t], y = keys[p];
+        if ((x > y) == ((t & k) == 0)) {
+          keys[t] = y;
+          keys[p] = x;
+        }
+      }
+      __syncthreads();
     }
   }
-  __syncthreads();
-  for (int c0 = 0; c0 < n; c0 += kSortChunk) {
-    const int m = min(kSortChunk, n - c0);
-    for (int t = threadIdx.x; t < m; t += blockDim.x)
-      chunk_w[t] = min(weight[c0 + t], kBuckets - 1);
-    __syncthreads();
-    for (int t = threadIdx.x; t < m; t += blockDim.x) {
-      const int w = chunk_w[t];
-      int before = 0;  // earlier rows of this chunk with the same weight
-      for (int j = 0; j < t; ++j) before += (chunk_w[j] == w);
-      order[start[w] + before] = c0 + t;
-    }
-    __syncthreads();
-    for (int t = threadIdx.x; t < m; t += blockDim.x) atomicAdd(&start[chunk_w[t]], 1);
-    __syncthreads();
+  // position of the first pair with this weight: inclusive max-scan of the
+  // group starts over the sorted positions
+  const uint64_t kt = keys[t];
+  int first = (t == 0 || (keys[t - 1] >> 32) != (kt >> 32)) ? t : 0;
+  const int lane = t & 31, wid = t >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, first, o);
+    if (lane >= o) first = max(first, v);
   }
+  if (lane == 31) warp_max[wid] = first;
+  __syncthreads();
+  if (wid == 0) {
+    int v = warp_max[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v = max(v, u);
+    }
+    warp_max[lane] = v;
+  }
+  __syncthreads();
+  if (wid > 0) first = max(first, warp_max[wid - 1]);
+  if (kt != ~0ull) rank[(int64_t)blockIdx.x * kSortChunk + (uint32_t)kt] = t - first;
+}
+
+// Exclusive prefix of each weight's counts down the chunks (one thread per
+// weight, the chunk counts loaded eight at a time); the totals go to `total`.
+__global__ void __launch_bounds__(256)
+    order_colscan_kernel(int* __restrict__ hist, int chunks, int buckets, int* __restrict__ total) {
+  const int w = blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= buckets) return;
+  int run = 0;
+  for (int c0 = 0; c0 < chunks; c0 += 8) {
+    int v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = (c0 + u < chunks) ? hist[(int64_t)(c0 + u) * buckets + w] : 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (c0 + u < chunks) hist[(int64_t)(c0 + u) * buckets + w] = run;
+      run += v[u];
+    }
+  }
+  total[w] = run;
+}
+
+// start[w] = number of rows whose weight is larger than w: one CTA; thread t
+// takes a run of consecutive weights from the largest down, sums it, and a
+// block-wide exclusive scan of the run sums gives each run's base.
+__global__ void __launch_bounds__(1024)
+    order_bucketscan_kernel(int* __restrict__ start, int buckets) {
+  __shared__ int warp_sum[32];
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const int per = (buckets + blockDim.x - 1) / blockDim.x;
+  const int p0 = t * per;  // positions p0.. of the list of weights from the largest down
+  int sum = 0;
+  for (int k0 = 0; k0 < per; k0 += 8) {
+    int v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int w = buckets - 1 - (p0 + k0 + u);
+      v[u] = (k0 + u < per && w >= 0) ? start[w] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) sum += v[u];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int x = warp_sum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    warp_sum[lane] = x;
+  }
+  __syncthreads();
+  int run = (wid > 0 ? warp_sum[wid - 1] : 0) + incl - sum;
+  for (int k = 0; k < per; ++k) {
+    const int w = buckets - 1 - (p0 + k);
+    if (w < 0) break;
+    const int v = start[w];
+    start[w] = run;
+    run += v;
+  }
+}
+
+__global__ void order_scatter_kernel(const int* __restrict__ weight, int n, int buckets,
+                                     const int* __restrict__ hist, const int* __restrict__ start,
+                                     const int* __restrict__ rank, int* __restrict__ order) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int w = clamp_weight(weight[i], buckets);
+  const int64_t c = i / kSortChunk;
+  order[start[w] + hist[c * buckets + w] + rank[i]] = (int)i;
+}
+
+static cudaError_t launch_heavy_first(const int* weight, int64_t n, const PlanPtrs& pp, int* order,
+                                      cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t chunks = (n + kSortChunk - 1) / kSortChunk;
+  const int buckets = (int)pp.sort_buckets;
+  cudaError_t e = cudaMemsetAsync(pp.sort_hist, 0, (size_t)(chunks * buckets) * 4, st);
+  if (e != cudaSuccess) return e;
+  order_chunk_kernel<<<(unsigned)chunks, kSortChunk, 0, st>>>(weight, (int)n, buckets,
+                                                              pp.sort_hist, pp.sort_rank);
+  order_colscan_kernel<<<(unsigned)((buckets + 255) / 256), 256, 0, st>>>(pp.sort_hist, (int)chunks,
+                                                                         buckets, pp.sort_start);
+  order_bucketscan_kernel<<<1, 1024, 0, st>>>(pp.sort_start, buckets);
+  order_scatter_kernel<<<(unsigned)chunks, kSortChunk, 0, st>>>(
+      weight, (int)n, buckets, pp.sort_hist, pp.sort_start, pp.sort_rank, order);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tile_plan(const attn_fwd_params& p, const PlanPtrs& pp, int64_t nq, int64_t nk,
@@ -188,13 +329,14 @@ cudaError_t launch_tile_plan(const attn_fwd_params& p, const PlanPtrs& pp, int64
       p.kv_segment_ids, p.kv_segment_pos, p.b, p.s_kv, nk, pp.kv_sum);
   tile_class_kernel<<<dim3((unsigned)nq, (unsigned)p.b), 256, 0, st>>>(
       pp.q_sum, pp.kv_sum, nq, nk, p.window_left, pp.classes, pp.q_range, pp.q_weight);
-  heavy_first_kernel<<<1, 1024, 0, st>>>(pp.q_weight, (int)(p.b * nq), pp.q_order);
-  if (need_kv_side) {
-    kv_range_kernel<<<dim3((unsigned)nk, (unsigned)p.b), 256, 0, st>>>(pp.classes, nq, nk,
-                                                                      pp.kv_range, pp.kv_weight);
-    heavy_first_kernel<<<1, 1024, 0, st>>>(pp.kv_weight, (int)(p.b * nk), pp.kv_order);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_heavy_first(pp.q_weight, p.b * nq, pp, pp.q_order, st);
+  if (e == cudaSuccess && need_kv_side) {
+    kv_range_kernel<<<dim3((unsigned)((nk + 31) / 32), (unsigned)p.b), 1024, 0, st>>>(
+        pp.classes, nq, nk, pp.kv_range, pp.kv_weight);
+    e = launch_heavy_first(pp.kv_weight, p.b * nk, pp, pp.kv_order, st);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 // ============================================================== permutation

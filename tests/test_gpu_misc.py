@@ -200,3 +200,36 @@ def test_concurrent_calls_from_host_threads(det):
         check_grad(dq.cpu(), want[2].cpu(), "dq")
         if det:
             assert torch.equal(dq, want[2])
+
+
+@pytest.mark.parametrize("name,b,s", [
+    ("full_swa_64k", None, None),     # the benchmark's workload
+    ("packed_thd", None, None),
+    ("long_rows", 2, 1 << 20),        # 8192 tiles per row: 16384 units, weights up to 8192
+    ("ragged", 3, 3000),              # ragged tail, many equal weights
+])
+def test_heavy_first_order_is_stable_argsort(name, b, s):
+    """The work order of the kernels equals a host stable argsort of the plan
+    weights, heaviest first (bit for bit, both sides), at the 64k workload and
+    at two rows of a million tokens (no cap on the weights)."""
+    import long_context_attention_attn_gb300 as ga
+    if name in workload.WORKLOADS:
+        w = workload.WORKLOADS[name]
+        b, s, slots, window = w.b, w.s, w.slots, w.window_left
+        ids, pos = workload.segments(b, s, slots)
+    elif name == "long_rows":
+        ids, pos = workload.segments(b, s, None)  # one causal segment per row
+        window = 300000
+    else:
+        ids, pos = workload.random_segments(b, s, seed=3)
+        window = 700
+    dev_ids, dev_pos = ids.cuda(), pos.cuda()
+    q = torch.empty(b, s, 1, 64, dtype=torch.bfloat16, device="cuda")  # only shapes are read
+    cls, _ = ga.attn_tile_plan(q, q, dev_ids, dev_pos, window_left=window)
+    qo, ko = ga.attn_tile_order(q, q, dev_ids, dev_pos, window_left=window)
+    torch.cuda.synchronize()
+    c = cls.cpu().numpy() != 0
+    q_w = c.sum(axis=2).reshape(-1)
+    k_w = c.sum(axis=1).reshape(-1)
+    np.testing.assert_array_equal(qo.cpu().numpy(), np.argsort(-q_w, kind="stable"))
+    np.testing.assert_array_equal(ko.cpu().numpy(), np.argsort(-k_w, kind="stable"))

@@ -39,7 +39,7 @@ class Workload:
     cp_size: int = 0          # >0: ring emulation over cp_size logical shards
     note: str = ""
     d_v: int = 0              # head dim of v / out when it differs from q / k's (0: d)
-    fwd_only: bool = False    # head dims the backward does not take: measured forward only
+    fwd_only: bool = False    # measured forward only
 
     @property
     def scale(self) -> float:
@@ -63,16 +63,16 @@ WORKLOADS = {
                          note="one segment, causal, ring emulation over 4 shards"),
     "full_swa_64k": Workload("full_swa_64k", 2, 65536, 128, 8, 128, 4, 8192, bwd=True,
                              note="4 slots of 16384 (12288 valid), causal, window (8192,0)"),
-    # Other head dims (TE tutorial, "next steps": MLA head dims), forward only,
-    # on the packed_swa packing and on one causal 32k segment.
-    "packed_swa_d256": Workload("packed_swa_d256", 2, 16384, 32, 8, 256, 4, 1024,
-                                fwd_only=True, note="packed_swa's packing at d = 256"),
+    # Other head dims (TE tutorial, "next steps": MLA head dims), forward and
+    # backward, on the packed_swa packing and on one causal 32k segment.
+    "packed_swa_d256": Workload("packed_swa_d256", 2, 16384, 32, 8, 256, 4, 1024, bwd=True,
+                                note="packed_swa's packing at d = 256"),
     "packed_swa_mla": Workload("packed_swa_mla", 2, 16384, 32, 8, 192, 4, 1024, d_v=128,
-                               fwd_only=True, note="packed_swa's packing, d_qk 192, d_v 128"),
-    "causal_32k_d256": Workload("causal_32k_d256", 1, 32768, 32, 8, 256, None, -1,
-                                fwd_only=True, note="one causal segment of 32768, d = 256"),
+                               bwd=True, note="packed_swa's packing, d_qk 192, d_v 128"),
+    "causal_32k_d256": Workload("causal_32k_d256", 1, 32768, 32, 8, 256, None, -1, bwd=True,
+                                note="one causal segment of 32768, d = 256"),
     "causal_32k_mla": Workload("causal_32k_mla", 1, 32768, 32, 8, 192, None, -1, d_v=128,
-                               fwd_only=True, note="one causal segment, d_qk 192, d_v 128"),
+                               bwd=True, note="one causal segment, d_qk 192, d_v 128"),
     # Profiling case: one segment of 32768 with the 64k workload's window and
     # GQA group size, so a query tile meets ~65 key tiles as there, in a
     # problem of a few hundred MB with several waves of CTAs (kernel counters
