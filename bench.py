@@ -236,6 +236,26 @@ def oracle_sample(w, budget_s=12.0, max_blocks=48):
     return flops / dt / 1e12, info
 
 
+def host_link(h, d, h_back, stream):
+    """Pinned host <-> device copy bandwidth of this machine (GB/s), measured with
+    CUDA events on the copy stream: the bound of the end-to-end figure, whose
+    step moves its inputs in and its gradients out."""
+    import torch
+    res = {}
+    for name, dst, src in (("h2d_gbs", d, h), ("d2h_gbs", h_back, d)):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)  # warm-up
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(3):
+                dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = 3 * src.numel() * src.element_size() / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    res["bytes"] = h.numel() * h.element_size()
+    return res
+
+
 def hbm_components(ga, dev, pk):
     """HBM-bound rows of the hot path at the ring workload's shapes (b=1,
     s=32768, 64 query heads, d=128): one merge of a full-sequence fp32 partial
@@ -573,13 +593,16 @@ def run_ours(args, rank, world, local_rank):
         b_.record(s_d2h)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(a.elapsed_time(b_) / n_e2e, dist, dev)
+        link = host_link(h_in["q"], d_in[0]["q"], h_out[0]["dq"], s_h2d)
         e2e = {"value": whole_job_tflops(world, fwd_flop + bwd_flop, e2e_ms),
                "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo,
                "copies": "every step's inputs in and gradients out inside the timed region, "
                          "on two copy streams overlapping the neighbouring steps' compute "
                          "(double-buffered device tensors); a step's forward starts once "
-                         "its own inputs have landed, its dout copy overlapping it"}
+                         "its own inputs have landed, its dout copy overlapping it",
+               "host_link": link,
+               "copy_bound_ms": 1e3 * (bi / (link["h2d_gbs"] * 1e9) + bo / (link["d2h_gbs"] * 1e9))}
         del h_in, h_out, d_in, d_out
 
     if dist:
