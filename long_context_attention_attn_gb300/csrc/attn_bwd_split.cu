@@ -17,13 +17,14 @@
 // in registers, written back to TMEM as bf16 as the A operands of
 // dV += P^T dO and dK += dS^T Q.
 //
-// attn_bwd_dq_kernel: one CTA owns a 128-row query tile of one query head and
-// keeps dQ in TMEM while it walks the key tiles the tile sees, as the forward
-// pass does: S = Q K^T and dP = dO V^T (queries on TMEM lanes, so LSE and D
-// are per-thread scalars), scale * dS = scale * P * (dP - D) written back as
-// bf16 over its S buffer, the A operand of dQ += dS K.  dQ leaves TMEM once,
-// as bf16 (or added into an fp32 accumulator), so no partial sum of dQ ever
-// travels through global memory.
+// attn_bwd_dq_tmem_kernel: one CTA owns a 128-row query tile of one query
+// head and keeps dQ in TMEM while it walks the key tiles the tile sees, as
+// the forward pass does: S = Q K^T and dP = dO V^T (queries on TMEM lanes, so
+// LSE and D are per-thread scalars; Q, and dO where it fits, held in TMEM as
+// the A operands), scale * dS = scale * P * (dP - D) written back as bf16 over
+// the dP columns, the A operand of dQ += dS K.  dQ leaves TMEM once, as bf16
+// (or added into an fp32 accumulator), so no partial sum of dQ ever travels
+// through global memory.
 //
 // Both kernels: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warp 2
 // per-step vector / descriptor loader, warps 4-11 two element-wise
@@ -621,69 +622,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// ============================================================== dQ
-// DK, DV: head dims; BN: keys per tile; NSB: S buffers in TMEM; NKV: K / V
-// shared-memory slots (K and V tiles alternate).  Deadlock-free issue order
-// needs NKV >= 2 * NSB (S(n + NSB) reuses the slot K(n) leaves).
-template <int DK, int DV, int BN, int NSB, int NKV>
-struct QLayout {
-  static constexpr int kQChunk = 128 * 128;   // 128 query rows x 128 B
-  static constexpr int kKVChunk = BN * 128;   // BN key rows x 128 B
-  static constexpr int kQTile = 128 * DK * 2;
-  static constexpr int kOTile = 128 * DV * 2;
-  static constexpr int kKTile = BN * DK * 2;
-  static constexpr int kVTile = BN * DV * 2;
-  static constexpr int kSlot = kKTile > kVTile ? kKTile : kVTile;
-  static constexpr int kIdEntry = 2 * BN + 32;  // key ids, pos, then the class
-  static constexpr int q_off = 0;
-  static constexpr int do_off = q_off + kQTile;
+// ============================================================== dQ, TMEM operands
+// The dQ computation with the query tile (and, where TMEM has room, the dO
+// tile) loaded once into TMEM as the A operands of S = Q K^T (and dP =
+// dO V^T), so those products read only K / V from shared memory, and dS
+// (bf16) written over the dP columns it was computed from (the A operand of
+// dQ += dS K).  One S buffer suffices because S(n+1) may overwrite S(n) as
+// soon as the element-wise warps have loaded it, long before dQ(n); dP(n+1)
+// waits for dQ(n), which reads dS(n) from the dP columns.  Shared memory
+// holds a ring of NKV K / V slots (and the dO tile when it is not in TMEM):
+// the K tile of S(n+1) reuses the slot of K(n+1-NKV/2), freed by dQ long
+// before, so it is loaded well ahead.
+// TMEM: S [0,BN)  dP [BN,2BN)  Q [2BN, 2BN+DK/2)  dO [.., +DV/2) (OT)  dQ [512-DK, 512)
+// d <= 128: 128-key tiles, dO in TMEM, six slots; MLA (192 / 128): 64-key
+// tiles, dO in TMEM, six slots; d = 256: 64-key tiles, dO in shared memory
+// (the Q and dQ columns leave no room), four slots.
+template <int DK, int DV, int BN_, int NKV_, bool OT>
+struct QTLayout {
+  static constexpr int BN = BN_;
+  static constexpr int NKV = NKV_;
+  static constexpr int kQChunk = 128 * 128;  // 128 query rows x 128 B (the dO tile)
+  static_assert(kQChunk == 128 * 128, "dO tile chunk");
+  static constexpr int kKVChunk = BN * 128;  // BN key rows x 128 B
+  static constexpr int kKSlot = BN * DK * 2;
+  static constexpr int kVSlot = BN * DV * 2;
+  static constexpr int kSlot = kKSlot > kVSlot ? kKSlot : kVSlot;  // a K or V tile
+  static constexpr int kOTile = OT ? 0 : 128 * DV * 2;
+  static constexpr int kIdEntry = 2 * BN + 32;
+  static constexpr int do_off = 0;
   static constexpr int kv_off = do_off + kOTile;
   static constexpr int id_off = kv_off + NKV * kSlot;
   static constexpr int bar_off = id_off + NID * kIdEntry * 4;
   static constexpr int bytes = bar_off + 512;
   static constexpr int alloc = (bytes + 1024) > 150 * 1024 ? (bytes + 1024) : 150 * 1024;
-  // TMEM columns: NSB S buffers, dP, and dQ at the top
-  static constexpr uint32_t kColDP = NSB * BN;
-  static constexpr uint32_t kColDQ = 512 - DK;
-  static_assert(NSB * BN + BN <= kColDQ, "TMEM columns");
-  static_assert(NKV >= 2 * NSB, "K / V slots");
+  static constexpr uint32_t kColS = 0, kColDP = BN, kColQ = 2 * BN, kColO = 2 * BN + DK / 2,
+                            kColDQ = 512 - DK;
+  static_assert((OT ? kColO + DV / 2 : kColQ + DK / 2) <= kColDQ, "TMEM columns");
+  static_assert(NKV >= 4 && NKV <= 8, "K / V slots");
   static_assert(alloc <= 232448, "shared memory per block");
 };
 
-struct QBars {
+struct QTBars {
   uint64_t q_full;
+  uint64_t do_full;
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t id_full[NID];
   uint64_t id_empty[NID];
-  uint64_t s_full[2];
-  uint64_t ds_full[2];
-  uint64_t dq_done[2];
-  uint64_t dp_full, dp_free, drain;
+  uint64_t s_full, s_free, dp_full, ds_full, dq_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(QBars) <= 512, "barrier block too large");
+static_assert(sizeof(QTBars) <= 512, "barrier block too large");
 
-template <int DK, int DV, int BN, int NSB, int NKV>
+template <int DK, int DV, int BN_, int NKV_, bool OT>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_do, const SplitArgs a) {
-  using L = QLayout<DK, DV, BN, NSB, NKV>;
+    attn_bwd_dq_tmem_kernel(const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_do, const __nv_bfloat16* q,
+                            const __nv_bfloat16* dout, const SplitArgs a) {
+  using L = QTLayout<DK, DV, BN_, NKV_, OT>;
+  constexpr int BN = L::BN;
+  constexpr int NKV = L::NKV;
   constexpr int kSub = 128 / BN;  // key tiles per 128-key plan tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  QBars* bars = reinterpret_cast<QBars*>(smem + L::bar_off);
-  int* s_ids = reinterpret_cast<int*>(smem + L::id_off);  // [NID][kIdEntry]
+  QTBars* bars = reinterpret_cast<QTBars*>(smem + L::bar_off);
+  int* s_ids = reinterpret_cast<int*>(smem + L::id_off);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (a.status && *reinterpret_cast<volatile int*>(a.status) != kStatusOk) return;
 
-  // ---- work unit: (b, q tile) heavy first, then query head (a group's heads adjacent)
   const int rank = blockIdx.x / a.hq;
   const int h = blockIdx.x % a.hq;
   const int kvh = h / a.g;
@@ -695,7 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint8_t* cls_row = a.cls + (size_t)e * a.nk;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_full, 256);  // every element-wise thread stores its row (or arrives)
+    mbar_init(&bars->do_full, 1);
     for (int i = 0; i < NKV; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
@@ -704,13 +716,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->id_full[i], 1);
       mbar_init(&bars->id_empty[i], 256);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->ds_full[i], 256);
-      mbar_init(&bars->dq_done[i], 1);
-    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 256);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->dp_free, 256);
+    mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->dq_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -728,22 +738,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     regs_dec<kRegsControl>();
     if (warp == 0) {
-      // ====================================================== producer
+      // ====================================================== producer (K, V)
       int last_use[NKV];
       for (int i = 0; i < NKV; ++i) last_use[i] = -1;
       bool ok = true;
       if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_do);
-        mbar_arrive_expect_tx(&bars->q_full, L::kQTile + L::kOTile);
-        for (int c = 0; c < DK / 64; ++c)
-          tma_load_4d(smem_u32(smem + L::q_off + c * L::kQChunk), &tm_q, c * 64, h, qt * 128, bi,
-                      &bars->q_full);
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(smem_u32(smem + L::do_off + c * L::kQChunk), &tm_do, c * 64, h, qt * 128,
-                      bi, &bars->q_full);
+        if constexpr (!OT) {
+          tma_prefetch_desc(&tm_do);
+          mbar_arrive_expect_tx(&bars->do_full, L::kOTile);
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_4d(smem_u32(smem + L::do_off + c * L::kQChunk), &tm_do, c * 64, h, qt * 128,
+                        bi, &bars->do_full);
+        }
       }
       int n = 0;
       for (int j = kSub * rng.x; j < kSub * (rng.y + 1) && ok; ++j) {
@@ -754,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
             if (ok) {
-              mbar_arrive_expect_tx(&bars->kv_full[slot], kv == 0 ? L::kKTile : L::kVTile);
+              mbar_arrive_expect_tx(&bars->kv_full[slot], kv == 0 ? L::kKSlot : L::kVSlot);
               for (int c = 0; c < (kv == 0 ? DK : DV) / 64; ++c)
                 tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kSlot + c * L::kKVChunk),
                             kv == 0 ? &tm_k : &tm_v, c * 64, kvh, j * BN, bi, &bars->kv_full[slot]);
@@ -766,83 +774,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n;
       }
       if (lane == 0) {
-        mbar_wait_drain(&bars->q_full, 0, a.status);
+        if constexpr (!OT) mbar_wait_drain(&bars->do_full, 0, a.status);
         for (int i = 0; i < NKV; ++i)
           if (last_use[i] >= 0) mbar_wait_drain(&bars->kv_full[i], last_use[i] & 1, a.status);
       }
     } else if (warp == 1) {
       // ====================================================== MMA issuer
-      // S(0..NSB-1), dP(0); then per tile n: dQ(n) (once dS(n) is in TMEM;
-      // releases K(n)), dP(n+1) (once dP(n) has been read; releases V(n+1)),
-      // S(n+NSB) (once dQ(n) has consumed the buffer).
+      // S(0), dP(0); then per tile n: S(n+1) once S(n) has been loaded by the
+      // element-wise warps, dQ(n) once dS(n) is in TMEM (releases K(n)),
+      // dP(n+1) once dQ(n) has read dS(n) from the dP columns (releases V(n+1)).
       if (lane == 0) {
-        constexpr uint32_t id_s = idesc_bf16_f32(128, BN, false, false);   // S, dP
-        constexpr uint32_t id_q = idesc_bf16_f32(128, DK, false, true);    // dQ (A in TMEM)
-        const uint32_t q_km = sdesc_lo(smem_u32(smem + L::q_off), 16);
-        const uint32_t do_km = sdesc_lo(smem_u32(smem + L::do_off), 16);
+        constexpr uint32_t id_s = idesc_bf16_f32(128, BN, false, false);  // S, dP (A in TMEM)
+        constexpr uint32_t id_q = idesc_bf16_f32(128, DK, false, true);   // dQ (A in TMEM)
         const uint32_t kv_km = sdesc_lo(smem_u32(smem + L::kv_off), 16);
         const uint32_t kv_mn = sdesc_lo(smem_u32(smem + L::kv_off), L::kKVChunk);
-        const uint32_t t_dp = tmem + L::kColDP, t_dq = tmem + L::kColDQ;
-        constexpr int kHB = BN / 2;  // key columns of one element-wise half
+        const uint32_t do_km = sdesc_lo(smem_u32(smem + L::do_off), 16);
         auto issue_s = [&](int m) -> bool {
           const int slot = (2 * m) % NKV;
-          bool k_ok = mbar_wait(&bars->kv_full[slot], ((2 * m) / NKV) & 1, ctx);
-          if (!k_ok) return false;
+          if (!mbar_wait(&bars->kv_full[slot], ((2 * m) / NKV) & 1, ctx)) return false;
           tc_fence_after();
           const uint32_t kb = kv_km + (uint32_t)((slot * L::kSlot) >> 4);
-          const uint32_t d_s = tmem + (uint32_t)((m % NSB) * BN);
 #pragma unroll
           for (int kk = 0; kk < DK / 16; ++kk) {
-            const uint32_t offa = (uint32_t)((kk / 4) * L::kQChunk + (kk % 4) * 32) >> 4;
             const uint32_t offb = (uint32_t)((kk / 4) * L::kKVChunk + (kk % 4) * 32) >> 4;
-            mma_ss_lo(d_s, q_km + offa, kb + offb, id_s, kk > 0 ? 1u : 0u);
+            mma_ts_lo(tmem + L::kColS, tmem + L::kColQ + kk * 8, kb + offb, id_s,
+                      kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[m % NSB]);
+          mma_commit(&bars->s_full);
           return true;
         };
         auto issue_dp = [&](int m) -> bool {
           const int slot = (2 * m + 1) % NKV;
-          bool v_ok = mbar_wait(&bars->kv_full[slot], ((2 * m + 1) / NKV) & 1, ctx);
-          if (!v_ok) return false;
+          if (!mbar_wait(&bars->kv_full[slot], ((2 * m + 1) / NKV) & 1, ctx)) return false;
           tc_fence_after();
           const uint32_t vb = kv_km + (uint32_t)((slot * L::kSlot) >> 4);
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk) {
-            const uint32_t offa = (uint32_t)((kk / 4) * L::kQChunk + (kk % 4) * 32) >> 4;
             const uint32_t offb = (uint32_t)((kk / 4) * L::kKVChunk + (kk % 4) * 32) >> 4;
-            mma_ss_lo(t_dp, do_km + offa, vb + offb, id_s, kk > 0 ? 1u : 0u);
+            if constexpr (OT) {
+              mma_ts_lo(tmem + L::kColDP, tmem + L::kColO + kk * 8, vb + offb, id_s,
+                        kk > 0 ? 1u : 0u);
+            } else {
+              const uint32_t offa = (uint32_t)((kk / 4) * L::kQChunk + (kk % 4) * 32) >> 4;
+              mma_ss_lo(tmem + L::kColDP, do_km + offa, vb + offb, id_s, kk > 0 ? 1u : 0u);
+            }
           }
           mma_commit(&bars->dp_full);
           mma_commit(&bars->kv_empty[slot]);  // V(m) has no other reader
           return true;
         };
         bool ok = mbar_wait(&bars->q_full, 0, ctx);
-        for (int m = 0; m < NSB && m < nt && ok; ++m) ok = issue_s(m);
-        if (ok && nt > 0) ok = issue_dp(0);
+        if constexpr (!OT) {
+          if (ok) ok = mbar_wait(&bars->do_full, 0, ctx);
+        }
+        if (ok && nt > 0) ok = issue_s(0) && issue_dp(0);
         for (int n = 0; n < nt && ok; ++n) {
-          // dQ += dS(n) K(n)  (A = dS in TMEM, B = K(n) MN-major)
-          ok = mbar_wait(&bars->ds_full[n % NSB], (n / NSB) & 1, ctx);
+          if (n + 1 < nt) {
+            ok = mbar_wait(&bars->s_free, n & 1, ctx) && issue_s(n + 1);
+            if (!ok) break;
+          }
+          ok = mbar_wait(&bars->ds_full, n & 1, ctx);
           if (!ok) break;
           tc_fence_after();
           const int kslot = (2 * n) % NKV;
           const uint32_t kb = kv_mn + (uint32_t)((kslot * L::kSlot) >> 4);
-          const uint32_t d_s = tmem + (uint32_t)((n % NSB) * BN);
+          // dQ += dS K: K-step kk (16 keys) reads the dS columns of half kk / (BN / 32)
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t col = (kk / (kHB / 16)) * kHB + (kk % (kHB / 16)) * 8;
-            mma_ts_lo(t_dq, d_s + col, kb + (uint32_t)((kk * 16 * 128) >> 4), id_q,
-                      (n > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars->dq_done[n % NSB]);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts_lo(tmem + L::kColDQ,
+                      tmem + L::kColDP + (kk / (BN / 32)) * (BN / 2) + (kk % (BN / 32)) * 8,
+                      kb + (uint32_t)((kk * 16 * 128) >> 4), id_q, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->dq_done);
           mma_commit(&bars->kv_empty[kslot]);  // K(n): S(n) and dQ(n) have read it
           if (n + 1 < nt) {
-            ok = mbar_wait(&bars->dp_free, n & 1, ctx);
-            if (ok) ok = issue_dp(n + 1);
-          }
-          if (ok && n + NSB < nt) {
-            // S(n + NSB) overwrites the buffer dQ(n) reads
-            ok = mbar_wait(&bars->dq_done[n % NSB], (n / NSB) & 1, ctx);
-            if (ok) ok = issue_s(n + NSB);
+            ok = mbar_wait(&bars->dq_done, n & 1, ctx) && issue_dp(n + 1);
+            if (!ok) break;
           }
         }
         mma_commit(&bars->drain);
@@ -890,381 +896,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int grow = qt * 128 + row;
     const bool row_in = grow < a.s_q;
-    const int iq = row_in ? a.q_ids[(int64_t)bi * a.s_q + grow] : 0;
-    const int pq = row_in ? a.q_pos[(int64_t)bi * a.s_q + grow] : 0;
-    const int64_t lidx = ((int64_t)bi * a.hq + h) * a.s_q + grow;
-    const float lse = row_in ? a.lse[lidx] : -INFINITY;
-    const float Dr = row_in ? a.Dv[lidx] : 0.f;
-    // 2^(scale log2(e) S - c2) = scale * P with c2 = log2(e) (LSE - ln scale);
-    // a row without keys (LSE = -inf) takes c2 = +inf, so P = 0
-    const float c2 = (lse == -INFINITY) ? INFINITY : (lse + a.c_shift * a.scale) * kLog2e;
-    const float sl2 = a.scale_log2;
-    const uint32_t t_dph = tmem + lane_off + L::kColDP + kHB * w;
-    int n = 0;
-    bool ok = true;
-    for (; n < nt; ++n) {
-      const int en = n % NID;
-      const uint32_t t_sh = tmem + lane_off + (uint32_t)((n % NSB) * BN) + kHB * w;
-      ok = mbar_wait(&bars->id_full[en], (n / NID) & 1, ctx);
-      ok = mbar_wait(&bars->s_full[n % NSB], (n / NSB) & 1, ctx) && ok;
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t r[kHB];
-#pragma unroll
-      for (int c = 0; c < kHB; c += 32) tmem_ld32(t_sh + c, &r[c]);
-      tmem_wait_ld();
-      float p[kHB];
-#pragma unroll
-      for (int u = 0; u < kHB; u += 2) {
-        float x0, x1;
-        fma_f32x2(x0, x1, __uint_as_float(r[u]), __uint_as_float(r[u + 1]), sl2, sl2, -c2, -c2);
-        p[u] = ex2(x0);
-        p[u + 1] = ex2(x1);
-      }
-      const int* ent = s_ids + en * L::kIdEntry;
-      if (ent[2 * BN] == kPartial) {
-        const int4* id4 = reinterpret_cast<const int4*>(ent + kHB * w);
-        const int4* ps4 = reinterpret_cast<const int4*>(ent + BN + kHB * w);
-#pragma unroll
-        for (int c = 0; c < kHB / 4; ++c) {
-          const int4 i4 = id4[c];
-          const int4 k4 = ps4[c];
-          const int ia[4] = {i4.x, i4.y, i4.z, i4.w};
-          const int ka[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (!visible(iq, pq, ia[u], ka[u], a.window)) p[4 * c + u] = 0.f;
-        }
-      }
-      mbar_arrive(&bars->id_empty[en]);
-      // dS = P * (dP - D), scaled like P
-      ok = mbar_wait(&bars->dp_full, n & 1, ctx);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < kHB; c += 32) tmem_ld32(t_dph + c, &r[c]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars->dp_free);
-      uint32_t pk2[kHB / 2];
-#pragma unroll
-      for (int c = 0; c < kHB / 2; ++c) {
-        float d0, d1;
-        fma_f32x2(d0, d1, p[2 * c], p[2 * c + 1], __uint_as_float(r[2 * c]),
-                  __uint_as_float(r[2 * c + 1]), -p[2 * c] * Dr, -p[2 * c + 1] * Dr);
-        pk2[c] = pack_bf16(d0, d1);
-      }
-      // dS over the first half of this half's own S columns (K-major A operand)
-#pragma unroll
-      for (int c = 0; c < kHB / 2; c += 16) tmem_st16(t_sh + c, &pk2[c]);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->ds_full[n % NSB]);
-    }
-    // ---- epilogue: dQ row (columns [w * DK / 2, (w + 1) * DK / 2))
-    if (ok && n > 0) {
-      ok = mbar_wait(&bars->dq_done[(n - 1) % NSB], ((n - 1) / NSB) & 1, ctx);
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-    }
-    if (ok) {
-      constexpr int kHalfD = DK / 2;
-      const int64_t orow = (((int64_t)bi * a.s_q + grow) * a.hq + h) * DK + kHalfD * w;
-      const uint32_t src = tmem + lane_off + L::kColDQ + kHalfD * w;
-#pragma unroll 1
-      for (int c = 0; c < kHalfD; c += 32) {
-        uint32_t o[32];
-        if (n > 0) {
-          tmem_ld32(src + c, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) o[u] = 0u;
-        }
-        if (!row_in) continue;
-        if (a.accumulate) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dq) + orow + c);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            float4 v = dst[u];
-            v.x += __uint_as_float(o[4 * u + 0]);
-            v.y += __uint_as_float(o[4 * u + 1]);
-            v.z += __uint_as_float(o[4 * u + 2]);
-            v.w += __uint_as_float(o[4 * u + 3]);
-            dst[u] = v;
-          }
-          continue;
-        }
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + orow + c);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 v;
-          v.x = pack_bf16(__uint_as_float(o[8 * u + 0]), __uint_as_float(o[8 * u + 1]));
-          v.y = pack_bf16(__uint_as_float(o[8 * u + 2]), __uint_as_float(o[8 * u + 3]));
-          v.z = pack_bf16(__uint_as_float(o[8 * u + 4]), __uint_as_float(o[8 * u + 5]));
-          v.w = pack_bf16(__uint_as_float(o[8 * u + 6]), __uint_as_float(o[8 * u + 7]));
-          dst[u] = v;
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
-}
-
-// ============================================================== dQ, d <= 128
-// The dQ computation with every product reading only its B operand from
-// shared memory: the query and dO tiles are loaded once into TMEM (the A
-// operands of S = Q K^T and dP = dO V^T), and dS (bf16) is written over the
-// dP columns it was computed from (the A operand of dQ += dS K).  One S
-// buffer suffices because S(n+1) may overwrite S(n) as soon as the
-// element-wise warps have loaded it, long before dQ(n); dP(n+1) waits for
-// dQ(n), which reads dS(n) from the dP columns.  Shared memory then holds
-// only K / V tiles: six 128-key slots, so the K tile of S(n+1) reuses the
-// slot of K(n-2) and is loaded well ahead.
-// TMEM: S [0,128)  dP [128,256)  Q [256, 256+D/2)  dO [256+D/2, 256+D)  dQ [512-D, 512)
-template <int D>
-struct QTLayout {
-  static constexpr int BN = 128;
-  static constexpr int NKV = 6;
-  static constexpr int kKVChunk = BN * 128;  // BN key rows x 128 B
-  static constexpr int kSlot = BN * D * 2;   // a K or V tile
-  static constexpr int kIdEntry = 2 * BN + 32;
-  static constexpr int kv_off = 0;
-  static constexpr int id_off = kv_off + NKV * kSlot;
-  static constexpr int bar_off = id_off + NID * kIdEntry * 4;
-  static constexpr int bytes = bar_off + 512;
-  static constexpr int alloc = (bytes + 1024) > 150 * 1024 ? (bytes + 1024) : 150 * 1024;
-  static constexpr uint32_t kColS = 0, kColDP = BN, kColQ = 2 * BN, kColO = 2 * BN + D / 2,
-                            kColDQ = 512 - D;
-  static_assert(kColO + D / 2 <= kColDQ, "TMEM columns");
-  static_assert(alloc <= 232448, "shared memory per block");
-};
-
-struct QTBars {
-  uint64_t q_full;
-  uint64_t kv_full[8];
-  uint64_t kv_empty[8];
-  uint64_t id_full[NID];
-  uint64_t id_empty[NID];
-  uint64_t s_full, s_free, dp_full, ds_full, dq_done, drain;
-  uint32_t tmem_base;
-  int abort_flag;
-};
-static_assert(sizeof(QTBars) <= 512, "barrier block too large");
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_tmem_kernel(const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* q,
-                            const __nv_bfloat16* dout, const SplitArgs a) {
-  using L = QTLayout<D>;
-  constexpr int BN = L::BN;
-  constexpr int NKV = L::NKV;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  QTBars* bars = reinterpret_cast<QTBars*>(smem + L::bar_off);
-  int* s_ids = reinterpret_cast<int*>(smem + L::id_off);
-
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  if (a.status && *reinterpret_cast<volatile int*>(a.status) != kStatusOk) return;
-
-  const int rank = blockIdx.x / a.hq;
-  const int h = blockIdx.x % a.hq;
-  const int kvh = h / a.g;
-  const int e = a.order[rank];
-  const int bi = e / a.nq;
-  const int qt = e % a.nq;
-  const int2 rng = a.range[e];
-  const int nt = a.weight[e];  // non-SKIP 128-key tiles
-  const uint8_t* cls_row = a.cls + (size_t)e * a.nk;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 256);  // every element-wise thread stores its row
-    for (int i = 0; i < NKV; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
-    }
-    for (int i = 0; i < NID; ++i) {
-      mbar_init(&bars->id_full[i], 1);
-      mbar_init(&bars->id_empty[i], 256);
-    }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 256);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_full, 256);
-    mbar_init(&bars->dq_done, 1);
-    mbar_init(&bars->drain, 1);
-    bars->abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-  const WaitCtx ctx{&bars->abort_flag, a.status};
-
-  if (warp < 4) {
-    regs_dec<kRegsControl>();
-    if (warp == 0) {
-      // ====================================================== producer (K, V)
-      int last_use[NKV];
-      for (int i = 0; i < NKV; ++i) last_use[i] = -1;
-      bool ok = true;
-      if (lane == 0) {
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-      }
-      int n = 0;
-      for (int j = rng.x; j <= rng.y && ok; ++j) {
-        if (cls_row[j] == kSkip) continue;
-#pragma unroll 1
-        for (int kv = 0; kv < 2 && ok; ++kv) {
-          const int ld = 2 * n + kv, slot = ld % NKV, use = ld / NKV;
-          if (lane == 0) {
-            ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
-            if (ok) {
-              mbar_arrive_expect_tx(&bars->kv_full[slot], L::kSlot);
-              for (int c = 0; c < D / 64; ++c)
-                tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kSlot + c * L::kKVChunk),
-                            kv == 0 ? &tm_k : &tm_v, c * 64, kvh, j * BN, bi, &bars->kv_full[slot]);
-              last_use[slot] = use;
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
-        ++n;
-      }
-      if (lane == 0)
-        for (int i = 0; i < NKV; ++i)
-          if (last_use[i] >= 0) mbar_wait_drain(&bars->kv_full[i], last_use[i] & 1, a.status);
-    } else if (warp == 1) {
-      // ====================================================== MMA issuer
-      // S(0), dP(0); then per tile n: S(n+1) once S(n) has been loaded by the
-      // element-wise warps, dQ(n) once dS(n) is in TMEM (releases K(n)),
-      // dP(n+1) once dQ(n) has read dS(n) from the dP columns (releases V(n+1)).
-      if (lane == 0) {
-        constexpr uint32_t id_s = idesc_bf16_f32(128, BN, false, false);  // S, dP (A in TMEM)
-        constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);    // dQ (A in TMEM)
-        const uint32_t kv_km = sdesc_lo(smem_u32(smem + L::kv_off), 16);
-        const uint32_t kv_mn = sdesc_lo(smem_u32(smem + L::kv_off), L::kKVChunk);
-        auto issue_s = [&](int m) -> bool {
-          const int slot = (2 * m) % NKV;
-          if (!mbar_wait(&bars->kv_full[slot], ((2 * m) / NKV) & 1, ctx)) return false;
-          tc_fence_after();
-          const uint32_t kb = kv_km + (uint32_t)((slot * L::kSlot) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t offb = (uint32_t)((kk / 4) * L::kKVChunk + (kk % 4) * 32) >> 4;
-            mma_ts_lo(tmem + L::kColS, tmem + L::kColQ + kk * 8, kb + offb, id_s,
-                      kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars->s_full);
-          return true;
-        };
-        auto issue_dp = [&](int m) -> bool {
-          const int slot = (2 * m + 1) % NKV;
-          if (!mbar_wait(&bars->kv_full[slot], ((2 * m + 1) / NKV) & 1, ctx)) return false;
-          tc_fence_after();
-          const uint32_t vb = kv_km + (uint32_t)((slot * L::kSlot) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t offb = (uint32_t)((kk / 4) * L::kKVChunk + (kk % 4) * 32) >> 4;
-            mma_ts_lo(tmem + L::kColDP, tmem + L::kColO + kk * 8, vb + offb, id_s,
-                      kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars->dp_full);
-          mma_commit(&bars->kv_empty[slot]);  // V(m) has no other reader
-          return true;
-        };
-        bool ok = mbar_wait(&bars->q_full, 0, ctx);
-        if (ok && nt > 0) ok = issue_s(0) && issue_dp(0);
-        for (int n = 0; n < nt && ok; ++n) {
-          if (n + 1 < nt) {
-            ok = mbar_wait(&bars->s_free, n & 1, ctx) && issue_s(n + 1);
-            if (!ok) break;
-          }
-          ok = mbar_wait(&bars->ds_full, n & 1, ctx);
-          if (!ok) break;
-          tc_fence_after();
-          const int kslot = (2 * n) % NKV;
-          const uint32_t kb = kv_mn + (uint32_t)((kslot * L::kSlot) >> 4);
-          // dQ += dS K: K-step kk reads the dS columns of half kk / 4
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts_lo(tmem + L::kColDQ, tmem + L::kColDP + (kk / 4) * (BN / 2) + (kk % 4) * 8,
-                      kb + (uint32_t)((kk * 16 * 128) >> 4), id_q, (n > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars->dq_done);
-          mma_commit(&bars->kv_empty[kslot]);  // K(n): S(n) and dQ(n) have read it
-          if (n + 1 < nt) {
-            ok = mbar_wait(&bars->dq_done, n & 1, ctx) && issue_dp(n + 1);
-            if (!ok) break;
-          }
-        }
-        mma_commit(&bars->drain);
-        mbar_wait_drain(&bars->drain, 0, a.status);
-      }
-    } else if (warp == 2) {
-      // ====================================================== key descriptor loader
-      int n = 0;
-      bool ok = true;
-      for (int j = rng.x; j <= rng.y && ok; ++j) {
-        const uint8_t kind = cls_row[j];
-        if (kind == kSkip) continue;
-        const int en = n % NID, use = n / NID;
-        const int64_t base = (int64_t)bi * a.s_kv;
-        int vid[BN / 32], vpos[BN / 32];
-#pragma unroll
-        for (int u = 0; u < BN / 32; ++u) {
-          const int tok = j * BN + u * 32 + lane;
-          const bool in = tok < a.s_kv;
-          vid[u] = in ? a.kv_ids[base + tok] : 0;
-          vpos[u] = in ? a.kv_pos[base + tok] : 0;
-        }
-        if (lane == 0) ok = mbar_wait(&bars->id_empty[en], (use & 1) ^ 1, ctx);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        int* dst = s_ids + en * L::kIdEntry;
-#pragma unroll
-        for (int u = 0; u < BN / 32; ++u) {
-          dst[u * 32 + lane] = vid[u];
-          dst[BN + u * 32 + lane] = vpos[u];
-        }
-        if (lane == 0) dst[2 * BN] = kind;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->id_full[en]);
-        ++n;
-      }
-    }
-  } else {
-    regs_inc<kRegsCompute>();
-    // ======================================================== element-wise
-    constexpr int kHB = BN / 2;  // key columns of this half
-    const int w = (warp - 4) / 4;
-    const int wq = warp % 4;
-    const int row = wq * 32 + lane;  // query row (TMEM lane)
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const int grow = qt * 128 + row;
-    const bool row_in = grow < a.s_q;
-    {
+    if (w == 0 || OT) {
       // the query row (half 0) or the dO row (half 1) into TMEM as bf16 pairs:
       // column c holds elements 2c, 2c + 1 (the row's own byte order)
-      const __nv_bfloat16* src = (w == 0 ? q : dout) + (((int64_t)bi * a.s_q + grow) * a.hq + h) * D;
+      const int width = (w == 0) ? DK : DV;
+      const __nv_bfloat16* src =
+          (w == 0 ? q : dout) + (((int64_t)bi * a.s_q + grow) * a.hq + h) * width;
       const uint4* src4 = reinterpret_cast<const uint4*>(src);
       const uint32_t dst = tmem + lane_off + (w == 0 ? L::kColQ : L::kColO);
 #pragma unroll 1
-      for (int c = 0; c < D / 2; c += 32) {
+      for (int c = 0; c < width / 2; c += 32) {
         uint32_t v32[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -1279,6 +920,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->q_full);
+    } else {
+      mbar_arrive(&bars->q_full);  // the dO tile comes by TMA
     }
     const int iq = row_in ? a.q_ids[(int64_t)bi * a.s_q + grow] : 0;
     const int pq = row_in ? a.q_pos[(int64_t)bi * a.s_q + grow] : 0;
@@ -1356,8 +999,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     if (ok) {
-      constexpr int kHalfD = D / 2;
-      const int64_t orow = (((int64_t)bi * a.s_q + grow) * a.hq + h) * D + kHalfD * w;
+      constexpr int kHalfD = DK / 2;
+      const int64_t orow = (((int64_t)bi * a.s_q + grow) * a.hq + h) * DK + kHalfD * w;
       const uint32_t src = tmem + lane_off + L::kColDQ + kHalfD * w;
 #pragma unroll 1
       for (int c = 0; c < kHalfD; c += 32) {
@@ -1403,19 +1046,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int D>
+template <int DK, int DV, int BN, int NKV, bool OT>
 cudaError_t launch_dq_tmem(const SplitArgs& a, const SplitLaunch& Lc, cudaStream_t st) {
-  using L = QTLayout<D>;
+  using L = QTLayout<DK, DV, BN, NKV, OT>;
   const int64_t units = (int64_t)a.b * a.nq * a.hq;
   if (units == 0) return cudaSuccess;
   static std::atomic<int> smem_set[kMaxDevices];
-  auto kern = attn_bwd_dq_tmem_kernel<D>;
+  auto kern = attn_bwd_dq_tmem_kernel<DK, DV, BN, NKV, OT>;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), L::alloc, kLaunchRegs,
                                     smem_set);
   if (e != cudaSuccess) return e;
   const attn_fwd_params& f = Lc.p->fwd;
   kern<<<(unsigned)units, kThreads, L::alloc, st>>>(
-      Lc.tm_k, Lc.tm_v, static_cast<const __nv_bfloat16*>(f.q),
+      Lc.tm_kb, Lc.tm_vb, Lc.tm_do, static_cast<const __nv_bfloat16*>(f.q),
       static_cast<const __nv_bfloat16*>(Lc.p->dout), a);
   return cudaGetLastError();
 }
@@ -1431,20 +1074,6 @@ cudaError_t launch_dkdv(const SplitArgs& a, const SplitLaunch& Lc, cudaStream_t 
                                     smem_set);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)units, kThreads, L::alloc, st>>>(Lc.tm_q_a, Lc.tm_k, Lc.tm_v, Lc.tm_do_a, a);
-  return cudaGetLastError();
-}
-
-template <int DK, int DV, int BN, int NSB, int NKV>
-cudaError_t launch_dq(const SplitArgs& a, const SplitLaunch& Lc, cudaStream_t st) {
-  using L = QLayout<DK, DV, BN, NSB, NKV>;
-  const int64_t units = (int64_t)a.b * a.nq * a.hq;
-  if (units == 0) return cudaSuccess;
-  static std::atomic<int> smem_set[kMaxDevices];
-  auto kern = attn_bwd_dq_kernel<DK, DV, BN, NSB, NKV>;
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), L::alloc, kLaunchRegs,
-                                    smem_set);
-  if (e != cudaSuccess) return e;
-  kern<<<(unsigned)units, kThreads, L::alloc, st>>>(Lc.tm_q, Lc.tm_kb, Lc.tm_vb, Lc.tm_do, a);
   return cudaGetLastError();
 }
 
@@ -1506,10 +1135,10 @@ cudaError_t launch_attn_bwd_split(const SplitLaunch& Lc, cudaStream_t st) {
   aq.range = Lc.plan.q_range;
   aq.weight = Lc.plan.q_weight;
   aq.order = Lc.plan.q_order;
-  if (f.d == 128) return launch_dq_tmem<128>(aq, Lc, st);
-  if (f.d == 64) return launch_dq_tmem<64>(aq, Lc, st);
-  if (f.d == 192) return launch_dq<192, 128, 64, 2, 4>(aq, Lc, st);
-  return launch_dq<256, 256, 64, 1, 2>(aq, Lc, st);
+  if (f.d == 128) return launch_dq_tmem<128, 128, 128, 6, true>(aq, Lc, st);
+  if (f.d == 64) return launch_dq_tmem<64, 64, 128, 6, true>(aq, Lc, st);
+  if (f.d == 192) return launch_dq_tmem<192, 128, 64, 6, true>(aq, Lc, st);
+  return launch_dq_tmem<256, 256, 64, 4, false>(aq, Lc, st);
 }
 
 }  // namespace gb300
