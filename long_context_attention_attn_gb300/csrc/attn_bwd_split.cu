@@ -60,7 +60,8 @@ __device__ __forceinline__ void split3(float x, uint32_t out[3]) {
 }
 
 struct SplitArgs {
-  const __nv_bfloat16* k;  // read directly when the key tile is kept in TMEM
+  const __nv_bfloat16* k;  // read directly when the key / value tile is kept in TMEM
+  const __nv_bfloat16* v;
   const int* q_ids;
   const int* q_pos;
   const int* kv_ids;
@@ -94,10 +95,12 @@ __device__ __forceinline__ bool visible(int iq, int pq, int ik, int pk, int wind
 // ============================================================== dK / dV
 // DK, DV: head dims of q / k and of v; BM: query rows per step (128, or 64
 // where the head dims leave no room); NSPLIT: column slices of dK / dV (each
-// CTA owns one); NQ / NO: Q / dO shared-memory stages; KT: the key tile is
-// kept in TMEM (the A operand of S^T = K Q^T) instead of shared memory, which
-// at d = 256 frees the room for two Q and two dO stages.
-template <int DK, int DV, int BM, int NSPLIT, int NQ, int NO, bool KT = false>
+// CTA owns one); NQ / NO: Q / dO shared-memory stages; KT / VT: the key /
+// value tile is kept in TMEM (the A operand of S^T = K Q^T / dP^T = V dO^T)
+// instead of shared memory, where the TMEM columns allow: at d = 256 the key
+// tile (which frees the room for two Q and two dO stages), for MLA the value
+// tile (the product then reads only dO from shared memory).
+template <int DK, int DV, int BM, int NSPLIT, int NQ, int NO, bool KT = false, bool VT = false>
 struct ALayout {
   static constexpr int DKS = DK / NSPLIT;  // dK columns of this CTA
   static constexpr int DVS = DV / NSPLIT;  // dV columns of this CTA
@@ -112,7 +115,8 @@ struct ALayout {
   static constexpr int kVec = 2 * BM + 32;   // ids, pos of the step's rows, then the class
   static constexpr int k_off = 0;
   static constexpr int v_off = k_off + (KT ? 0 : kKTile);
-  static constexpr int q_off = v_off + kVTile;
+  static constexpr int kVTileS = VT ? 0 : kVTile;  // bytes of V in shared memory
+  static constexpr int q_off = v_off + kVTileS;
   static constexpr int do_off = q_off + NQ * kQTile;
   static constexpr int e_off = do_off + NO * kOTile;
   static constexpr int aug_off = e_off + 2 * kE;
@@ -123,15 +127,16 @@ struct ALayout {
   // TMEM columns: two BM-wide regions that S^T and dP^T take in turn (step t:
   // S^T in region t & 1, dP^T in the other), then the dV and dK slices
   static constexpr uint32_t kColR = 0, kColDV = 2 * BM, kColDK = 2 * BM + DVS,
-                            kColK = 2 * BM + DVS + DKS;  // the key tile (KT)
-  static_assert(2 * BM + DVS + DKS + (KT ? DK / 2 : 0) <= 512, "TMEM columns");
+                            kColK = 2 * BM + DVS + DKS,                   // the key tile (KT)
+                            kColV = 2 * BM + DVS + DKS + (KT ? DK / 2 : 0);  // the value tile (VT)
+  static_assert(kColV + (VT ? DV / 2 : 0) <= 512, "TMEM columns");
   static_assert(alloc <= 232448, "shared memory per block");
   static_assert(DKS % 64 == 0 || DKS == 64 || DKS % 32 == 0, "dK slice");
 };
 
 struct ABars {
   uint64_t kv_full;
-  uint64_t k_full;  // the key tile is in TMEM (KT)
+  uint64_t k_full;  // the key / value tiles are in TMEM (KT, VT)
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t do_full[2];
@@ -177,13 +182,13 @@ struct AStepIter {
   __device__ int row0() const { return i * 128 + sub * BM; }
 };
 
-template <int DK, int DV, int BM, int NSPLIT, int NQ, int NO, bool KT>
+template <int DK, int DV, int BM, int NSPLIT, int NQ, int NO, bool KT, bool VT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do, const SplitArgs a) {
-  using L = ALayout<DK, DV, BM, NSPLIT, NQ, NO, KT>;
+  using L = ALayout<DK, DV, BM, NSPLIT, NQ, NO, KT, VT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -275,15 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
-        mbar_arrive_expect_tx(&bars->kv_full, (KT ? 0 : L::kKTile) + L::kVTile);
+        mbar_arrive_expect_tx(&bars->kv_full, (KT ? 0 : L::kKTile) + L::kVTileS);
         if constexpr (!KT) {
           for (int c = 0; c < DK / 64; ++c)
             tma_load_4d(smem_u32(smem + L::k_off + c * L::kKChunk), &tm_k, c * 64, kvh, kt * 128,
                         bi, &bars->kv_full);
         }
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(smem_u32(smem + L::v_off + c * L::kKChunk), &tm_v, c * 64, kvh, kt * 128, bi,
-                      &bars->kv_full);
+        if constexpr (!VT) {
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_4d(smem_u32(smem + L::v_off + c * L::kKChunk), &tm_v, c * 64, kvh, kt * 128,
+                        bi, &bars->kv_full);
+        }
       }
       for (AStepIter<BM> it = it0; it.valid() && ok; it.next(), ++t) {
         const int h = kvh * a.g + it.hh;
@@ -372,7 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < DV / 16; ++kk) {
             const uint32_t offv = (uint32_t)((kk / 4) * L::kKChunk + (kk % 4) * 32) >> 4;
             const uint32_t offo = (uint32_t)((kk / 4) * L::kQChunk + (kk % 4) * 32) >> 4;
-            mma_ss_lo(region(t + 1), v_km + offv, do_km + ostage + offo, id_st, kk > 0 ? 1u : 0u);
+            if constexpr (VT)
+              mma_ts_lo(region(t + 1), tmem + L::kColV + kk * 8, do_km + ostage + offo, id_st,
+                        kk > 0 ? 1u : 0u);
+            else
+              mma_ss_lo(region(t + 1), v_km + offv, do_km + ostage + offo, id_st,
+                        kk > 0 ? 1u : 0u);
           }
           mma_ss_nosw(region(t + 1), e_d, aug, id_st, 1u);
           mma_commit(&bars->dp_full);
@@ -383,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // have read it), dK(t) (once dS^T(t) is in TMEM), dP^T(t+1) (into the
         // region P^T / dS^T(t) leave once dV(t) and dK(t) are done).
         bool ok = mbar_wait(&bars->kv_full, 0, ctx);
-        if constexpr (KT) {
+        if constexpr (KT || VT) {
           if (ok) ok = mbar_wait(&bars->k_full, 0, ctx);
         }
         if (ok && nsteps_total > 0) ok = issue_s(0) && issue_dp(0);
@@ -503,25 +515,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ik = key_in ? a.kv_ids[(int64_t)bi * a.s_kv + key] : 0;
     const int pk = key_in ? a.kv_pos[(int64_t)bi * a.s_kv + key] : 0;
     const float sl2 = a.scale_log2;
-    if constexpr (KT) {
-      // this thread's key row into TMEM as bf16 pairs (column c holds d
-      // elements 2c, 2c + 1): half w stores d [w * DK / 2, (w + 1) * DK / 2)
-      const uint4* src4 = reinterpret_cast<const uint4*>(
-          a.k + ((int64_t)bi * a.s_kv + key) * a.k_stride + (int64_t)kvh * DK + w * (DK / 2));
-      const uint32_t dst = tmem + lane_off + L::kColK + w * (DK / 4);
+    if constexpr (KT || VT) {
+      // this thread's key (KT) and value (VT) rows into TMEM as bf16 pairs
+      // (column c holds d elements 2c, 2c + 1): half w stores the d range
+      // [w * D / 2, (w + 1) * D / 2) of each
+      auto store_row = [&](const __nv_bfloat16* base, int64_t stride, int width, uint32_t col) {
+        const uint4* src4 = reinterpret_cast<const uint4*>(
+            base + ((int64_t)bi * a.s_kv + key) * stride + (int64_t)kvh * width + w * (width / 2));
+        const uint32_t dst = tmem + lane_off + col + w * (width / 4);
 #pragma unroll 1
-      for (int c = 0; c < DK / 4; c += 32) {
-        uint32_t v32[32];
+        for (int c = 0; c < width / 4; c += 32) {
+          uint32_t v32[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 x = key_in ? src4[c / 4 + u] : make_uint4(0u, 0u, 0u, 0u);
-          v32[4 * u] = x.x;
-          v32[4 * u + 1] = x.y;
-          v32[4 * u + 2] = x.z;
-          v32[4 * u + 3] = x.w;
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = key_in ? src4[c / 4 + u] : make_uint4(0u, 0u, 0u, 0u);
+            v32[4 * u] = x.x;
+            v32[4 * u + 1] = x.y;
+            v32[4 * u + 2] = x.z;
+            v32[4 * u + 3] = x.w;
+          }
+          tmem_st32(dst + c, v32);
         }
-        tmem_st32(dst + c, v32);
-      }
+      };
+      if constexpr (KT) store_row(a.k, a.k_stride, DK, L::kColK);
+      if constexpr (VT) store_row(a.v, a.v_stride, DV, L::kColV);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->k_full);
@@ -1101,13 +1118,13 @@ cudaError_t launch_dq_tmem(const SplitArgs& a, const SplitLaunch& Lc, cudaStream
   return cudaGetLastError();
 }
 
-template <int DK, int DV, int BM, int NSPLIT, int NQ, int NO, bool KT = false>
+template <int DK, int DV, int BM, int NSPLIT, int NQ, int NO, bool KT = false, bool VT = false>
 cudaError_t launch_dkdv(const SplitArgs& a, const SplitLaunch& Lc, cudaStream_t st) {
-  using L = ALayout<DK, DV, BM, NSPLIT, NQ, NO, KT>;
+  using L = ALayout<DK, DV, BM, NSPLIT, NQ, NO, KT, VT>;
   const int64_t units = (int64_t)a.b * a.nk * a.hkv * NSPLIT;
   if (units == 0) return cudaSuccess;
   static std::atomic<int> smem_set[kMaxDevices];
-  auto kern = attn_bwd_dkdv_kernel<DK, DV, BM, NSPLIT, NQ, NO, KT>;
+  auto kern = attn_bwd_dkdv_kernel<DK, DV, BM, NSPLIT, NQ, NO, KT, VT>;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), L::alloc, kLaunchRegs,
                                     smem_set);
   if (e != cudaSuccess) return e;
@@ -1131,6 +1148,7 @@ cudaError_t launch_attn_bwd_split(const SplitLaunch& Lc, cudaStream_t st) {
   const int64_t dv = f.d_v > 0 ? f.d_v : f.d;
   SplitArgs a;
   a.k = static_cast<const __nv_bfloat16*>(f.k);
+  a.v = static_cast<const __nv_bfloat16*>(f.v);
   a.q_ids = f.q_segment_ids;
   a.q_pos = f.q_segment_pos;
   a.kv_ids = f.kv_segment_ids;
@@ -1165,7 +1183,7 @@ cudaError_t launch_attn_bwd_split(const SplitLaunch& Lc, cudaStream_t st) {
   cudaError_t e;
   if (f.d == 128 && dv == 128) e = launch_dkdv<128, 128, 128, 1, 2, 2>(ak, Lc, st);
   else if (f.d == 64 && dv == 64) e = launch_dkdv<64, 64, 128, 1, 2, 2>(ak, Lc, st);
-  else if (f.d == 192 && dv == 128) e = launch_dkdv<192, 128, 64, 1, 2, 2>(ak, Lc, st);
+  else if (f.d == 192 && dv == 128) e = launch_dkdv<192, 128, 64, 1, 2, 2, false, true>(ak, Lc, st);
   else if (f.d == 256 && dv == 256) e = launch_dkdv<256, 256, 64, 2, 2, 2, true>(ak, Lc, st);
   else return cudaErrorNotSupported;
   if (e != cudaSuccess) return e;
