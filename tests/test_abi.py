@@ -160,6 +160,19 @@ def test_device_status_rejects_null(ga):
     assert ga.lib().attn_read_device_status(None, None) == 1
 
 
+def test_tile_order_rejects_invalid_arguments_on_host(ga):
+    """The work-order debug hook validates like attn_tile_plan, before any
+    launch (the pointers here are fake and never dereferenced)."""
+    p = _params(ga)
+    p.workspace_bytes = 1 << 30
+    assert ga.lib().attn_tile_order(ctypes.byref(p), None, 1 << 20, None) == 1   # no q_order
+    assert ga.lib().attn_tile_order(ctypes.byref(p), 1 << 20, (1 << 20) + 2, None) == 1  # misaligned
+    p.workspace_bytes = 16
+    assert ga.lib().attn_tile_order(ctypes.byref(p), 1 << 20, 1 << 21, None) == 1  # workspace
+    p = _params(ga, d=96)
+    assert ga.lib().attn_tile_order(ctypes.byref(p), 1 << 20, 1 << 21, None) == 2  # head dim
+
+
 def test_segments_rejects_invalid_arguments_on_host(ga):
     a, o = 1 << 20, 1 << 24
     f = ga.lib().attn_segments_from_seqlens

@@ -199,3 +199,26 @@ def test_ring_backward_at_ring_workload(ring):
                                psc, w.window_left, w.scale, rows=rows)
         check_grad(dk[0, k0:k0 + nk, kvh].cpu(), rk[0, keys, 0], f"dk kvh{kvh} k{k0}")
         check_grad(dv[0, k0:k0 + nk, kvh].cpu(), rv[0, keys, 0], f"dv kvh{kvh} k{k0}")
+
+
+def test_ring_backward_deterministic_mode(ring):
+    """ring_attn_bwd(deterministic=True): every block call sums its dQ on chip
+    in a fixed order, so two runs give the same bits, and the result equals
+    the oracle's full backward."""
+    from tests.parity import check_grad
+    b, s, hq, hkv, d, window, R = 1, 2048, 4, 2, 128, 700, 4
+    q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=91, with_dout=True)
+    ids, pos = workload.segments(b, s, 2)
+    g = [x.to(DEV) for x in (q, k, v, dout, ids, pos)]
+    out, lse = ring.ring_attn_fwd(g[0], g[1], g[2], g[4], g[5], R, window_left=window,
+                                  scale=d ** -0.5)
+    runs = [ring.ring_attn_bwd(g[0], g[1], g[2], out, lse, g[3], g[4], g[5], R,
+                               window_left=window, scale=d ** -0.5, deterministic=True)
+            for _ in range(2)]
+    torch.cuda.synchronize()
+    for a_, b_ in zip(*runs):
+        assert torch.equal(a_, b_)
+    rq, rk, rv = A.attn_bwd(q, k, v, dout, ids, pos, ids, pos, window, d ** -0.5)
+    check_grad(runs[0][0].cpu(), rq, "dq")
+    check_grad(runs[0][1].cpu(), rk, "dk")
+    check_grad(runs[0][2].cpu(), rv, "dv")
