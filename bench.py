@@ -537,8 +537,11 @@ def run_ours(args, rank, world, local_rank):
     # end to end through the public API: pinned host inputs in, gradients out.
     # Every step copies its inputs host -> device and its gradients device ->
     # host inside the timed region; as in a training loop with prefetch, the
-    # copies run on their own streams into double-buffered device tensors, so
-    # step i+1's inputs and step i-1's gradients move while step i computes.
+    # copies run on a copy stream of their own into double-buffered device
+    # tensors, so step i+1's inputs and step i-1's gradients move while step i
+    # computes.  One copy stream for both directions, one copy at a time: on
+    # some of these boxes the link moves far less with both directions at once
+    # than with either alone (host_link.both_gbs).
     e2e = None
     if not args.no_e2e and not fwd_only:
         h_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v),
@@ -550,7 +553,8 @@ def run_ours(args, rank, world, local_rank):
         d_out = [(dq, dk, dv), (torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv))]
         bi = sum(t.numel() * t.element_size() for t in h_in.values())
         bo = sum(t.numel() * t.element_size() for t in h_out[0].values())
-        s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        s_copy = torch.cuda.Stream(device=dev)
+        s_h2d = s_d2h = s_copy
         ev = lambda: torch.cuda.Event()
         h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         fwd_in_done = [ev(), ev()]  # q, k, v, ids, pos of the set have landed (dout may not)
@@ -617,14 +621,13 @@ def run_ours(args, rank, world, local_rank):
                "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo,
                "copies": "every step's inputs in and gradients out inside the timed region, "
-                         "on two copy streams overlapping the neighbouring steps' compute "
-                         "(double-buffered device tensors); a step's forward starts once "
-                         "its own inputs have landed, its dout copy overlapping it",
+                         "on one copy stream (one direction at a time) overlapping the "
+                         "neighbouring steps' compute (double-buffered device tensors); a "
+                         "step's forward starts once its own inputs have landed, its dout "
+                         "copy overlapping it",
                "host_link": link,
-               # the copies alone: each direction at its one-way rate, and the
-               # total at the both-directions rate
-               "copy_bound_ms": 1e3 * max(bi / (link["h2d_gbs"] * 1e9), bo / (link["d2h_gbs"] * 1e9),
-                                          (bi + bo) / (link["both_gbs"] * 1e9))}
+               # the copies alone, one after the other at the one-way rates
+               "copy_bound_ms": 1e3 * (bi / (link["h2d_gbs"] * 1e9) + bo / (link["d2h_gbs"] * 1e9))}
         del h_in, h_out, d_in, d_out
 
     if dist:

@@ -9,8 +9,10 @@
 // (both read the same kv head, so every K/V tile loaded into shared memory
 // feeds both; one head when d_v = 256), walking the keys in 64-key tiles.
 // Roles (384 threads):
-//   warp 0        TMA producer: Q tiles once, then K and V tiles into a ring
-//                 of shared-memory slots.
+//   warp 0        TMA producer: Q tiles once, then K and V tiles into two
+//                 rings of shared-memory slots, one for K and one for V (at
+//                 d_qk 192 / d_v 128 a K tile is 24 KB and a V tile 16 KB, so
+//                 separate rings hold a tile more than one ring of 24 KB slots).
 //   warps 1, 3    MMA issuers, one thread per head slot: S_h = Q_h K^T and
 //                 O_h += P_h V on tcgen05; warp 1 also owns the TMEM allocation.
 //   warp 2        descriptor loader: each key tile's ids / pos / class.
@@ -43,15 +45,18 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = kFwdKeyTile;  // keys per tile (half of the plan's 128-key tile)
-constexpr int NST = 8;   // K/V shared-memory slots (K and V tiles alternate), d <= 128
-// Query heads per CTA and K/V slots by head dims (DK of q / k, DV of v / out):
-// DV = 256 takes one head slot (its O accumulator fills TMEM columns
-// [256, 512)) and keeps the query tile in TMEM columns [128, 256) (the second
-// slot's S buffers), the A operand of S = Q K^T, so shared memory holds six
-// 32 KB K/V slots and no Q; DK = 192 (DV = 128) five 24 KB slots.
+// Query heads per CTA and K / V ring slots by head dims (DK of q / k, DV of
+// v / out): d <= 128 four K and four V slots; DV = 256 takes one head slot
+// (its O accumulator fills TMEM columns [256, 512)) and keeps the query tile
+// in TMEM columns [128, 256) (the second slot's S buffers), the A operand of
+// S = Q K^T, so shared memory holds three 32 KB K and three 32 KB V slots and
+// no Q; DK = 192 (DV = 128): three 24 KB K and three 16 KB V slots next to the
+// two 48 KB query tiles.
 template <int DK, int DV> constexpr int kSlots = DV <= 128 ? 2 : 1;
 template <int DK, int DV> constexpr bool kQInTmem = DK == 256;
-template <int DK, int DV> constexpr int kNst = DK <= 128 ? NST : (DK == 192 ? 5 : 6);
+template <int DK, int DV> constexpr int kKSlots = DK <= 128 ? 4 : 3;
+template <int DK, int DV> constexpr int kVSlots = DK <= 128 ? 4 : 3;
+constexpr int kMaxRing = 4;  // slots per ring, at most
 constexpr int NID = 4;   // ids/pos ring entries
 constexpr int kThreads = 384;
 // Registers per thread at launch (65536 / 384, rounded down to a multiple of 8).
@@ -94,10 +99,10 @@ struct Layout {
   static constexpr int kTileBytes = BM * DK * 2;      // a Q tile
   static constexpr int kKBytes = BN * DK * 2;         // a K tile
   static constexpr int kVBytes = BN * DV * 2;         // a V tile
-  static constexpr int kKVBytes = kKBytes > kVBytes ? kKBytes : kVBytes;  // a K / V slot
   static constexpr int q_off = 0;                     // kSlots Q tiles (none when in TMEM)
-  static constexpr int kv_off = q_off + (kQInTmem<DK, DV> ? 0 : kSlots<DK, DV> * kTileBytes);
-  static constexpr int id_off = kv_off + kNst<DK, DV> * kKVBytes;  // NID x kIdEntry ints
+  static constexpr int k_off = q_off + (kQInTmem<DK, DV> ? 0 : kSlots<DK, DV> * kTileBytes);
+  static constexpr int v_off = k_off + kKSlots<DK, DV> * kKBytes;  // the V ring
+  static constexpr int id_off = v_off + kVSlots<DK, DV> * kVBytes;  // NID x kIdEntry ints
   static constexpr int bar_off = id_off + NID * kIdEntry * 4;
   static constexpr int bytes = bar_off + 512;
   // + slack for 1024-byte alignment; at least 150 KB so that one CTA (which
@@ -107,8 +112,10 @@ struct Layout {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[NST];
-  uint64_t kv_empty[NST];
+  uint64_t k_full[kMaxRing];
+  uint64_t k_empty[kMaxRing];  // one arrival per softmax warp
+  uint64_t v_full[kMaxRing];
+  uint64_t v_empty[kMaxRing];
   uint64_t id_full[NID];
   uint64_t id_empty[NID];
   uint64_t s_full[2][2];  // [slot][S buffer]
@@ -148,7 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = e % a.nq;
   const int h0 = kvh * a.g + kSlots<DK, DV> * pair;
   const int nslots = min(kSlots<DK, DV>, a.g - kSlots<DK, DV> * pair);
-  constexpr int NSTD = kNst<DK, DV>;
+  constexpr int NKS = kKSlots<DK, DV>;
+  constexpr int NVS = kVSlots<DK, DV>;
+  static_assert(NKS <= kMaxRing && NVS <= kMaxRing, "ring slots");
   constexpr int NIDD = NID;
   constexpr bool QT = kQInTmem<DK, DV>;
   constexpr uint32_t kColQ = 2 * BN;  // query tile in TMEM (QT only)
@@ -161,9 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, QT ? 128 : 1);  // TMA, or the 128 threads storing Q into TMEM
-    for (int i = 0; i < NSTD; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 4 * nslots);  // one arrival per softmax warp
+    for (int i = 0; i < NKS; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 4 * nslots);
+    }
+    for (int i = 0; i < NVS; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 4 * nslots);
     }
     for (int i = 0; i < NIDD; ++i) {
       mbar_init(&bars->id_full[i], 1);
@@ -210,35 +223,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     int n = 0;
-    int last_use[NSTD];
-    for (int i = 0; i < NSTD; ++i) last_use[i] = -1;
+    int last_k[NKS], last_v[NVS];
+    for (int i = 0; i < NKS; ++i) last_k[i] = -1;
+    for (int i = 0; i < NVS; ++i) last_v[i] = -1;
     bool ok = true;
     for (int j2 = 2 * rng.x; j2 <= 2 * rng.y + 1 && ok && !a.withhold_kv; ++j2) {
       if (cls_row[j2 >> 1] == kSkip) continue;
-      // K tile, then V tile of 64-key tile j2
-#pragma unroll 1
-      for (int kv = 0; kv < 2 && ok; ++kv) {
-        const int ld = 2 * n + kv, slot = ld % NSTD, use = ld / NSTD;
-        if (lane == 0) {
-          ok = mbar_wait(&bars->kv_empty[slot], (use & 1) ^ 1, ctx);
-          if (ok) {
-            mbar_arrive_expect_tx(&bars->kv_full[slot], kv == 0 ? L::kKBytes : L::kVBytes);
-            for (int c = 0; c < (kv == 0 ? L::kChunksK : L::kChunksV); ++c)
-              tma_load_4d(smem_u32(smem + L::kv_off + slot * L::kKVBytes + c * L::kChunkKV),
-                          kv == 0 ? &tm_k : &tm_v, c * 64, kvh, j2 * BN, bi, &bars->kv_full[slot]);
-            last_use[slot] = use;
-          }
+      // K tile, then V tile of 64-key tile j2, each into its own ring
+      if (lane == 0) {
+        const int sk = n % NKS, uk = n / NKS;
+        ok = mbar_wait(&bars->k_empty[sk], (uk & 1) ^ 1, ctx);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars->k_full[sk], L::kKBytes);
+          for (int c = 0; c < L::kChunksK; ++c)
+            tma_load_4d(smem_u32(smem + L::k_off + sk * L::kKBytes + c * L::kChunkKV), &tm_k,
+                        c * 64, kvh, j2 * BN, bi, &bars->k_full[sk]);
+          last_k[sk] = uk;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        const int sv = n % NVS, uv = n / NVS;
+        if (ok) ok = mbar_wait(&bars->v_empty[sv], (uv & 1) ^ 1, ctx);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars->v_full[sv], L::kVBytes);
+          for (int c = 0; c < L::kChunksV; ++c)
+            tma_load_4d(smem_u32(smem + L::v_off + sv * L::kVBytes + c * L::kChunkKV), &tm_v,
+                        c * 64, kvh, j2 * BN, bi, &bars->v_full[sv]);
+          last_v[sv] = uv;
+        }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
       ++n;
     }
     // Drain: every TMA copy this warp issued has landed before the CTA exits
     // (already true on the normal path; bounded after an abort).
     if (lane == 0) {
       if (!QT) mbar_wait_drain(&bars->q_full, 0, a.status);
-      for (int i = 0; i < NSTD; ++i)
-        if (last_use[i] >= 0) mbar_wait_drain(&bars->kv_full[i], last_use[i] & 1, a.status);
+      for (int i = 0; i < NKS; ++i)
+        if (last_k[i] >= 0) mbar_wait_drain(&bars->k_full[i], last_k[i] & 1, a.status);
+      for (int i = 0; i < NVS; ++i)
+        if (last_v[i] >= 0) mbar_wait_drain(&bars->v_full[i], last_v[i] & 1, a.status);
     }
   } else if (warp == 1 || warp == 3) {
     // ======================================================== MMA issuers
@@ -252,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16_f32(BM, DV, false, true);
       // base descriptors: K-major Q / K tiles, MN-major V tiles (128B swizzle)
       const uint32_t da = sdesc_lo(smem_u32(smem + L::q_off + sl * L::kTileBytes), 16);
-      const uint32_t kv_lo_k = sdesc_lo(smem_u32(smem + L::kv_off), 16);
-      const uint32_t kv_lo_v = sdesc_lo(smem_u32(smem + L::kv_off), L::kChunkKV);
+      const uint32_t k_lo = sdesc_lo(smem_u32(smem + L::k_off), 16);
+      const uint32_t v_lo = sdesc_lo(smem_u32(smem + L::v_off), L::kChunkKV);
       const uint32_t d_s0 = tmem + 2 * sl * BN;  // buffer bb at d_s0 + bb * BN
       const uint32_t d_o = tmem + 4 * BN + sl * DV;
       bool ok = mbar_wait(&bars->q_full, 0, ctx);
@@ -264,12 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = -2; n < nt && ok; ++n) {
         if (n >= 0) {
           // O_sl += P_sl(n) V(n): needs V(n) and the softmax of tile n
-          const int ldv = 2 * n + 1, slot_v = ldv % NSTD;
-          ok = mbar_wait(&bars->kv_full[slot_v], (ldv / NSTD) & 1, ctx);
+          const int slot_v = n % NVS;
+          ok = mbar_wait(&bars->v_full[slot_v], (n / NVS) & 1, ctx);
           if (ok) ok = mbar_wait(&bars->p_full[sl][n & 1], (n >> 1) & 1, ctx);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t dv = kv_lo_v + ((slot_v * L::kKVBytes) >> 4);
+          const uint32_t dv = v_lo + ((slot_v * L::kVBytes) >> 4);
           const uint32_t d_s = d_s0 + (n & 1) * BN;
           const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
@@ -282,12 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (m2 < nt) {
           // S_sl(m2) = Q_sl K(m2)^T into buffer m2 & 1: needs K(m2), and PV(n)
           // done (P(n) lives in that buffer)
-          const int ldk = 2 * m2, slot_k = ldk % NSTD;
-          ok = mbar_wait(&bars->kv_full[slot_k], (ldk / NSTD) & 1, ctx);
+          const int slot_k = m2 % NKS;
+          ok = mbar_wait(&bars->k_full[slot_k], (m2 / NKS) & 1, ctx);
           if (ok && n >= 0) ok = mbar_wait(&bars->o_done[sl][n & 1], (n >> 1) & 1, ctx);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t db = kv_lo_k + ((slot_k * L::kKVBytes) >> 4);
+          const uint32_t db = k_lo + ((slot_k * L::kKBytes) >> 4);
           const uint32_t d_s = d_s0 + (m2 & 1) * BN;
 #pragma unroll
           for (int kk = 0; kk < DK / 16; ++kk) {
@@ -391,9 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // S_sl(n) is complete, so this slot is done with K(n) and (its S(n) was
         // issued after PV_sl(n-2) completed) with V(n-2): release both slots.
+        // (Releasing them with tcgen05.commit from the MMA threads instead, right
+        // after the MMAs that read them, made the forward 6-11 % slower.)
         if (lane == 0) {
-          mbar_arrive(&bars->kv_empty[(2 * n) % NSTD]);
-          if (n > 1) mbar_arrive(&bars->kv_empty[(2 * n - 3) % NSTD]);
+          mbar_arrive(&bars->k_empty[n % NKS]);
+          if (n > 1) mbar_arrive(&bars->v_empty[(n - 2) % NVS]);
         }
         const uint32_t t_s = t_s0 + (n & 1) * BN;
         uint32_t sr[BN];
