@@ -33,6 +33,11 @@
 // through the just-finished Q stage; warp 3 issues the TMA reduce-adds of the
 // dS-buffer half first and hands that buffer back to the next step's dS as soon
 // as the TMA has read it, then those of the Q-stage half.
+// Where an operation needs several events, they complete one mbarrier with
+// several expected arrivals (dP^T(t): dO(t) landed and dQ(t-1) read out; the
+// element-wise dS phase: dP^T(t) done and the dS buffer's staging read), so
+// that the issuing thread waits once: every wait on the MMA thread's and the
+// element-wise warps' path costs latency per step.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -123,13 +128,12 @@ struct BBars {
   uint64_t kv_full;
   uint64_t q_full[NQ];
   uint64_t q_empty[NQ];
-  uint64_t do_full;
+  uint64_t dp_ready;  // dO(t) landed and dQ(t-1) read out of TMEM: dP^T(t) may go
   uint64_t do_empty;
   uint64_t vec_full[NV];
   uint64_t vec_empty[NV];
-  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, dk_done;
+  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dk_done;
   uint64_t stg_ready[2];  // dQ staging written: [0] dS buffer half, [1] Q stage half
-  uint64_t stg_free;      // the dS buffer half has been read by the TMA
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -205,22 +209,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
     }
-    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->dp_ready, 1 + 256);  // dO(t) (TMA) + the 256 read-outs of dQ(t-1)
     mbar_init(&bars->do_empty, 1);
     for (int i = 0; i < NV; ++i) {
       mbar_init(&bars->vec_full[i], 1);
       mbar_init(&bars->vec_empty[i], 256);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_full, 2);  // dP^T(t) complete, and the dS buffer's staging of step t-1 read
     mbar_init(&bars->p_full, 256);
     mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_empty, 256);
     mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->stg_ready[0], 128);
     mbar_init(&bars->stg_ready[1], 128);
-    mbar_init(&bars->stg_free, 1);  // arrived by the reduce issuer once the TMA read the staging
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -296,10 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         ok = mbar_wait(&bars->do_empty, (t & 1) ^ 1, ctx);
         if (ok) {
-          mbar_arrive_expect_tx(&bars->do_full, L::kTile);
+          mbar_arrive_expect_tx(&bars->dp_ready, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_4d(smem_u32(smem + L::do_off + c * L::kChunk), &tm_do, c * 64, h, qt * BM, bi,
-                        &bars->do_full);
+                        &bars->dp_ready);
           last_do = t;
         }
       }
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&bars->kv_full, 0, a.status);
       for (int i = 0; i < NQ; ++i)
         if (last_q[i] >= 0) mbar_wait_drain(&bars->q_full[i], last_q[i] & 1, a.status);
-      if (last_do >= 0) mbar_wait_drain(&bars->do_full, last_do & 1, a.status);
+      if (last_do >= 0) mbar_wait_drain(&bars->dp_ready, last_do & 1, a.status);
     }
   } else if (warp == 1) {
     // ======================================================== MMA issuer
@@ -351,9 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ss_nosw(t_s, e_s, aug, id_kk, 1u);
         mma_commit(&bars->s_full);
         // dP^T = V dO^T
-        ok = mbar_wait(&bars->do_full, t & 1, ctx);
-        // dP^T overwrites the previous dQ tile: it must have been read out
-        if (ok && t > 0) ok = mbar_wait(&bars->dq_empty, (t - 1) & 1, ctx);
+        // dO(t) landed and (dP^T overwrites the previous dQ tile) dQ(t-1) read out
+        ok = mbar_wait(&bars->dp_ready, t & 1, ctx);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -398,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int t = 0;
       bool ok = true;
+      mbar_arrive(&bars->dp_full);  // step 0's dS buffer holds no staging
       for (StepIter it = it0; it.valid() && ok; it.next(), ++t) {
         const int h = kvh * a.g + it.hh;
         const int qt = it.i;
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_reduce_add_4d(&tm_dq, s0 + k * L::kChunk, 32 * k, h, qt * BM, bi);
         bulk_commit_group();
         // The next step's stg_ready[1] phase must not complete before this wait
-        // has seen the current one: it follows stg_free below, arrived after.
+        // has seen the current one: it follows the dp_full arrival below.
         ok = mbar_wait(&bars->stg_ready[1], t & 1, ctx);
         if (!ok) break;
 #pragma unroll
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_reduce_add_4d(&tm_dq, s1 + k * L::kChunk, kHalfR + 32 * k, h, qt * BM, bi);
         bulk_commit_group();
         bulk_wait_group_read<1>();
-        mbar_arrive(&bars->stg_free);  // dS buffer half read: reusable
+        mbar_arrive(&bars->dp_full);  // dS buffer half read: the next step's dS may go there
         bulk_wait_group_read<0>();
         mbar_arrive(&bars->q_empty[t % NQ]);  // Q stage reusable
       }
@@ -496,6 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kRounds = kHalf / 32;  // 32-column staging boxes per half
     int t = 0;
     bool ok = true;
+    // step 0's dP^T has no previous dQ tile to wait for
+    mbar_arrive(&bars->dp_ready);
     for (; t < nsteps_total; ++t) {
       const int en = t % NV;
       ok = mbar_wait(&bars->vec_full[en], (t / NV) & 1, ctx);
@@ -561,13 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk2[c] = pack_bf16(d0, d1);
       }
       tmem_st32(tmem + lane_off + kColS + 64 * w + 32, pk2);
-      // The dS buffer doubles as the dQ staging area of the previous step: wait
-      // until the TMA has read it.
-      if (t > 0) {
-        ok = mbar_wait(&bars->stg_free, (t - 1) & 1, ctx);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
+      // (The dS buffer doubles as the dQ staging area of the previous step:
+      // dp_full also waited until the TMA had read it.)
       // dS (queries x keys) in shared memory, MN-major 128B-swizzled: key row kr
       // holds this half's 64 query values.
 #pragma unroll
@@ -579,8 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->ds_full);
-      // dQ tile readout: TMEM lanes are query rows here
-      ok = mbar_wait(&bars->dq_full, t & 1, ctx);
+      // dQ tile readout: TMEM lanes are query rows here.  Half 1 stages its
+      // columns in the Q stage, whose last reader is dK (issued after dQ): it
+      // waits for dK alone, whose commit covers dQ too.
+      ok = (w == 0) ? mbar_wait(&bars->dq_full, t & 1, ctx) : mbar_wait(&bars->dk_done, t & 1, ctx);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -590,16 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kHalf; c += 32) tmem_ld32(src + c, &q[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bars->dq_empty);
+      mbar_arrive(&bars->dp_ready);  // for the next step's dP^T
       // dQ (scaled already: dS carries the factor) into the fp32 accumulator.  Half 0 stages its columns in
       // the dS buffer (free: the dQ MMA has read it), half 1 in the Q stage of
       // this step (free once dK, its last reader, is done), as 32-column boxes
       // of 128 rows x 128 B (128B-swizzled); warp 3 issues the reduce-adds.
-      if (w == 1) {
-        ok = mbar_wait(&bars->dk_done, t & 1, ctx);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
       {
         uint8_t* stage = (w == 0) ? smem + L::ds_off : smem + L::q_off + (t % NQ) * L::kTile;
 #pragma unroll

@@ -28,7 +28,11 @@
 //
 // Both kernels: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warp 2
 // per-step vector / descriptor loader, warps 4-11 two element-wise
-// warpgroups (warp 3 idle).  Every wait is bounded (see ptx.cuh).
+// warpgroups (warp 3 idle).  Every wait is bounded (see ptx.cuh).  Where a
+// product needs its operand tile and a TMEM region to be free, both events
+// complete the tile's barrier (the region's readers arrive on it as well), so
+// the MMA thread waits once per product: each extra wait on its path costs
+// latency every step.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -143,7 +147,7 @@ struct ABars {
   uint64_t do_empty[2];
   uint64_t vec_full[NV];
   uint64_t vec_empty[NV];
-  uint64_t s_full, dp_full, p_full, ds_full, dp_free, dk_done, drain;
+  uint64_t s_full, dp_full, p_full, ds_full, dk_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -222,9 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->k_full, 256);  // every element-wise thread stores its part of the key tile
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->q_full[i], 1);
+      // Q(t) landed (TMA) and dP^T(t-1) read by the 256 element-wise threads
+      // (S^T(t) goes into the region dP^T(t-1) leaves)
+      mbar_init(&bars->q_full[i], 1 + 256);
       mbar_init(&bars->q_empty[i], 1);
-      mbar_init(&bars->do_full[i], 1);
+      // dO(t) landed (TMA) and dK(t-1) done (dP^T(t) goes into the region
+      // P^T / dS^T(t-1) leave; MMA commit)
+      mbar_init(&bars->do_full[i], 1 + 1);
       mbar_init(&bars->do_empty[i], 1);
     }
     for (int i = 0; i < NV; ++i) {
@@ -235,7 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, 256);
     mbar_init(&bars->ds_full, 256);
-    mbar_init(&bars->dp_free, 256);
     mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -348,8 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S^T(t) - c = K Q^T + E_S Aug^T into region t  (M = keys, N = BM queries)
         auto issue_s = [&](int t) -> bool {
           const int qs = t % NQ;
-          bool w_ok = mbar_wait(&bars->q_full[qs], (t / NQ) & 1, ctx);
-          if (w_ok) w_ok = mbar_wait(&bars->vec_full[t % NV], (t / NV) & 1, ctx);
+          // the augment tile (usually ready long before), then Q(t) and the region
+          bool w_ok = mbar_wait(&bars->vec_full[t % NV], (t / NV) & 1, ctx);
+          if (w_ok) w_ok = mbar_wait(&bars->q_full[qs], (t / NQ) & 1, ctx);
           if (!w_ok) return false;
           tc_fence_after();
           const uint32_t qstage = (uint32_t)(qs * L::kQTile) >> 4;
@@ -398,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (KT || VT) {
           if (ok) ok = mbar_wait(&bars->k_full, 0, ctx);
         }
+        mbar_arrive(&bars->do_full[0]);  // step 0 has no dK before it
         if (ok && nsteps_total > 0) ok = issue_s(0) && issue_dp(0);
         for (int t = 0; t < nsteps_total && ok; ++t) {
           const int qs = t % NQ, os = t % NO;
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // can only arrive once dK(t) has released the stage.
           if constexpr (NQ > 1) {
             if (t + 1 < nsteps_total) {
-              ok = mbar_wait(&bars->dp_free, t & 1, ctx) && issue_s(t + 1);
+              ok = issue_s(t + 1);
               if (!ok) break;
             }
           }
@@ -438,14 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bars->dk_done);
           mma_commit(&bars->q_empty[qs]);
+          if (t + 1 < nsteps_total) mma_commit(&bars->do_full[(t + 1) % NO]);
           if constexpr (NQ == 1) {
             if (t + 1 < nsteps_total) {
-              ok = mbar_wait(&bars->dp_free, t & 1, ctx) && issue_s(t + 1);
+              ok = issue_s(t + 1);
               if (!ok) break;
             }
           }
           if (t + 1 < nsteps_total) {
-            ok = mbar_wait(&bars->dk_done, t & 1, ctx) && issue_dp(t + 1);
+            ok = issue_dp(t + 1);
             if (!ok) break;
           }
         }
@@ -545,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int t = 0;
     bool ok = true;
+    mbar_arrive(&bars->q_full[0]);  // S^T(0) has no dP^T before it to wait for
     for (; t < nsteps_total; ++t) {
       const int en = t % NV;
       // this half's S^T columns (region t & 1) and dP^T columns (the other region)
@@ -601,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kHB; c += 32) tmem_ld32(t_dph + c, &r[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bars->dp_free);
+      mbar_arrive(&bars->q_full[(t + 1) % NQ]);  // S^T(t+1) may take the dP^T region
       mbar_arrive(&bars->vec_empty[en]);
 #pragma unroll
       for (int c = 0; c < kHB / 2; ++c) {
@@ -724,7 +735,7 @@ struct QTBars {
   uint64_t kv_empty[8];
   uint64_t id_full[NID];
   uint64_t id_empty[NID];
-  uint64_t s_full, s_free, dp_full, ds_full, dq_done, drain;
+  uint64_t s_full, dp_full, ds_full, dq_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -763,8 +774,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 256);  // every element-wise thread stores its row (or arrives)
     mbar_init(&bars->do_full, 1);
+    // K tiles take the even slots, V tiles the odd ones (NKV is even).  K(n):
+    // landed (TMA) and S(n-1) loaded by the 256 element-wise threads (S(n)
+    // overwrites it); V(n): landed and dQ(n-1) done (dP(n) overwrites the dS
+    // columns dQ(n-1) reads; MMA commit).
+    static_assert(NKV % 2 == 0, "K / V slots alternate");
     for (int i = 0; i < NKV; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_full[i], (i % 2 == 0) ? 1 + 256 : 1 + 1);
       mbar_init(&bars->kv_empty[i], 1);
     }
     for (int i = 0; i < NID; ++i) {
@@ -772,7 +788,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->id_empty[i], 256);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 256);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->dq_done, 1);
@@ -882,10 +897,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (!OT) {
           if (ok) ok = mbar_wait(&bars->do_full, 0, ctx);
         }
+        mbar_arrive(&bars->kv_full[1]);  // dP(0) has no dQ before it
         if (ok && nt > 0) ok = issue_s(0) && issue_dp(0);
         for (int n = 0; n < nt && ok; ++n) {
           if (n + 1 < nt) {
-            ok = mbar_wait(&bars->s_free, n & 1, ctx) && issue_s(n + 1);
+            ok = issue_s(n + 1);
             if (!ok) break;
           }
           ok = mbar_wait(&bars->ds_full, n & 1, ctx);
@@ -901,8 +917,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kb + (uint32_t)((kk * 16 * 128) >> 4), id_q, (n > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars->dq_done);
           mma_commit(&bars->kv_empty[kslot]);  // K(n): S(n) and dQ(n) have read it
+          if (n + 1 < nt) mma_commit(&bars->kv_full[(2 * n + 3) % NKV]);  // V(n+1)'s barrier
           if (n + 1 < nt) {
-            ok = mbar_wait(&bars->dq_done, n & 1, ctx) && issue_dp(n + 1);
+            ok = issue_dp(n + 1);
             if (!ok) break;
           }
         }
@@ -989,6 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_dph = tmem + lane_off + L::kColDP + kHB * w;
     int n = 0;
     bool ok = true;
+    mbar_arrive(&bars->kv_full[0]);  // S(0) overwrites no earlier S
     for (; n < nt; ++n) {
       const int en = n % NID;
       ok = mbar_wait(&bars->id_full[en], (n / NID) & 1, ctx);
@@ -1001,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kHB; c += 32) tmem_ld32(t_sh + c, &r[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bars->s_free);  // S(n+1) may overwrite the S columns
+      mbar_arrive(&bars->kv_full[(2 * n + 2) % NKV]);  // S(n+1) may overwrite the S columns
       float p[kHB];
 #pragma unroll
       for (int u = 0; u < kHB; u += 2) {
