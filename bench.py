@@ -606,25 +606,31 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         # the same K steps as the device-timed value; the first copy-in and
         # the last copy-out are not hidden behind a neighbouring step
+        # three passes of the K steps, the median reported: the host link is
+        # shared with other tenants on these boxes and can stall one pass
         n_e2e = max(2, args.steps)
-        if dist:
-            dist.barrier()
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s_h2d)
-        run(n_e2e)
-        s_d2h.wait_stream(stream)
-        b_.record(s_d2h)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(a.elapsed_time(b_) / n_e2e, dist, dev)
+        passes = []
+        for _ in range(3):
+            if dist:
+                dist.barrier()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s_h2d)
+            run(n_e2e)
+            s_d2h.wait_stream(stream)
+            b_.record(s_d2h)
+            torch.cuda.synchronize()
+            passes.append(max_over_ranks(a.elapsed_time(b_) / n_e2e, dist, dev))
+        e2e_ms = median(passes)
         link = host_link(h_in["q"], d_in[0]["q"], h_out[0]["dq"], s_h2d)
         e2e = {"value": whole_job_tflops(world, fwd_flop + bwd_flop, e2e_ms),
-               "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": bi,
+               "unit": "TFLOP/s", "ms_per_step": e2e_ms, "passes_ms_per_step": passes,
+               "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo,
                "copies": "every step's inputs in and gradients out inside the timed region, "
                          "on one copy stream (one direction at a time) overlapping the "
                          "neighbouring steps' compute (double-buffered device tensors); a "
                          "step's forward starts once its own inputs have landed, its dout "
-                         "copy overlapping it",
+                         "copy overlapping it; the median of three passes of the K steps",
                "host_link": link,
                # the copies alone, one after the other at the one-way rates
                "copy_bound_ms": 1e3 * (bi / (link["h2d_gbs"] * 1e9) + bo / (link["d2h_gbs"] * 1e9))}
