@@ -128,6 +128,17 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
+// First plan tile at or after j in [j, last] whose class is not SKIP (last + 1
+// if none): 32 class bytes per warp load.  All 32 lanes must call it.
+__device__ __forceinline__ int next_live_tile(const uint8_t* cls_row, int j, int last, int lane) {
+  for (; j <= last; j += 32) {
+    const uint8_t cl = (j + lane <= last) ? cls_row[j + lane] : (uint8_t)kSkip;
+    const uint32_t live = __ballot_sync(0xffffffffu, cl != kSkip);
+    if (live != 0u) return j + __ffs(live) - 1;
+  }
+  return last + 1;
+}
+
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -228,7 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < NVS; ++i) last_v[i] = -1;
     bool ok = true;
     for (int j2 = 2 * rng.x; j2 <= 2 * rng.y + 1 && ok && !a.withhold_kv; ++j2) {
-      if (cls_row[j2 >> 1] == kSkip) continue;
+      if (cls_row[j2 >> 1] == kSkip) {
+        // jump over the run of SKIP tiles (the loop header then takes j2 to the
+        // first half of the next live plan tile)
+        j2 = 2 * next_live_tile(cls_row, (j2 >> 1) + 1, rng.y, lane) - 1;
+        continue;
+      }
       // K tile, then V tile of 64-key tile j2, each into its own ring
       if (lane == 0) {
         const int sk = n % NKS, uk = n / NKS;
@@ -335,7 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j2 = 2 * rng.x; j2 <= 2 * rng.y + 1 && ok; ++j2) {
       const uint8_t kind = cls_row[j2 >> 1];
-      if (kind == kSkip) continue;
+      if (kind == kSkip) {
+        j2 = 2 * next_live_tile(cls_row, (j2 >> 1) + 1, rng.y, lane) - 1;
+        continue;
+      }
       const int j = j2;  // 64-key tile index
       const int en = n % NIDD, use = n / NIDD;
       const int64_t base = (int64_t)bi * a.s_kv;
