@@ -341,8 +341,9 @@ def per_config(ga, dev, pk, big=None):
     """fwd / bwd TFLOP/s (valid pairs; medians of 10 single calls after 3
     warm-ups) on every workload of the pages' set, the ring workload as one
     call, as R = 4 logical ring shards (fused and separate merge, forward and
-    backward), and the all-gather strategy at the tutorial's 64k shape with
-    stripe 512 (``big`` = the resident full_swa_64k inputs, if any)."""
+    backward), and the all-gather strategy (forward and backward) at the
+    tutorial's 64k shape with stripe 512 (``big`` = the resident full_swa_64k
+    inputs, if any)."""
     import torch
 
     import workload
@@ -410,18 +411,24 @@ def per_config(ga, dev, pk, big=None):
             "what": "attn_bwd(deterministic=True): dK / dV kernel + dQ kernel, dQ summed on "
                     "chip in a fixed order (bit-identical run to run)",
             "bwd_ms": det_ms, "bwd_tflops": 10 * w.d * w.hq * pairs / det_ms / 1e9}
-        del out, lse, ws, grads
+        del ws, grads
         torch.cuda.empty_cache()
-        ag = lambda: ring.allgather_attn_fwd(big["q"], big["k"], big["v"], big["ids"], big["pos"],
-                                             4, window_left=w.window_left, scale=w.scale,
-                                             stripe_size=512, check_status=False)
+        ag = lambda: ring.allgather_attn_fwd(q, k, v, ids, pos, 4, window_left=w.window_left,
+                                             scale=w.scale, stripe_size=512, check_status=False)
+        agb = lambda: ring.allgather_attn_bwd(q, k, v, out, lse, big["dout"], ids, pos, 4,
+                                              window_left=w.window_left, scale=w.scale,
+                                              stripe_size=512, check_status=False)
         ag_ms = _timed_calls(ag, iters=5)
-        ff = 4 * w.d * w.hq * pairs
+        agb_ms = _timed_calls(agb, iters=5)
+        ff, bf = 4 * w.d * w.hq * pairs, 10 * w.d * w.hq * pairs
         res["allgather_64k"] = {
             "what": "full_swa_64k as 4 logical all-gather shards (striped reorder, stripe 512; "
-                    "each shard's queries against the whole reordered K/V in one attn_fwd; "
-                    "inverse reorder)",
-            "fwd_ms": ag_ms, "fwd_tflops": ff / ag_ms / 1e9}
+                    "forward: each shard's queries against the whole reordered K/V in one "
+                    "attn_fwd; backward: one attn_bwd per shard against the whole K/V, dK / dV "
+                    "accumulated over the shards in fp32; inverse reorder)",
+            "fwd_ms": ag_ms, "fwd_tflops": ff / ag_ms / 1e9, "bwd_ms": agb_ms,
+            "bwd_tflops": bf / agb_ms / 1e9, "step_tflops": (ff + bf) / (ag_ms + agb_ms) / 1e9}
+        del out, lse
         torch.cuda.empty_cache()
     return res
 

@@ -233,3 +233,58 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
         log.check("ring_attn_bwd")
     inv = lambda x: inverse_reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
     return inv(dq), inv(dk), inv(dv)
+
+
+def allgather_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *,
+                       window_left: int = -1, scale: Optional[float] = None,
+                       strategy: int = STRIPED, stripe_size: int = 512,
+                       check_status: bool = True, deterministic: bool = False):
+    """Backward of all-gather context parallelism, emulated on one GPU (TE
+    tutorial section 5, "AllGather"; "Context parallelism and ring attention",
+    section "Communication choices").
+
+    Shard r keeps its query rows, final output O_r, LSE_r and dO_r of the
+    reordered sequence and meets the whole reordered K/V (its all-gathered
+    copy) in one attn_bwd call: that call gives dQ_r in full and adds the
+    shard's share of dK and dV into accumulators over the whole sequence (on a
+    mesh, a reduce-scatter of those accumulators returns every device its own
+    rows).  P uses the final LSE and D = rowsum(dO * O) the final output, so
+    the sum over shards is the full gradient.  Returns (dq, dk, dv) fp32 in
+    natural token order.  ``check_status`` and ``deterministic`` as in
+    :func:`ring_attn_bwd`.
+    """
+    b, s, hq, d = q.shape
+    R = int(cp_size)
+    if s % R:
+        raise ValueError("sequence length must be divisible by cp_size")
+    n = s // R
+    dev = q.device
+    re = lambda x: reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
+    qr, kr, vr, outr, dor = re(q), re(k), re(v), re(out), re(dout)
+    idr, posr = re(ids), re(pos)
+    dq = torch.zeros(b, s, hq, d, dtype=torch.float32, device=dev)
+    dk = torch.zeros(b, s, k.shape[2], d, dtype=torch.float32, device=dev)
+    dv = torch.zeros(b, s, k.shape[2], v.shape[3], dtype=torch.float32, device=dev)
+    lse_sh = torch.empty(R, hq, n, dtype=torch.float32, device=dev)
+    ws = torch.empty(workspace_bytes_bwd(qr[:1, :n], kr[:1], idr[:1, :n], posr[:1, :n],
+                                         window_left, v=vr[:1], deterministic=deterministic),
+                     dtype=torch.uint8, device=dev)
+    log = _StatusLog(b * R, dev) if check_status else None
+    for bi in range(b):
+        # this row's LSE in reordered order, then [Hq, R*n] -> [R, Hq, n]
+        lse_r = reorder_causal_lb(lse[bi], strategy, R, stripe_size, seq_dim=1)
+        inverse_reorder_causal_lb(lse_r.view(1, hq * s), STRIPED, hq, n, seq_dim=1,
+                                  out=lse_sh.view(1, R * hq * n))
+        kv = slice(bi, bi + 1)
+        for r in range(R):
+            rows = slice(r * n, (r + 1) * n)
+            attn_bwd(qr[kv, rows], kr[kv], vr[kv], outr[kv, rows], lse_sh[r:r + 1], dor[kv, rows],
+                     idr[kv, rows], posr[kv, rows], idr[kv], posr[kv], window_left=window_left,
+                     scale=scale, dq=dq[kv, rows], dk=dk[kv], dv=dv[kv], accumulate_fp32=True,
+                     workspace=ws, deterministic=deterministic)
+            if log is not None:
+                log.record(ws)
+    if log is not None:
+        log.check("allgather_attn_bwd")
+    inv = lambda x: inverse_reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
+    return inv(dq), inv(dk), inv(dv)

@@ -222,3 +222,77 @@ def test_ring_backward_deterministic_mode(ring):
     check_grad(runs[0][0].cpu(), rq, "dq")
     check_grad(runs[0][1].cpu(), rk, "dk")
     check_grad(runs[0][2].cpu(), rv, "dv")
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,window,slots,R,strategy,stripe", [
+    (1, 4096, 4, 2, 128, -1, 4, 4, RO.STRIPED, 512),
+    (2, 2048, 4, 1, 64, 300, 2, 4, RO.STRIPED, 128),
+    (1, 3072, 2, 2, 128, -1, None, 3, RO.DUAL_CHUNK, 1),
+])
+def test_allgather_backward_matches_oracle(ring, b, s, hq, hkv, d, window, slots, R, strategy,
+                                           stripe):
+    """All-gather backward: each shard's queries against the whole reordered
+    K/V in one attn_bwd call, dK/dV summed over the shards in fp32; equals the
+    oracle's full backward, with exact zeros on padding."""
+    from tests.parity import check_grad
+    q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=R * 11 + s, with_dout=True)
+    ids, pos = workload.segments(b, s, slots)
+    g = [x.to(DEV) for x in (q, k, v, dout, ids, pos)]
+    out, lse = ring.allgather_attn_fwd(g[0], g[1], g[2], g[4], g[5], R, window_left=window,
+                                       scale=d ** -0.5, strategy=strategy, stripe_size=stripe)
+    dq, dk, dv = ring.allgather_attn_bwd(g[0], g[1], g[2], out, lse, g[3], g[4], g[5], R,
+                                         window_left=window, scale=d ** -0.5, strategy=strategy,
+                                         stripe_size=stripe)
+    torch.cuda.synchronize()
+    rq, rk, rv = A.attn_bwd(q, k, v, dout, ids, pos, ids, pos, window, d ** -0.5)
+    check_grad(dq.cpu(), rq, "dq")
+    check_grad(dk.cpu(), rk, "dk")
+    check_grad(dv.cpu(), rv, "dv")
+    pad = (ids == 0).to(DEV)
+    assert torch.all(dq[pad] == 0) and torch.all(dk[pad] == 0) and torch.all(dv[pad] == 0)
+
+
+def test_allgather_backward_tutorial_shape(ring):
+    """The TE tutorial's AllGather case (64k packed workload, 4 shards, stripe
+    512) backward: equal to the single-call backward on every element (both
+    within the gradient tolerance of each other) and to the oracle on sampled
+    query rows (dQ) and key tiles (dK, dV, complete: every row that sees those
+    keys is included)."""
+    import long_context_attention_attn_gb300 as ga
+    from tests.parity import check_grad
+    w = workload.WORKLOADS["full_swa_64k"]
+    x = workload.make(w, device=DEV, with_dout=True)
+    q, k, v, ids, pos, dout = x["q"], x["k"], x["v"], x["ids"], x["pos"], x["dout"]
+    out, lse = ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale)
+    dq, dk, dv = ring.allgather_attn_bwd(q, k, v, out, lse, dout, ids, pos, 4,
+                                         window_left=w.window_left, scale=w.scale)
+    fq, fk, fv = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=w.window_left,
+                             scale=w.scale)
+    torch.cuda.synchronize()
+    for name, a_, b_ in (("dq", dq, fq), ("dk", dk, fk), ("dv", dv, fv)):
+        num = (a_.float() - b_.float()).norm().item()
+        den = b_.float().norm().item()
+        assert num <= 1e-2 * den, f"all-gather vs single-call {name}: rel-L2 {num / den:.3e}"
+    del fq, fk, fv
+    g = w.hq // w.hkv
+    idc, psc = ids.cpu(), pos.cpu()
+    for bi, kvh, r0, nr in ((0, 1, 9000, 64), (1, 6, 3 * 16384 + 5000, 64)):
+        hs = slice(kvh * g, kvh * g + g)
+        rows = np.arange(r0, r0 + nr)
+        rq, _, _ = A.attn_bwd(q[bi:bi + 1, :, hs].cpu(), k[bi:bi + 1, :, kvh:kvh + 1].cpu(),
+                              v[bi:bi + 1, :, kvh:kvh + 1].cpu(), dout[bi:bi + 1, :, hs].cpu(),
+                              idc[bi:bi + 1], psc[bi:bi + 1], idc[bi:bi + 1], psc[bi:bi + 1],
+                              w.window_left, w.scale, rows=rows)
+        check_grad(dq[bi, r0:r0 + nr, hs].cpu(), rq[0, rows], f"dq b{bi} kvh{kvh} r{r0}")
+    for bi, kvh, k0, nk in ((0, 3, 16384 + 11000, 64),):
+        keys = np.arange(k0, k0 + nk)
+        rows = A.rows_seeing_keys(idc[bi], psc[bi], idc[bi], psc[bi], w.window_left, keys)
+        hs = slice(kvh * g, kvh * g + g)
+        _, rk, rv = A.attn_bwd(q[bi:bi + 1, :, hs].cpu(), k[bi:bi + 1, :, kvh:kvh + 1].cpu(),
+                               v[bi:bi + 1, :, kvh:kvh + 1].cpu(), dout[bi:bi + 1, :, hs].cpu(),
+                               idc[bi:bi + 1], psc[bi:bi + 1], idc[bi:bi + 1], psc[bi:bi + 1],
+                               w.window_left, w.scale, rows=rows)
+        check_grad(dk[bi, k0:k0 + nk, kvh].cpu(), rk[0, keys, 0], f"dk b{bi} kvh{kvh} k{k0}")
+        check_grad(dv[bi, k0:k0 + nk, kvh].cpu(), rv[0, keys, 0], f"dv b{bi} kvh{kvh} k{k0}")
+    del x, out, lse, dq, dk, dv
+    torch.cuda.empty_cache()
