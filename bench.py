@@ -506,9 +506,12 @@ def run_ours(args, rank, world, local_rank):
         if ev:
             ev[1].record(stream)
         if not fwd_only:
+            # ev[3] / ev[4]: recorded by attn_bwd right before and after its main
+            # kernel(s), the roofline's timing
             ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, window_left=w.window_left,
                         scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-                        deterministic=args.deterministic)
+                        deterministic=args.deterministic,
+                        kernel_events=(ev[3], ev[4]) if ev else None)
         if ev:
             ev[2].record(stream)
 
@@ -519,7 +522,7 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status {ga.status_string(status)}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = Clocks(local_rank)
     if dist:
         dist.barrier()
@@ -538,6 +541,7 @@ def run_ours(args, rank, world, local_rank):
     # per-call figures: medians over the timed steps
     fwd_avg = median([e[0].elapsed_time(e[1]) for e in evs])
     bwd_avg = median([e[1].elapsed_time(e[2]) for e in evs])
+    bwd_kernel_ms = None if fwd_only else median([e[3].elapsed_time(e[4]) for e in evs])
     ms_per_step = max_over_ranks(total_ms / args.steps, dist, dev)
     value = whole_job_tflops(world, fwd_flop + bwd_flop, ms_per_step)
 
@@ -658,6 +662,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_per_config:
         per_cfg = per_config(ga, dev, pk, big=x if w.name == WORKLOAD else None)
     bwd_tflops = bwd_flop / (bwd_avg * 1e-3) / 1e12
+    bwd_kernel_tflops = bwd_flop / (bwd_kernel_ms * 1e-3) / 1e12
     per_gpu = value / world
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -690,17 +695,25 @@ def run_ours(args, rank, world, local_rank):
                         "sustained": 100 * per_gpu / pk["bf16_sustained"],
                         "source": pk["source"]},
         "components": {"fwd_ms": fwd_avg, "bwd_ms": bwd_avg, "fwd_tflops": fwd_tflops,
-                       "bwd_tflops": bwd_tflops,
+                       "bwd_tflops": bwd_tflops, "bwd_kernel_ms": bwd_kernel_ms,
+                       "bwd_kernel_tflops": bwd_kernel_tflops,
                        "fwd_pct_of_burst_peak": 100 * fwd_tflops / pk["bf16_burst"],
                        "bwd_pct_of_burst_peak": 100 * bwd_tflops / pk["bf16_burst"],
-                       "timing": "medians of the timed steps' per-call CUDA events",
+                       "timing": "medians of the timed steps' per-call CUDA events; "
+                                 "bwd_kernel_ms: the backward's main kernel(s) alone, between "
+                                 "events attn_bwd records around their launch",
                        "hbm_rows": hbm, "per_config": per_cfg},
-        "roofline": {"kernel": ("attn_bwd (dK / dV kernel + dQ kernel + D pre-pass and plan; "
-                                "timed per call)" if split_bwd else
-                                "attn_bwd (fused backward + its D pre-pass, plan and dQ "
-                                "finalise; timed per call)"),
-                     "bound": "tensor", "achieved": bwd_tflops, "peak": pk["bf16_sustained"],
-                     "unit": "TFLOP/s", "frac": bwd_tflops / pk["bf16_sustained"],
+        "roofline": {"kernel": ("attn_bwd_dkdv_kernel + attn_bwd_dq_tmem_kernel (timed between "
+                                "CUDA events attn_bwd records around them, on its stream)"
+                                if split_bwd else
+                                "attn_bwd_kernel (the fused backward kernel, timed between CUDA "
+                                "events attn_bwd records around its launch, on its stream)"),
+                     "bound": "tensor", "achieved": bwd_kernel_tflops,
+                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                     "frac": bwd_kernel_tflops / pk["bf16_sustained"],
+                     "call": {"what": "the whole attn_bwd call (plan, D pre-pass, kernel(s), "
+                                      "dQ finalise)", "achieved": bwd_tflops,
+                              "frac": bwd_tflops / pk["bf16_sustained"]},
                      "peak_kind": f"bf16 sustained, {pk['source']}",
                      "traffic": bwd_traffic() if (w.name == WORKLOAD and not split_bwd) else None,
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read+write)"},

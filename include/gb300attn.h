@@ -154,6 +154,14 @@ typedef struct attn_fwd_params {
  *                   summed in a fixed order on chip and written once, so every
  *                   output is bit-identical from run to run (slower at d <= 128).
  *                   d = 256 and (192, 128) always take this pair.
+ *  kernel_events    optional timing hook: two events (cudaEvent_t cast to
+ *                   void*) that the caller created, or both NULL.  attn_bwd then
+ *                   records kernel_events[0] on the stream just before its main
+ *                   kernel (the fused kernel, or the dK / dV kernel of the pair)
+ *                   and kernel_events[1] just after it (after the dQ kernel of
+ *                   the pair), so that their elapsed time is the main kernels'
+ *                   alone, without the tile plan, the D pre-pass and the dQ
+ *                   finalise.  Setting only one of them is ATTN_ERR_INVALID_ARG.
  */
 typedef struct attn_bwd_params {
   attn_fwd_params fwd;
@@ -163,6 +171,7 @@ typedef struct attn_bwd_params {
   void* dv;
   int32_t accumulate_fp32;
   int32_t deterministic;
+  void* kernel_events[2];
 } attn_bwd_params;
 
 /* Scratch sizes (bytes) for the given problem; 0 on invalid sizes. */

@@ -244,6 +244,14 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t dv = fwd_dv(f);
   if (p->deterministic != 0 && p->deterministic != 1) return ATTN_ERR_INVALID_ARG;
+  if ((p->kernel_events[0] == nullptr) != (p->kernel_events[1] == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  // optional timing hook around the main kernel(s)
+  auto mark = [&](int i) -> cudaError_t {
+    return p->kernel_events[i]
+               ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(p->kernel_events[i]), st)
+               : cudaSuccess;
+  };
   if (use_split_bwd(p)) {
     SplitLaunch sl;
     sl.p = p;
@@ -265,7 +273,9 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
     if (e == cudaSuccess) e = launch_tile_plan(*f, sl.plan, sl.nq, sl.nk, true, st);
     if (e == cudaSuccess)
       e = launch_bwd_preprocess(f->out, p->dout, sl.D, nullptr, f->b, f->s_q, f->h_q, dv, st);
+    if (e == cudaSuccess) e = mark(0);
     if (e == cudaSuccess) e = launch_attn_bwd_split(sl, st);
+    if (e == cudaSuccess) e = mark(1);
     if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
     return cuda_status(e);
   }
@@ -296,7 +306,9 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   if (e == cudaSuccess)
     e = launch_bwd_preprocess(f->out, p->dout, bl.D, acc ? nullptr : bl.dq_acc, f->b, f->s_q,
                               f->h_q, f->d, st);
+  if (e == cudaSuccess) e = mark(0);
   if (e == cudaSuccess) e = launch_attn_bwd(bl, st);
+  if (e == cudaSuccess) e = mark(1);
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
   if (e == cudaSuccess && !acc) e = launch_dq_finalize(bl.dq_acc, p->dq, (int64_t)n_dq, st);
   return cuda_status(e);

@@ -233,3 +233,28 @@ def test_heavy_first_order_is_stable_argsort(name, b, s):
     k_w = c.sum(axis=1).reshape(-1)
     np.testing.assert_array_equal(qo.cpu().numpy(), np.argsort(-q_w, kind="stable"))
     np.testing.assert_array_equal(ko.cpu().numpy(), np.argsort(-k_w, kind="stable"))
+
+
+@pytest.mark.parametrize("det", [False, True])
+def test_bwd_kernel_events_bracket_the_main_kernel(ga, det):
+    """attn_bwd's timing hook: the two events it records around its main
+    kernel(s) give a positive time inside the whole call's, and the gradients
+    are those of a call without the hook (bit for bit where the path is
+    deterministic; dK / dV always)."""
+    w = workload.WORKLOADS["packed_swa"]
+    x = workload.make(w, device=DEV, with_dout=True)
+    q, k, v, ids, pos, dout = x["q"], x["k"], x["v"], x["ids"], x["pos"], x["dout"]
+    out, lse = ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale)
+    kw = dict(window_left=w.window_left, scale=w.scale, deterministic=det)
+    ref = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, **kw)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record()
+    got = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, kernel_events=(ev[1], ev[2]), **kw,
+                      check_status=True)
+    ev[3].record()
+    torch.cuda.synchronize()
+    kernel_ms, call_ms = ev[1].elapsed_time(ev[2]), ev[0].elapsed_time(ev[3])
+    assert 0 < kernel_ms < call_ms
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+    if det:
+        assert torch.equal(got[0], ref[0])
