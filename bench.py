@@ -378,7 +378,12 @@ def per_config(ga, dev, pk, big=None):
             rf = lambda: ring.ring_attn_fwd(q, k, v, ids, pos, R, fused_merge=True, **kw)
             rs = lambda: ring.ring_attn_fwd(q, k, v, ids, pos, R, fused_merge=False, **kw)
             rb = lambda: ring.ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, R, **kw)
+            bf_ = lambda: ring.ring_attn_fwd(q, k, v, ids, pos, R, fused_merge=True,
+                                             batch_shards=True, **kw)
+            bb_ = lambda: ring.ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, R,
+                                             batch_shards=True, **kw)
             fused_ms, sep_ms, rb_ms = _timed_calls(rf), _timed_calls(rs), _timed_calls(rb)
+            bfw_ms, bbw_ms = _timed_calls(bf_), _timed_calls(bb_)
             res["ring_cp4_shards"] = {
                 "what": f"{R} logical dual-chunk ring shards: reorder, {R}x{R} block attn_fwd "
                         "calls with the merge folded into the epilogue (fused) or as a separate "
@@ -386,7 +391,12 @@ def per_config(ga, dev, pk, big=None):
                         "in fp32 accumulate mode with the final LSE",
                 "fwd_fused_ms": fused_ms, "fwd_separate_ms": sep_ms, "bwd_ms": rb_ms,
                 "fwd_fused_tflops": ff / fused_ms / 1e9, "fwd_separate_tflops": ff / sep_ms / 1e9,
-                "bwd_tflops": bf / rb_ms / 1e9}
+                "bwd_tflops": bf / rb_ms / 1e9,
+                "batched": {"what": "batch_shards=True: one call per ring step over all "
+                                    "shards, the held K/V blocks (and dK / dV sums) rotated "
+                                    "between steps",
+                            "fwd_ms": bfw_ms, "bwd_ms": bbw_ms,
+                            "fwd_tflops": ff / bfw_ms / 1e9, "bwd_tflops": bf / bbw_ms / 1e9}}
         del x, q, k, v, ids, pos, dout, ws, out, lse, dq, dk, dv
         torch.cuda.empty_cache()
     if big is not None:

@@ -50,7 +50,8 @@ class _StatusLog:
 
 def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
                   scale: Optional[float] = None, strategy: int = DUAL_CHUNK, stripe_size: int = 1,
-                  fused_merge: bool = True, check_status: bool = True):
+                  fused_merge: bool = True, check_status: bool = True,
+                  batch_shards: bool = False):
     """Forward attention computed as cp_size ring steps per logical shard.
 
     q bf16 [b,s,Hq,d]; k, v bf16 [b,s,Hkv,d]; ids/pos int32 [b,s] (natural
@@ -60,6 +61,10 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
     ``check_status`` reads every call's device status word once at the end
     (one synchronisation) and raises :class:`AttnError` if a bounded
     device-side wait gave up, rather than returning undefined output.
+    ``batch_shards`` runs each ring step as one call over all shards (the
+    shards' queries as a batch of b*R rows, the K/V blocks they hold at that
+    step rotated into place, as a ring's send / receive would move them)
+    instead of one call per shard and step; the result is the same.
     """
     b, s, hq, d = q.shape
     dv = v.shape[3]  # the output takes V's head dim
@@ -70,6 +75,9 @@ def ring_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1,
     dev = q.device
     re = lambda x: reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
     qr, kr, vr, idr, posr = re(q), re(k), re(v), re(ids), re(pos)
+    if batch_shards:
+        return _ring_fwd_batched(qr, kr, vr, idr, posr, R, window_left, scale, strategy,
+                                 stripe_size, fused_merge, check_status, dv)
     out = torch.empty(b, s, hq, dv, dtype=q.dtype, device=dev)
     lse = torch.empty(b, hq, s, dtype=torch.float32, device=dev)
     acc = torch.empty(1, n, hq, dv, dtype=torch.float32, device=dev)
@@ -173,7 +181,7 @@ def allgather_attn_fwd(q, k, v, ids, pos, cp_size: int, *, window_left: int = -1
 def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_left: int = -1,
                   scale: Optional[float] = None, strategy: int = DUAL_CHUNK,
                   stripe_size: int = 1, check_status: bool = True,
-                  deterministic: bool = False):
+                  deterministic: bool = False, batch_shards: bool = False):
     """Backward of ring attention, emulated on one GPU.
 
     Shard r keeps its query rows, final output O_r, LSE_r and dO_r; at step t
@@ -189,7 +197,11 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
     Returns fp32 (dq [b,s,Hq,d], dk, dv [b,s,Hkv,d]) in natural order.
     ``check_status`` as in :func:`ring_attn_fwd`; ``deterministic`` as in
     :func:`attn_bwd` (the block calls then add fixed-order sums, so the
-    result is bit-identical from run to run).
+    result is bit-identical from run to run).  ``batch_shards`` runs each ring
+    step as one call over all shards, with the K/V blocks and their dK / dV
+    accumulators rotated one shard on between steps (a ring moves the dK / dV
+    partial sums along with the blocks); dK / dV are then summed over the
+    shards in another order, equal within fp32 rounding.
     """
     b, s, hq, d = q.shape
     hkv = k.shape[2]
@@ -201,6 +213,9 @@ def ring_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *, window_lef
     re = lambda x: reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
     qr, kr, vr, outr, dor = re(q), re(k), re(v), re(out), re(dout)
     idr, posr = re(ids), re(pos)
+    if batch_shards:
+        return _ring_bwd_batched(qr, kr, vr, outr, dor, idr, posr, lse, R, window_left, scale,
+                                 strategy, stripe_size, check_status, deterministic)
     dq = torch.zeros(b, s, hq, d, dtype=torch.float32, device=dev)
     dk = torch.zeros(b, s, hkv, d, dtype=torch.float32, device=dev)
     dv = torch.zeros(b, s, hkv, v.shape[3], dtype=torch.float32, device=dev)
@@ -288,3 +303,114 @@ def allgather_attn_bwd(q, k, v, out, lse, dout, ids, pos, cp_size: int, *,
         log.check("allgather_attn_bwd")
     inv = lambda x: inverse_reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
     return inv(dq), inv(dk), inv(dv)
+
+
+
+def _shard_lse(lse_rows, strategy, R, stripe_size, n):
+    """[Hq, s] LSE of one batch row in natural order -> [R, Hq, n] by shard."""
+    hq, s = lse_rows.shape
+    lse_r = reorder_causal_lb(lse_rows, strategy, R, stripe_size, seq_dim=1)
+    out = torch.empty(R, hq, n, dtype=torch.float32, device=lse_rows.device)
+    inverse_reorder_causal_lb(lse_r.view(1, hq * s), STRIPED, hq, n, seq_dim=1,
+                              out=out.view(1, R * hq * n))
+    return out
+
+
+def _natural_lse(lse_sh, strategy, R, stripe_size, out_row):
+    """[R, Hq, n] LSE of one batch row by shard -> its [Hq, s] in natural order."""
+    _, hq, n = lse_sh.shape
+    lse_t = reorder_causal_lb(lse_sh.reshape(1, R * hq * n), STRIPED, hq, n, seq_dim=1)
+    inverse_reorder_causal_lb(lse_t.view(hq, R * n), strategy, R, stripe_size, seq_dim=1,
+                              out=out_row)
+
+
+def _held_blocks(x, R, t):
+    """The block every shard holds at ring step t, as a batch of b*R shards:
+    shard r holds block (r - t) mod R of its batch row."""
+    b, s = x.shape[:2]
+    xs = x.reshape(b, R, s // R, *x.shape[2:])
+    if t:
+        xs = torch.roll(xs, shifts=t, dims=1)
+    return xs.reshape(b * R, s // R, *x.shape[2:])
+
+
+def _ring_fwd_batched(qr, kr, vr, idr, posr, R, window_left, scale, strategy, stripe_size,
+                      fused_merge, check_status, dv):
+    b, s, hq, d = qr.shape
+    n = s // R
+    B = b * R
+    dev = qr.device
+    qa, ida, pa = qr.view(B, n, hq, d), idr.view(B, n), posr.view(B, n)
+    out_r = torch.empty(b, s, hq, dv, dtype=qr.dtype, device=dev)
+    out_ra = out_r.view(B, n, hq, dv)
+    lse_a = torch.empty(B, hq, n, dtype=torch.float32, device=dev)
+    acc = torch.empty(B, n, hq, dv, dtype=torch.float32, device=dev)
+    blk = torch.empty_like(acc) if not fused_merge else None
+    blk_lse = torch.empty_like(lse_a) if not fused_merge else None
+    ws = torch.empty(workspace_bytes_fwd(qa, kr.view(B, n, *kr.shape[2:]), ida, pa,
+                                         window_left=window_left, v=vr.view(B, n, *vr.shape[2:])),
+                     dtype=torch.uint8, device=dev)
+    log = _StatusLog(R, dev) if check_status else None
+    for t in range(R):
+        kt, vt = _held_blocks(kr, R, t), _held_blocks(vr, R, t)
+        it, pt = _held_blocks(idr, R, t), _held_blocks(posr, R, t)
+        kw = dict(window_left=window_left, scale=scale, workspace=ws)
+        if R == 1:
+            attn_fwd(qa, kt, vt, ida, pa, it, pt, out=out_ra, lse=lse_a, **kw)
+        elif t == 0:
+            attn_fwd(qa, kt, vt, ida, pa, it, pt, out=acc, lse=lse_a, out_fp32=True, **kw)
+        elif fused_merge:
+            attn_fwd(qa, kt, vt, ida, pa, it, pt, out=acc, lse=lse_a, out_fp32=True,
+                     merge_into_out=True, out_final=out_ra if t == R - 1 else None, **kw)
+        else:
+            attn_fwd(qa, kt, vt, ida, pa, it, pt, out=blk, lse=blk_lse, out_fp32=True, **kw)
+            attn_merge_partial(acc, lse_a, blk, blk_lse, out_final=out_ra if t == R - 1 else None)
+        if log is not None:
+            log.record(ws)
+    lse = torch.empty(b, hq, s, dtype=torch.float32, device=dev)
+    for bi in range(b):
+        _natural_lse(lse_a[bi * R:(bi + 1) * R], strategy, R, stripe_size, lse[bi])
+    out = inverse_reorder_causal_lb(out_r, strategy, R, stripe_size, seq_dim=1)
+    if log is not None:
+        log.check("ring_attn_fwd")
+    return out, lse
+
+
+def _ring_bwd_batched(qr, kr, vr, outr, dor, idr, posr, lse, R, window_left, scale, strategy,
+                      stripe_size, check_status, deterministic):
+    b, s, hq, d = qr.shape
+    hkv, dv = kr.shape[2], vr.shape[3]
+    n = s // R
+    B = b * R
+    dev = qr.device
+    qa, outa, doa = qr.view(B, n, hq, d), outr.view(B, n, hq, dv), dor.view(B, n, hq, dv)
+    ida, pa = idr.view(B, n), posr.view(B, n)
+    lse_a = torch.empty(B, hq, n, dtype=torch.float32, device=dev)
+    for bi in range(b):
+        lse_a[bi * R:(bi + 1) * R] = _shard_lse(lse[bi], strategy, R, stripe_size, n)
+    dq = torch.zeros(b, s, hq, d, dtype=torch.float32, device=dev)
+    # the dK / dV partial sums travel with their blocks: position r holds the
+    # sums of block (r - t) mod R during step t
+    dk_held = torch.zeros(b, s, hkv, d, dtype=torch.float32, device=dev)
+    dv_held = torch.zeros(b, s, hkv, dv, dtype=torch.float32, device=dev)
+    ws = torch.empty(workspace_bytes_bwd(qa, kr.view(B, n, hkv, d), ida, pa, window_left,
+                                         v=vr.view(B, n, hkv, dv), deterministic=deterministic),
+                     dtype=torch.uint8, device=dev)
+    log = _StatusLog(R, dev) if check_status else None
+    for t in range(R):
+        kt, vt = _held_blocks(kr, R, t), _held_blocks(vr, R, t)
+        it, pt = _held_blocks(idr, R, t), _held_blocks(posr, R, t)
+        attn_bwd(qa, kt, vt, outa, lse_a, doa, ida, pa, it, pt, window_left=window_left,
+                 scale=scale, dq=dq.view(B, n, hq, d), dk=dk_held.view(B, n, hkv, d),
+                 dv=dv_held.view(B, n, hkv, dv), accumulate_fp32=True, workspace=ws,
+                 deterministic=deterministic)
+        if log is not None:
+            log.record(ws)
+        # pass the partial sums on with their blocks (after the last step every
+        # block's sums are back at its own position)
+        dk_held = _held_blocks(dk_held, R, 1).view(b, s, hkv, d)
+        dv_held = _held_blocks(dv_held, R, 1).view(b, s, hkv, dv)
+    if log is not None:
+        log.check("ring_attn_bwd")
+    inv = lambda x: inverse_reorder_causal_lb(x, strategy, R, stripe_size, seq_dim=1)
+    return inv(dq), inv(dk_held), inv(dv_held)

@@ -296,3 +296,42 @@ def test_allgather_backward_tutorial_shape(ring):
         check_grad(dv[bi, k0:k0 + nk, kvh].cpu(), rv[0, keys, 0], f"dv b{bi} kvh{kvh} k{k0}")
     del x, out, lse, dq, dk, dv
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,window,slots,R,strategy,stripe", [
+    (1, 2048, 4, 2, 128, -1, None, 4, RO.DUAL_CHUNK, 1),
+    (2, 1536, 4, 1, 64, 200, 2, 3, RO.DUAL_CHUNK, 1),
+    (1, 4096, 2, 1, 128, -1, 4, 4, RO.STRIPED, 128),
+])
+def test_ring_batched_shards(ring, b, s, hq, hkv, d, window, slots, R, strategy, stripe):
+    """batch_shards=True (one call per ring step over all shards, K/V blocks
+    and dK / dV sums rotated between steps): the forward equals the per-shard
+    form bit for bit (every block computes the same tiles and merges in the
+    same step order), the backward equals the oracle (its dK / dV sums over
+    the shards run in another order)."""
+    from tests.parity import check_grad
+    q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=R * 13 + s, with_dout=True)
+    ids, pos = workload.segments(b, s, slots)
+    g = [x.to(DEV) for x in (q, k, v, dout, ids, pos)]
+    kw = dict(window_left=window, scale=d ** -0.5, strategy=strategy, stripe_size=stripe)
+    for fused in (True, False):
+        o1, l1 = ring.ring_attn_fwd(g[0], g[1], g[2], g[4], g[5], R, fused_merge=fused, **kw)
+        o2, l2 = ring.ring_attn_fwd(g[0], g[1], g[2], g[4], g[5], R, fused_merge=fused,
+                                    batch_shards=True, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    dq, dk, dv = ring.ring_attn_bwd(g[0], g[1], g[2], o1, l1, g[3], g[4], g[5], R,
+                                    batch_shards=True, **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv = A.attn_bwd(q, k, v, dout, ids, pos, ids, pos, window, d ** -0.5)
+    check_grad(dq.cpu(), rq, "dq")
+    check_grad(dk.cpu(), rk, "dk")
+    check_grad(dv.cpu(), rv, "dv")
+    pad = (ids == 0).to(DEV)
+    assert torch.all(dq[pad] == 0) and torch.all(dk[pad] == 0) and torch.all(dv[pad] == 0)
+    # deterministic mode: fixed-order sums, two runs give the same bits
+    runs = [ring.ring_attn_bwd(g[0], g[1], g[2], o1, l1, g[3], g[4], g[5], R, batch_shards=True,
+                               deterministic=True, **kw) for _ in range(2)]
+    torch.cuda.synchronize()
+    for a_, b_ in zip(*runs):
+        assert torch.equal(a_, b_)
