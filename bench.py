@@ -372,6 +372,27 @@ def per_config(ga, dev, pk, big=None):
         res[name] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "fwd_tflops": ff / f_ms / 1e9,
                      "bwd_tflops": bf / b_ms / 1e9, "step_tflops": (ff + bf) / (f_ms + b_ms) / 1e9,
                      "valid_pairs_per_head": pairs}
+        if name != "ring_cp4":
+            # the same fwd + bwd step captured once in a CUDA graph and replayed:
+            # the small workloads are bound by their ~20 launches per step
+            def both():
+                fwd()
+                bwd()
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                both()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                both()
+            g_ms = _timed_calls(graph.replay)
+            if ga.read_device_status(ws) != 0:
+                raise RuntimeError(f"{name} (graph): device status {ga.read_device_status(ws)}")
+            res[name]["step_graph_ms"] = g_ms
+            res[name]["step_graph_tflops"] = (ff + bf) / g_ms / 1e9
+            del graph
         if name == "ring_cp4":
             R = w.cp_size
             kw = dict(window_left=w.window_left, scale=w.scale, check_status=False)

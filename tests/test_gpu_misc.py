@@ -258,3 +258,49 @@ def test_bwd_kernel_events_bracket_the_main_kernel(ga, det):
     assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
     if det:
         assert torch.equal(got[0], ref[0])
+
+
+@pytest.mark.parametrize("name", ["tiny", "packed_thd"])
+def test_fwd_bwd_replay_from_cuda_graph(ga, name):
+    """A whole fwd + bwd step captured once in a CUDA graph (every call only
+    enqueues work on the stream; the tensor maps are kernel arguments by
+    value) and replayed on new inputs written in place gives what eager calls
+    give on those inputs: forward bit for bit, dK / dV bit for bit, dQ bit for
+    bit in the deterministic mode."""
+    w = workload.WORKLOADS[name]
+    x = workload.make(w, device=DEV, with_dout=True)
+    q, k, v, ids, pos, dout = x["q"], x["k"], x["v"], x["ids"], x["pos"], x["dout"]
+    kw = dict(window_left=w.window_left, scale=w.scale)
+    wsf = torch.empty(ga.workspace_bytes_fwd(q, k, ids, pos, **kw, v=v), dtype=torch.uint8,
+                      device=DEV)
+    wsb = torch.empty(ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left, v=v,
+                                             deterministic=True), dtype=torch.uint8, device=DEV)
+    out, lse = torch.empty_like(q), torch.empty(w.b, w.hq, w.s, dtype=torch.float32, device=DEV)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def step():
+        ga.attn_fwd(q, k, v, ids, pos, out=out, lse=lse, workspace=wsf, **kw)
+        ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, dq=dq, dk=dk, dv=dv, workspace=wsb,
+                    deterministic=True, **kw)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture (kernel attributes set once)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    y = workload.make(w, device=DEV, with_dout=True, seed=workload.SEED + 7)
+    for name_, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        t.copy_(y[name_])
+    g.replay()
+    torch.cuda.synchronize()
+    got = [t.clone() for t in (out, lse, dq, dk, dv)]
+    assert ga.read_device_status(wsf) == 0 and ga.read_device_status(wsb) == 0
+    ro, rl = ga.attn_fwd(q, k, v, ids, pos, **kw)
+    rq, rk, rv = ga.attn_bwd(q, k, v, ro, rl, dout, ids, pos, deterministic=True, **kw)
+    torch.cuda.synchronize()
+    for a_, b_ in zip(got, (ro, rl, rq, rk, rv)):
+        assert torch.equal(a_, b_)
