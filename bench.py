@@ -576,27 +576,31 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = max_over_ranks(total_ms / args.steps, dist, dev)
     value = whole_job_tflops(world, fwd_flop + bwd_flop, ms_per_step)
 
-    # end to end through the public API: pinned host inputs in, gradients out.
-    # Every step copies its inputs host -> device and its gradients device ->
-    # host inside the timed region; as in a training loop with prefetch, the
-    # copies run on a copy stream of their own into double-buffered device
-    # tensors, so step i+1's inputs and step i-1's gradients move while step i
-    # computes.  One copy stream for both directions, one copy at a time: on
+    # End to end through the public API, every step: the step's inputs copied
+    # host -> device from pinned memory and the step's result read back.  The
+    # result is the loss vdot(out, dout) whose gradient the step computes (the
+    # sum of the D vector attn_bwd returns in `delta`; the gradients stay on
+    # the device, as an optimizer would use them there): `e2e`.  With every
+    # gradient copied back to the host instead: `e2e_grads_out`.  As in a
+    # training loop with prefetch, the copies run on a copy stream of their own
+    # into double-buffered device tensors, so step i+1's inputs (and step
+    # i-1's results) move while step i computes; one copy at a time, since on
     # some of these boxes the link moves far less with both directions at once
     # than with either alone (host_link.both_gbs).
-    e2e = None
+    e2e = e2e_grads = None
     if not args.no_e2e and not fwd_only:
         h_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v),
                                                          ("dout", dout), ("ids", ids),
                                                          ("pos", pos))}
         h_out = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                   for n, t in (("dq", dq), ("dk", dk), ("dv", dv))} for _ in range(2)]
+        h_loss = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(2)]
         d_in = [{n: torch.empty_like(t, device=dev) for n, t in h_in.items()} for _ in range(2)]
         d_out = [(dq, dk, dv), (torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv))]
+        delta = [torch.empty(w.b, w.hq, w.s, dtype=torch.float32, device=dev) for _ in range(2)]
+        loss = [torch.empty(1, dtype=torch.float32, device=dev) for _ in range(2)]
         bi = sum(t.numel() * t.element_size() for t in h_in.values())
-        bo = sum(t.numel() * t.element_size() for t in h_out[0].values())
         s_copy = torch.cuda.Stream(device=dev)
-        s_h2d = s_d2h = s_copy
         ev = lambda: torch.cuda.Event()
         h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         fwd_in_done = [ev(), ev()]  # q, k, v, ids, pos of the set have landed (dout may not)
@@ -605,19 +609,19 @@ def run_ours(args, rank, world, local_rank):
 
         def h2d(i):
             sl = i % 2
-            s_h2d.wait_event(comp_done[sl])  # step i-2 no longer reads this input set
-            with torch.cuda.stream(s_h2d):
+            s_copy.wait_event(comp_done[sl])  # step i-2 no longer reads this input set
+            with torch.cuda.stream(s_copy):
                 # the forward's inputs first; dout (read by the backward only) last
                 for n in ("q", "k", "v", "ids", "pos", "dout"):
                     d_in[sl][n].copy_(h_in[n], non_blocking=True)
                     if n == "pos":
-                        fwd_in_done[sl].record(s_h2d)
-            h2d_done[sl].record(s_h2d)
+                        fwd_in_done[sl].record(s_copy)
+            h2d_done[sl].record(s_copy)
 
-        def compute(i):
+        def compute(i, grads_out):
             sl = i % 2
             stream.wait_event(fwd_in_done[sl])
-            stream.wait_event(d2h_done[sl])  # step i-2's gradients have left this set
+            stream.wait_event(d2h_done[sl])  # step i-2's results have left this set
             x_ = d_in[sl]
             gq, gk, gv = d_out[sl]
             ga.attn_fwd(x_["q"], x_["k"], x_["v"], x_["ids"], x_["pos"],
@@ -625,58 +629,76 @@ def run_ours(args, rank, world, local_rank):
             stream.wait_event(h2d_done[sl])  # dout, for the backward
             ga.attn_bwd(x_["q"], x_["k"], x_["v"], out, lse, x_["dout"], x_["ids"], x_["pos"],
                         window_left=w.window_left, scale=w.scale, dq=gq, dk=gk, dv=gv,
-                        workspace=ws, deterministic=args.deterministic)
+                        workspace=ws, deterministic=args.deterministic,
+                        delta=None if grads_out else delta[sl])
+            if not grads_out:
+                torch.sum(delta[sl].view(-1), 0, keepdim=True, out=loss[sl])
             comp_done[sl].record(stream)
 
-        def d2h(i):
+        def d2h(i, grads_out):
             sl = i % 2
-            s_d2h.wait_event(comp_done[sl])
-            with torch.cuda.stream(s_d2h):
-                for n, t in zip(("dq", "dk", "dv"), d_out[sl]):
-                    h_out[sl][n].copy_(t, non_blocking=True)
-            d2h_done[sl].record(s_d2h)
+            s_copy.wait_event(comp_done[sl])
+            with torch.cuda.stream(s_copy):
+                if grads_out:
+                    for n, t in zip(("dq", "dk", "dv"), d_out[sl]):
+                        h_out[sl][n].copy_(t, non_blocking=True)
+                else:
+                    h_loss[sl].copy_(loss[sl], non_blocking=True)
+            d2h_done[sl].record(s_copy)
 
-        def run(nsteps):
+        def run(nsteps, grads_out):
             h2d(0)
             for i in range(nsteps):
                 if i + 1 < nsteps:
                     h2d(i + 1)
-                compute(i)
-                d2h(i)
+                compute(i, grads_out)
+                d2h(i, grads_out)
 
-        run(2)
-        torch.cuda.synchronize()
-        # the same K steps as the device-timed value; the first copy-in and
-        # the last copy-out are not hidden behind a neighbouring step
-        # three passes of the K steps, the median reported: the host link is
-        # shared with other tenants on these boxes and can stall one pass
-        n_e2e = max(2, args.steps)
-        passes = []
-        for _ in range(3):
-            if dist:
-                dist.barrier()
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(s_h2d)
-            run(n_e2e)
-            s_d2h.wait_stream(stream)
-            b_.record(s_d2h)
+        def measure(grads_out):
+            run(2, grads_out)
             torch.cuda.synchronize()
-            passes.append(max_over_ranks(a.elapsed_time(b_) / n_e2e, dist, dev))
-        e2e_ms = median(passes)
-        link = host_link(h_in["q"], d_in[0]["q"], h_out[0]["dq"], s_h2d)
-        e2e = {"value": whole_job_tflops(world, fwd_flop + bwd_flop, e2e_ms),
-               "unit": "TFLOP/s", "ms_per_step": e2e_ms, "passes_ms_per_step": passes,
-               "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo,
-               "copies": "every step's inputs in and gradients out inside the timed region, "
-                         "on one copy stream (one direction at a time) overlapping the "
-                         "neighbouring steps' compute (double-buffered device tensors); a "
-                         "step's forward starts once its own inputs have landed, its dout "
-                         "copy overlapping it; the median of three passes of the K steps",
-               "host_link": link,
-               # the copies alone, one after the other at the one-way rates
-               "copy_bound_ms": 1e3 * (bi / (link["h2d_gbs"] * 1e9) + bo / (link["d2h_gbs"] * 1e9))}
-        del h_in, h_out, d_in, d_out
+            # the same K steps as the device-timed value (the first copy-in and
+            # the last copy-out are not hidden behind a neighbouring step), three
+            # passes, the median reported: the host link is shared with other
+            # tenants on these boxes and can stall one pass
+            n_e2e = max(2, args.steps)
+            passes = []
+            for _ in range(3):
+                if dist:
+                    dist.barrier()
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s_copy)
+                run(n_e2e, grads_out)
+                s_copy.wait_stream(stream)
+                b_.record(s_copy)
+                torch.cuda.synchronize()
+                passes.append(max_over_ranks(a.elapsed_time(b_) / n_e2e, dist, dev))
+            return median(passes), passes
+
+        link = host_link(h_in["q"], d_in[0]["q"], h_out[0]["dq"], s_copy)
+        for grads_out in (False, True):
+            e2e_ms, passes = measure(grads_out)
+            bo = (sum(t.numel() * t.element_size() for t in h_out[0].values()) if grads_out
+                  else h_loss[0].numel() * h_loss[0].element_size())
+            rec = {"value": whole_job_tflops(world, fwd_flop + bwd_flop, e2e_ms),
+                   "unit": "TFLOP/s", "ms_per_step": e2e_ms, "passes_ms_per_step": passes,
+                   "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                   "result": ("dq, dk, dv (bf16)" if grads_out else
+                              "the loss vdot(out, dout) = sum of attn_bwd's delta (fp32)"),
+                   "copies": "every step's inputs in and its result out inside the timed "
+                             "region, on one copy stream (one direction at a time) overlapping "
+                             "the neighbouring steps' compute (double-buffered device tensors); "
+                             "a step's forward starts once its own inputs have landed, its dout "
+                             "copy overlapping it; the median of three passes of the K steps",
+                   "host_link": link,
+                   # the copies alone, one after the other at the one-way rates
+                   "copy_bound_ms": 1e3 * (bi / (link["h2d_gbs"] * 1e9)
+                                           + bo / (link["d2h_gbs"] * 1e9))}
+            if grads_out:
+                e2e_grads = rec
+            else:
+                e2e = rec
+        del h_in, h_out, d_in, d_out, delta
 
     if dist:
         dist.destroy_process_group()
@@ -750,6 +772,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read+write)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "e2e_grads_out": e2e_grads,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }

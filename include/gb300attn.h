@@ -162,6 +162,12 @@ typedef struct attn_fwd_params {
  *                   the pair), so that their elapsed time is the main kernels'
  *                   alone, without the tile plan, the D pre-pass and the dQ
  *                   finalise.  Setting only one of them is ATTN_ERR_INVALID_ARG.
+ *  delta            optional output (NULL: none): fp32 [b, h_q, s_q], 4-byte
+ *                   aligned, D = rowsum(dO * O) of every query row and head,
+ *                   as the backward uses it (its workspace copy otherwise).
+ *                   Its sum is vdot(out, dout), the loss whose gradient this
+ *                   call computes (TE tutorial section 5 differentiates that
+ *                   vdot).  Must not overlap the other buffers.
  */
 typedef struct attn_bwd_params {
   attn_fwd_params fwd;
@@ -172,6 +178,7 @@ typedef struct attn_bwd_params {
   int32_t accumulate_fp32;
   int32_t deterministic;
   void* kernel_events[2];
+  float* delta;
 } attn_bwd_params;
 
 /* Scratch sizes (bytes) for the given problem; 0 on invalid sizes. */

@@ -57,6 +57,7 @@ class BwdParams(ctypes.Structure):
         ("fwd", FwdParams), ("dout", ctypes.c_void_p), ("dq", ctypes.c_void_p),
         ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p), ("accumulate_fp32", ctypes.c_int32),
         ("deterministic", ctypes.c_int32), ("kernel_events", ctypes.c_void_p * 2),
+        ("delta", ctypes.c_void_p),
     ]
 
 
@@ -262,7 +263,8 @@ def _attn_fwd_call(entry, q, k, v, q_ids, q_pos, kv_ids, kv_pos, window_left, sc
 def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
              window_left: int = -1, scale: Optional[float] = None, dq=None, dk=None, dv=None,
              accumulate_fp32: bool = False, workspace: Optional[torch.Tensor] = None,
-             check_status: bool = False, deterministic: bool = False, kernel_events=None):
+             check_status: bool = False, deterministic: bool = False, kernel_events=None,
+             delta=None):
     """Backward attention.  Returns (dq, dk, dv): bf16, or with
     ``accumulate_fp32`` the given fp32 tensors with this call's gradients added.
     ``deterministic`` takes the dK / dV + dQ kernel pair, whose results are
@@ -270,7 +272,10 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     reduce-adds in hardware order); head dims 256 and (192, 128) always take it.
     ``kernel_events`` (two timing ``torch.cuda.Event``) are recorded just
     before and after the main kernel(s), without the plan, the D pre-pass and
-    the dQ finalise.  ``check_status`` as in :func:`attn_fwd`."""
+    the dQ finalise.  ``delta`` (fp32 [b, Hq, s_q], optional) receives
+    D = rowsum(dO * O) of every query row and head; its sum is vdot(out,
+    dout), the loss whose gradient this call computes.  ``check_status`` as in
+    :func:`attn_fwd`."""
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
     _need_cuda(q, out, lse, dout, q_ids, q_pos, kv_ids, kv_pos, workspace, dq)
@@ -308,6 +313,11 @@ def attn_bwd(q, k, v, out, lse, dout, q_ids, q_pos, kv_ids=None, kv_pos=None, *,
     p.dout, p.dq, p.dk, p.dv = dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
     p.accumulate_fp32 = 1 if accumulate_fp32 else 0
     p.deterministic = 1 if deterministic else 0
+    if delta is not None:
+        _need_cuda(delta)
+        if delta.dtype != torch.float32 or delta.shape != (q.shape[0], q.shape[2], q.shape[1]):
+            raise ValueError("delta must be a contiguous fp32 [b, Hq, s_q] tensor")
+        p.delta = delta.data_ptr()
     if kernel_events is not None:
         for i, ev in enumerate(kernel_events):
             if not ev.cuda_event:  # a torch event exists once it has been recorded

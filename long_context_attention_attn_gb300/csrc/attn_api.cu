@@ -246,6 +246,31 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   if (p->deterministic != 0 && p->deterministic != 1) return ATTN_ERR_INVALID_ARG;
   if ((p->kernel_events[0] == nullptr) != (p->kernel_events[1] == nullptr))
     return ATTN_ERR_INVALID_ARG;
+  if (p->delta) {
+    // the optional D output: aligned, and clear of every other buffer
+    if (!aligned(p->delta, 4)) return ATTN_ERR_INVALID_ARG;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(p->delta);
+    const uintptr_t dn = (uintptr_t)(f->b * f->h_q * f->s_q) * 4;
+    const uintptr_t rows = (uintptr_t)(f->b * f->s_q * f->h_q);
+    const uintptr_t gsz = p->accumulate_fp32 ? 4 : 2;
+    const uintptr_t toks = (uintptr_t)(f->b * f->s_kv);
+    const uintptr_t kst = f->kv_token_stride > 0 ? (uintptr_t)f->kv_token_stride
+                                                 : (uintptr_t)(f->h_kv * f->d);
+    const uintptr_t vst = f->kv_token_stride > 0 ? (uintptr_t)f->kv_token_stride
+                                                 : (uintptr_t)(f->h_kv * dv);
+    const struct { const void* a; uintptr_t n; } others[] = {
+        {f->workspace, (uintptr_t)f->workspace_bytes},
+        {f->out, rows * (uintptr_t)dv * 2},
+        {p->dout, rows * (uintptr_t)dv * 2},
+        {f->lse, dn},
+        {p->dq, rows * (uintptr_t)f->d * gsz},
+        {p->dk, toks * kst * gsz},
+        {p->dv, toks * vst * gsz}};
+    for (const auto& o : others) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(o.a);
+      if (a0 < d0 + dn && d0 < a0 + o.n) return ATTN_ERR_INVALID_ARG;
+    }
+  }
   // optional timing hook around the main kernel(s)
   auto mark = [&](int i) -> cudaError_t {
     return p->kernel_events[i]
@@ -258,7 +283,7 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
     sl.plan = plan_ptrs(f->workspace, L);
     sl.nq = cdiv(f->s_q, kTile);
     sl.nk = cdiv(f->s_kv, kTile);
-    sl.D = reinterpret_cast<float*>(static_cast<char*>(f->workspace) + L.end);
+    sl.D = p->delta ? p->delta : reinterpret_cast<float*>(static_cast<char*>(f->workspace) + L.end);
     const int bm = split_bwd_query_rows(f->d, dv), bn = split_bwd_key_rows(f->d, dv);
     if (!encode_qkv_map(&sl.tm_q, f->q, f->b, f->s_q, f->h_q, f->d, 0) ||
         !encode_qkv_map(&sl.tm_do, p->dout, f->b, f->s_q, f->h_q, dv, 0) ||
@@ -286,7 +311,7 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
   bl.nq = cdiv(f->s_q, kTile);
   bl.nk = cdiv(f->s_kv, kTile);
   char* ws = static_cast<char*>(f->workspace);
-  bl.D = reinterpret_cast<float*>(ws + L.end);
+  bl.D = p->delta ? p->delta : reinterpret_cast<float*>(ws + L.end);
   const bool acc = p->accumulate_fp32 != 0;
   // accumulate mode: the dQ reduce-adds go straight into the caller's fp32 dq
   bl.dq_acc = acc ? static_cast<float*>(p->dq)

@@ -120,6 +120,11 @@ def test_bwd_rejects_invalid_arguments_on_host(ga):
     bp.kernel_events[0] = 1 << 12  # timing events come in pairs (never recorded here)
     assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
     bp.kernel_events[0] = None
+    bp.delta = (1 << 40) + 2  # the optional D output: 4-byte aligned
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
+    bp.delta = bp.fwd.workspace  # ... and clear of the other buffers
+    assert ga.lib().attn_bwd(ctypes.byref(bp), None) == 1
+    bp.delta = None
     # d = 256 and the MLA shape (192, 128) are taken (by the dK / dV + dQ kernel
     # pair); only the size query runs here, nothing is launched on the fake
     # pointers.  Their workspace holds no fp32 dQ accumulator.

@@ -255,3 +255,27 @@ def test_full_swa_64k_whole_slot_of_one_group(ga):
     pad = ids[0] == 0
     assert torch.all(got["out"][0, pad] == 0) and torch.all(got["dq"][0, pad] == 0)
     assert torch.all(got["dk"][0, pad] == 0) and torch.all(got["dv"][0, pad] == 0)
+
+
+@pytest.mark.parametrize("det", [False, True])
+def test_delta_output_is_rowsum_of_dout_times_out(det):
+    """attn_bwd's optional D output: rowsum(dO * O) of every query row and
+    head (fp64 reference from the same bf16 tensors), summing to vdot(out,
+    dout); passing it changes no gradient."""
+    import long_context_attention_attn_gb300 as ga
+    w = workload.WORKLOADS["packed_swa"]
+    x = workload.make(w, device=DEV, with_dout=True)
+    q, k, v, ids, pos, dout = x["q"], x["k"], x["v"], x["ids"], x["pos"], x["dout"]
+    kw = dict(window_left=w.window_left, scale=w.scale, deterministic=det)
+    out, lse = ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale)
+    ref = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, **kw)
+    delta = torch.full((w.b, w.hq, w.s), float("nan"), dtype=torch.float32, device=DEV)
+    got = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, delta=delta, check_status=True, **kw)
+    torch.cuda.synchronize()
+    want = (dout.double() * out.double()).sum(-1).permute(0, 2, 1)  # [b, Hq, s]
+    assert torch.allclose(delta.double(), want, rtol=1e-5, atol=1e-5)
+    loss = (dout.double() * out.double()).sum()
+    assert abs(delta.double().sum().item() - loss.item()) <= 1e-6 * max(1.0, abs(loss.item())) + 1e-2
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+    if det:
+        assert torch.equal(got[0], ref[0])
