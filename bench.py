@@ -13,6 +13,15 @@ Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
 instance of the workload (weak scaling, no data-path collective); the step
 time is the maximum over ranks.  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload (rank 0 only).
+
+The JSON line also carries: `roofline` for the backward kernel alone (timed
+between CUDA events attn_bwd records around its launch; `roofline.call` has
+the whole call), `e2e` (every step's inputs copied in from pinned host memory
+and its loss vdot(out, dout) read back) and `e2e_grads_out` (dq, dk, dv copied
+back instead), `cpu_baseline` (the oracle on the host cores), `clocks`
+(nvidia-smi during the timed region) and `components.per_config` (every
+workload of the pages' set, the ring and all-gather emulations, the
+deterministic backward, CUDA-graph replays of the small steps).
 """
 from __future__ import annotations
 
