@@ -120,7 +120,8 @@ def peaks():
 def bwd_traffic():
     """DRAM bytes per launch of the fused backward kernel on the benchmark
     workload, from the committed ncu summary, or None once the kernel sources
-    differ from the ones that summary was taken with."""
+    (the kernel itself and the plan that orders its work) differ from the
+    ones that summary was taken with."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "attn_bwd_dram_full_swa_64k.md")
     if not os.path.exists(path):
@@ -134,7 +135,7 @@ def bwd_traffic():
             vals[k.strip()] = v.strip()
     csrc = os.path.join(ROOT, "long_context_attention_attn_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("attn_bwd.cu", "ptx.cuh", "internal.h"):
+    for f in ("attn_bwd.cu", "kernels_misc.cu", "ptx.cuh", "internal.h"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     if vals.get("source_sha256") != h.hexdigest():

@@ -267,13 +267,23 @@ GB300ATTN_API int attn_segments_from_seqlens(const int32_t* seqlens, const int32
 GB300ATTN_API int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,
                    attn_stream_t stream);
 
-/* Debug hook: the order in which the kernels take their work units, heaviest
- * first (the units with the most non-SKIP tiles of the other side), equal
- * weights in index order (a stable sort).
- *  q_order   int32 [b * ceil(s_q/128)]:  (b, query tile) indices b * nq + tile
- *            (forward and dQ kernels)
- *  kv_order  int32 [b * ceil(s_kv/128)]: (b, key tile) indices b * nk + tile
- *            (dK / dV and fused backward kernels)
+/* Debug hook: the order in which the kernels take their work units.  Each
+ * side's order is one of two, chosen per call from the plan's weights (a
+ * unit's weight: its non-SKIP tiles of the other side):
+ *  - index order, descending on the query side and ascending on the key
+ *    side (heavy first within each causal segment; neighbouring tiles run
+ *    together and share their inputs through L2), taken when the heaviest
+ *    unit's CTA is at most 1/20 of an SM's share of the launch:
+ *    w_max * SMs * 20 <= (sum of w) * (CTAs per unit);
+ *  - otherwise heaviest first over all units, equal weights in index order
+ *    (a stable sort).
+ *  q_order   int32 [b * ceil(s_q/128)]:  (b, query tile) indices b * nq + tile,
+ *            as the forward takes them (CTAs per unit: h_kv * ceil(g / 2),
+ *            g = h_q / h_kv, or h_q when d_v = 256)
+ *  kv_order  int32 [b * ceil(s_kv/128)]: (b, key tile) indices b * nk + tile,
+ *            as the fused backward takes them (CTAs per unit: h_kv)
+ * (The dQ kernel of the deterministic backward decides with h_q CTAs per
+ * unit, its dK / dV kernel with h_kv, or 2 * h_kv at d = 256.)
  * Uses p->workspace like attn_fwd.  Not part of any computation's result:
  * the order only decides which CTAs run first. */
 GB300ATTN_API int attn_tile_order(const attn_fwd_params* p, int32_t* q_order, int32_t* kv_order,

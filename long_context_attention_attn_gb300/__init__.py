@@ -435,7 +435,9 @@ def attn_tile_plan(q, k, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left:
 def attn_tile_order(q, k, q_ids, q_pos, kv_ids=None, kv_pos=None, *, window_left: int = -1,
                     workspace=None):
     """The kernels' work order (debug hook): (q_order int32 [b*nq], kv_order
-    int32 [b*nk]), each a stable heaviest-first permutation of the units."""
+    int32 [b*nk]) as the forward and the fused backward take their units:
+    index order (descending on the query side) when the heaviest unit is a
+    small share of the launch, else a stable heaviest-first permutation."""
     kv_ids = q_ids if kv_ids is None else kv_ids
     kv_pos = q_pos if kv_pos is None else kv_pos
     _need_cuda(q, k, q_ids, q_pos, kv_ids, kv_pos)

@@ -150,7 +150,8 @@ static int fwd_impl(const attn_fwd_params* p, attn_stream_t stream, bool withhol
                       kFwdKeyTile))
     return ATTN_ERR_CUDA;
   cudaError_t e = cudaMemsetAsync(fl.plan.status, 0, sizeof(int), st);
-  if (e == cudaSuccess) e = launch_tile_plan(*p, fl.plan, fl.nq, fl.nk, false, st);
+  if (e == cudaSuccess)
+    e = launch_tile_plan(*p, fl.plan, fl.nq, fl.nk, false, fwd_ctas_per_tile(*p), 0, st);
   if (e == cudaSuccess) e = launch_attn_fwd(fl, st);
   return cuda_status(e);
 }
@@ -174,7 +175,7 @@ int attn_tile_plan(const attn_fwd_params* p, uint8_t* classes, int32_t* ranges,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t nq = cdiv(p->s_q, kTile), nk = cdiv(p->s_kv, kTile);
   const PlanPtrs pp = plan_ptrs(p->workspace, L);
-  cudaError_t e = launch_tile_plan(*p, pp, nq, nk, false, st);
+  cudaError_t e = launch_tile_plan(*p, pp, nq, nk, false, fwd_ctas_per_tile(*p), 0, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(classes, pp.classes, (size_t)(p->b * nq * nk), cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess)
@@ -205,7 +206,8 @@ int attn_tile_order(const attn_fwd_params* p, int32_t* q_order, int32_t* kv_orde
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t nq = cdiv(p->s_q, kTile), nk = cdiv(p->s_kv, kTile);
   const PlanPtrs pp = plan_ptrs(p->workspace, L);
-  cudaError_t e = launch_tile_plan(*p, pp, nq, nk, true, st);
+  // the orders the forward (query side) and the fused backward (key side) take
+  cudaError_t e = launch_tile_plan(*p, pp, nq, nk, true, fwd_ctas_per_tile(*p), p->h_kv, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(q_order, pp.q_order, (size_t)(p->b * nq) * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess)
@@ -295,7 +297,11 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
         !encode_qkv_map(&sl.tm_vb, f->v, f->b, f->s_kv, f->h_kv, dv, f->kv_token_stride, bn))
       return ATTN_ERR_CUDA;
     cudaError_t e = cudaMemsetAsync(sl.plan.status, 0, sizeof(int), st);
-    if (e == cudaSuccess) e = launch_tile_plan(*f, sl.plan, sl.nq, sl.nk, true, st);
+    // dQ kernel: one CTA per query tile and head; dK / dV kernel: one per key
+    // tile, kv head and column slice
+    if (e == cudaSuccess)
+      e = launch_tile_plan(*f, sl.plan, sl.nq, sl.nk, true, f->h_q,
+                           f->h_kv * split_bwd_col_slices(f->d, dv), st);
     if (e == cudaSuccess)
       e = launch_bwd_preprocess(f->out, p->dout, sl.D, nullptr, f->b, f->s_q, f->h_q, dv, st);
     if (e == cudaSuccess) e = mark(0);
@@ -325,7 +331,8 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
     return ATTN_ERR_CUDA;
   const size_t n_dq = (size_t)(f->b * f->s_q * f->h_q * f->d);
   cudaError_t e = cudaMemsetAsync(bl.plan.status, 0, sizeof(int), st);
-  if (e == cudaSuccess) e = launch_tile_plan(*f, bl.plan, bl.nq, bl.nk, true, st);
+  if (e == cudaSuccess)
+    e = launch_tile_plan(*f, bl.plan, bl.nq, bl.nk, true, f->h_q, f->h_kv, st);
   // the D pre-pass also zeroes the workspace's fp32 dQ accumulator (not the
   // caller's accumulator in accumulate mode)
   if (e == cudaSuccess)

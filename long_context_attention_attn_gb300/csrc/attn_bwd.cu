@@ -141,9 +141,10 @@ struct BBars {
 static_assert(sizeof(BBars) <= 256, "barrier block too large");
 
 // Iterates over the steps (head, query tile) of a CTA: heads outer, query
-// tiles inner.  CTAs of neighbouring key tiles of one kv head run at the same
-// time and walk the same head in step, so a dQ tile receives its reduce-adds
-// from them on consecutive steps while it is still in L2.
+// tiles inner.  In the plan's index order, CTAs of neighbouring key tiles of
+// one kv head run at the same time and walk the same head in step, so a dQ
+// tile receives its reduce-adds from them on consecutive steps while it is
+// still in L2.
 struct StepIter {
   int i, hh, i_first, i_end, g;
   const uint8_t* cls_col;  // cls + b*nq*nk + c, stride nk
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   if (a.status && *reinterpret_cast<volatile int*>(a.status) != kStatusOk) return;
 
-  // ---- work unit: kv head slowest, then (b, kv tile) heavy first (stable)
+  // ---- work unit: kv head slowest, then (b, kv tile) in the plan's work order
   const int nunits = a.b * a.nk;
   const int kvh = blockIdx.x / nunits;
   const int rank = blockIdx.x % nunits;

@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   if (a.status && *reinterpret_cast<volatile int*>(a.status) != kStatusOk) return;
 
-  // ---- work unit: kv head slowest, then (b, kv tile) heavy first, then slice
+  // ---- work unit: kv head slowest, then (b, kv tile) in work order, then slice
   const int nunits = a.b * a.nk;
   const int kvh = blockIdx.x / (nunits * NSPLIT);
   const int rem = blockIdx.x % (nunits * NSPLIT);
@@ -1159,6 +1159,8 @@ int split_bwd_query_rows(int64_t d, int64_t dv) {
 int split_bwd_key_rows(int64_t d, int64_t dv) {
   return (d == 256 || (d == 192 && dv == 128)) ? 64 : 128;
 }
+
+int split_bwd_col_slices(int64_t d, int64_t dv) { return (d == 256 && dv == 256) ? 2 : 1; }
 
 cudaError_t launch_attn_bwd_split(const SplitLaunch& Lc, cudaStream_t st) {
   const attn_bwd_params& p = *Lc.p;

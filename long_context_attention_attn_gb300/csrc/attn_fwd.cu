@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // A CTA of this launch already timed out: the outputs are undefined, stop.
   if (a.status && *reinterpret_cast<volatile int*>(a.status) != kStatusOk) return;
 
-  // ---- work unit: (b, q tile) heavy first, then kv head, then head pair
+  // ---- work unit: (b, q tile) in the plan's work order, then kv head, then head pair
   const int per_tile = a.hkv * a.npairs;
   const int rank = blockIdx.x / per_tile;
   const int rem = blockIdx.x % per_tile;
@@ -650,6 +650,13 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const FwdLaunch& Lc, int64_t units, c
 
 }  // namespace
 
+int64_t fwd_ctas_per_tile(const attn_fwd_params& p) {
+  const int64_t dv = p.d_v > 0 ? p.d_v : p.d;
+  const int64_t slots = dv <= 128 ? 2 : 1;  // query heads per CTA (kSlots)
+  const int64_t g = p.h_q / p.h_kv;
+  return p.h_kv * ((g + slots - 1) / slots);
+}
+
 cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   const attn_fwd_params& p = *Lc.p;
   FwdArgs a;
@@ -673,8 +680,7 @@ cudaError_t launch_attn_fwd(const FwdLaunch& Lc, cudaStream_t st) {
   a.hkv = (int)p.h_kv;
   a.g = (int)(p.h_q / p.h_kv);
   const int64_t dv = p.d_v > 0 ? p.d_v : p.d;
-  const int slots = dv <= 128 ? 2 : 1;  // query heads per CTA
-  a.npairs = (a.g + slots - 1) / slots;
+  a.npairs = (int)(fwd_ctas_per_tile(p) / p.h_kv);
   a.nq = (int)Lc.nq;
   a.nk = (int)Lc.nk;
   a.window = p.window_left;

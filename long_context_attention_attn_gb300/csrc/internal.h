@@ -64,12 +64,12 @@ struct PlanLayout {
   size_t kv_range;    // int2 [b, nk]  first/last non-SKIP q tile
   size_t q_weight;    // int  [b, nq]  number of non-SKIP kv tiles
   size_t kv_weight;   // int  [b, nk]  number of non-SKIP q tiles
-  size_t q_order;     // int  [b, nq]  (b, q tile) heavy first
-  size_t kv_order;    // int  [b, nk]  (b, kv tile) heavy first
+  size_t q_order;     // int  [b, nq]  (b, q tile) work order
+  size_t kv_order;    // int  [b, nk]  (b, kv tile) work order
   size_t classes;     // uint8 [b, nq, nk]
   size_t sort_hist;   // int [chunks, buckets]  heavy-first sort: per-chunk weight counts
   size_t sort_rank;   // int [max(b*nq, b*nk)]   rank among equal weights in the chunk
-  size_t sort_start;  // int [buckets]           first position of each weight
+  size_t sort_start;  // int [buckets + 1]       first position of each weight; the order chosen
   int64_t sort_buckets;  // max(nq, nk) + 1: weights are tile counts of the other side
   size_t end;
 };
@@ -94,7 +94,7 @@ inline PlanLayout plan_layout(int64_t b, int64_t nq, int64_t nk, size_t base = 0
   const int64_t chunks = (nmax + kSortChunk - 1) / kSortChunk;
   L.sort_hist = o;  o = align_up(o + (size_t)(chunks * L.sort_buckets) * 4, 256);
   L.sort_rank = o;  o = align_up(o + (size_t)nmax * 4, 256);
-  L.sort_start = o; o = align_up(o + (size_t)L.sort_buckets * 4, 256);
+  L.sort_start = o; o = align_up(o + (size_t)(L.sort_buckets + 1) * 4, 256);
   L.end = o;
   return L;
 }
@@ -135,8 +135,10 @@ inline PlanPtrs plan_ptrs(void* ws, const PlanLayout& L) {
 }
 
 // ---- kernels_misc.cu
+// q_ctas / kv_ctas: CTAs the kernel that takes the query / key side's work
+// order launches per unit (the order is chosen from it; kernels_misc.cu).
 cudaError_t launch_tile_plan(const attn_fwd_params& p, const PlanPtrs& pp, int64_t nq, int64_t nk,
-                             bool need_kv_side, cudaStream_t st);
+                             bool need_kv_side, int64_t q_ctas, int64_t kv_ctas, cudaStream_t st);
 cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t s, int64_t inner_bytes,
                            int strategy, int cp, int stripe, bool inverse, cudaStream_t st);
 cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, const float* lse_blk,
@@ -160,6 +162,8 @@ struct FwdLaunch {
   bool withhold_kv = false;  // debug hook (attn_fwd_test_timeout)
 };
 cudaError_t launch_attn_fwd(const FwdLaunch& L, cudaStream_t st);
+// forward CTAs per (b, query tile): one per kv head and slot group of its query heads
+int64_t fwd_ctas_per_tile(const attn_fwd_params& p);
 
 // ---- attn_bwd.cu
 struct BwdLaunch {
@@ -187,6 +191,8 @@ struct SplitLaunch {
 };
 int split_bwd_query_rows(int64_t d, int64_t dv);
 int split_bwd_key_rows(int64_t d, int64_t dv);
+// dK / dV kernel CTAs per (b, key tile) and kv head: column slices of dK / dV
+int split_bwd_col_slices(int64_t d, int64_t dv);
 cudaError_t launch_attn_bwd_split(const SplitLaunch& L, cudaStream_t st);
 
 // ---- attn_api.cu

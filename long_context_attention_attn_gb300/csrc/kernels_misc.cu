@@ -152,10 +152,39 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-// Stable counting sort of n work rows by weight, heaviest first: rows of equal
-// weight keep their index order, so neighbouring tiles stay neighbours in the
-// launch order (their K/V, Q and dQ tiles are then shared through L2 by the
-// CTAs running at the same time).  Row i goes to
+// SM count of the current device (cached per device; safe across host threads).
+static int sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  int n = cached ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (cached) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Work order of the units (rows) of one side: the CTAs of a launch take them
+// in this order.  Two orders, chosen per call on the device:
+// * index order (key side: ascending; query side: descending).  Under the
+//   causal mask a segment's key tiles get lighter and its query tiles heavier
+//   with the tile index, so both are heavy first within every segment, and
+//   neighbouring tiles run at the same time, sharing their K / V, Q / dO and
+//   fp32 dQ tiles through L2;
+// * heavy first over all units (a stable counting sort by weight): the last
+//   units to start are the lightest, which bounds the tail of the launch, but
+//   CTAs running at the same time come from different segments.
+// The largest unit bounds what the index order can lose at the tail: when one
+// CTA of it is under 1/kTailShare of an SM's share of the launch (weight_max *
+// SMs * kTailShare <= sum of weights * CTAs per unit) the index order is
+// taken.  On GB300 at b 2 s 65536 Hq 128 Hkv 8 d 128 window 8192 (ratio 3.7 %
+// for the fused backward, 0.5 % for the forward) it halved the kernels' DRAM
+// traffic at the same speed; on the same packing at s 16384 Hq 32 window 1024
+// (11.9 %) heavy first ran the backward 13 % faster.
+//
+// The sort places row i at
 //   (rows with a larger weight) + (rows of its weight in earlier chunks)
 //   + (rows of its weight earlier in its own chunk of kSortChunk rows).
 // order_chunk_kernel: per chunk, the weight counts (a [chunks, buckets]
@@ -164,8 +193,11 @@ __global__ void __launch_bounds__(1024)
 // memory, then the distance to the first pair of the same weight).
 // order_colscan_kernel / order_bucketscan_kernel: the table's prefix down the
 // chunks of each weight, and the first position of each weight (a suffix sum
-// over the weights).
+// over the weights); the bucket scan also takes the choice of order and
+// stores it after the weights' positions.
 // order_scatter_kernel: order[position] = row.
+constexpr int kTailShare = 20;
+
 __device__ __forceinline__ int clamp_weight(int w, int buckets) {
   return w < 0 ? 0 : (w >= buckets ? buckets - 1 : w);
 }
@@ -247,14 +279,20 @@ __global__ void __launch_bounds__(256)
 
 // start[w] = number of rows whose weight is larger than w: one CTA; thread t
 // takes a run of consecutive weights from the largest down, sums it, and a
-// block-wide exclusive scan of the run sums gives each run's base.
+// block-wide exclusive scan of the run sums gives each run's base.  The same
+// pass sums weight * count and finds the largest weight present, and thread 0
+// stores start[buckets] = 1 (heavy first) or 0 (index order).
 __global__ void __launch_bounds__(1024)
-    order_bucketscan_kernel(int* __restrict__ start, int buckets) {
+    order_bucketscan_kernel(int* __restrict__ start, int buckets, int64_t ctas_per_unit, int sms) {
   __shared__ int warp_sum[32];
+  __shared__ long long warp_work[32];
+  __shared__ int warp_wmax[32];
   const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
   const int per = (buckets + blockDim.x - 1) / blockDim.x;
   const int p0 = t * per;  // positions p0.. of the list of weights from the largest down
   int sum = 0;
+  long long work = 0;
+  int wmax = 0;
   for (int k0 = 0; k0 < per; k0 += 8) {
     int v[8];
 #pragma unroll
@@ -263,7 +301,12 @@ __global__ void __launch_bounds__(1024)
       v[u] = (k0 + u < per && w >= 0) ? start[w] : 0;
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) sum += v[u];
+    for (int u = 0; u < 8; ++u) {
+      const int w = buckets - 1 - (p0 + k0 + u);
+      sum += v[u];
+      work += (long long)v[u] * w;
+      if (v[u] > 0) wmax = max(wmax, w);
+    }
   }
   int incl = sum;
 #pragma unroll
@@ -271,7 +314,18 @@ __global__ void __launch_bounds__(1024)
     const int u = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += u;
   }
+  long long wk = work;
+  int wm = wmax;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    wk += __shfl_xor_sync(0xffffffffu, wk, o);
+    wm = max(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+  }
   if (lane == 31) warp_sum[wid] = incl;
+  if (lane == 0) {
+    warp_work[wid] = wk;
+    warp_wmax[wid] = wm;
+  }
   __syncthreads();
   if (wid == 0) {
     int x = warp_sum[lane];
@@ -281,6 +335,15 @@ __global__ void __launch_bounds__(1024)
       if (lane >= o) x += u;
     }
     warp_sum[lane] = x;
+    long long tw = lane < (int)(blockDim.x >> 5) ? warp_work[lane] : 0;
+    int tm = lane < (int)(blockDim.x >> 5) ? warp_wmax[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tw += __shfl_xor_sync(0xffffffffu, tw, o);
+      tm = max(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+    }
+    if (lane == 0)
+      start[buckets] = (long long)tm * sms * kTailShare > tw * ctas_per_unit ? 1 : 0;
   }
   __syncthreads();
   int run = (wid > 0 ? warp_sum[wid - 1] : 0) + incl - sum;
@@ -293,18 +356,28 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// order[position] = row: the sorted position (heavy first), or the row's own
+// index (reversed on the query side) when the bucket scan chose index order.
 __global__ void order_scatter_kernel(const int* __restrict__ weight, int n, int buckets,
                                      const int* __restrict__ hist, const int* __restrict__ start,
-                                     const int* __restrict__ rank, int* __restrict__ order) {
+                                     const int* __restrict__ rank, int reverse,
+                                     int* __restrict__ order) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
+  if (start[buckets] == 0) {
+    order[reverse ? n - 1 - i : i] = (int)i;
+    return;
+  }
   const int w = clamp_weight(weight[i], buckets);
   const int64_t c = i / kSortChunk;
   order[start[w] + hist[c * buckets + w] + rank[i]] = (int)i;
 }
 
-static cudaError_t launch_heavy_first(const int* weight, int64_t n, const PlanPtrs& pp, int* order,
-                                      cudaStream_t st) {
+// ctas_per_unit: CTAs the consuming kernel launches per unit; reverse: the
+// query side (index order descending).
+static cudaError_t launch_work_order(const int* weight, int64_t n, int64_t ctas_per_unit,
+                                     bool reverse, const PlanPtrs& pp, int* order,
+                                     cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   const int64_t chunks = (n + kSortChunk - 1) / kSortChunk;
   const int buckets = (int)pp.sort_buckets;
@@ -314,14 +387,15 @@ static cudaError_t launch_heavy_first(const int* weight, int64_t n, const PlanPt
                                                               pp.sort_hist, pp.sort_rank);
   order_colscan_kernel<<<(unsigned)((buckets + 255) / 256), 256, 0, st>>>(pp.sort_hist, (int)chunks,
                                                                          buckets, pp.sort_start);
-  order_bucketscan_kernel<<<1, 1024, 0, st>>>(pp.sort_start, buckets);
+  order_bucketscan_kernel<<<1, 1024, 0, st>>>(pp.sort_start, buckets,
+                                              ctas_per_unit > 0 ? ctas_per_unit : 1, sm_count());
   order_scatter_kernel<<<(unsigned)chunks, kSortChunk, 0, st>>>(
-      weight, (int)n, buckets, pp.sort_hist, pp.sort_start, pp.sort_rank, order);
+      weight, (int)n, buckets, pp.sort_hist, pp.sort_start, pp.sort_rank, reverse ? 1 : 0, order);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tile_plan(const attn_fwd_params& p, const PlanPtrs& pp, int64_t nq, int64_t nk,
-                             bool need_kv_side, cudaStream_t st) {
+                             bool need_kv_side, int64_t q_ctas, int64_t kv_ctas, cudaStream_t st) {
   const int wpb = 8;
   tile_summary_kernel<<<(unsigned)((p.b * nq + wpb - 1) / wpb), wpb * 32, 0, st>>>(
       p.q_segment_ids, p.q_segment_pos, p.b, p.s_q, nq, pp.q_sum);
@@ -330,11 +404,12 @@ cudaError_t launch_tile_plan(const attn_fwd_params& p, const PlanPtrs& pp, int64
   tile_class_kernel<<<dim3((unsigned)nq, (unsigned)p.b), 256, 0, st>>>(
       pp.q_sum, pp.kv_sum, nq, nk, p.window_left, pp.classes, pp.q_range, pp.q_weight);
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_heavy_first(pp.q_weight, p.b * nq, pp, pp.q_order, st);
+  if (e == cudaSuccess)
+    e = launch_work_order(pp.q_weight, p.b * nq, q_ctas, true, pp, pp.q_order, st);
   if (e == cudaSuccess && need_kv_side) {
     kv_range_kernel<<<dim3((unsigned)((nk + 31) / 32), (unsigned)p.b), 1024, 0, st>>>(
         pp.classes, nq, nk, pp.kv_range, pp.kv_weight);
-    e = launch_heavy_first(pp.kv_weight, p.b * nk, pp, pp.kv_order, st);
+    e = launch_work_order(pp.kv_weight, p.b * nk, kv_ctas, false, pp, pp.kv_order, st);
   }
   return e;
 }
@@ -398,20 +473,6 @@ __global__ void permute_elem_kernel(const T* __restrict__ in, T* __restrict__ ou
     const int64_t dst = o * s + (inverse ? j : i);
     out[dst * epr + k] = in[src * epr + k];
   }
-}
-
-// SM count of the current device (cached per device; safe across host threads).
-static int sm_count() {
-  static std::atomic<int> cache[kMaxDevices];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-  const bool cached = dev >= 0 && dev < kMaxDevices;
-  int n = cached ? cache[dev].load(std::memory_order_relaxed) : 0;
-  if (n > 0) return n;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
-  if (cached) cache[dev].store(n, std::memory_order_relaxed);
-  return n;
 }
 
 cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t s, int64_t inner_bytes,

@@ -202,16 +202,40 @@ def test_concurrent_calls_from_host_threads(det):
             assert torch.equal(dq, want[2])
 
 
-@pytest.mark.parametrize("name,b,s", [
-    ("full_swa_64k", None, None),     # the benchmark's workload
-    ("packed_thd", None, None),
-    ("long_rows", 2, 1 << 20),        # 8192 tiles per row: 16384 units, weights up to 8192
-    ("ragged", 3, 3000),              # ragged tail, many equal weights
+def _expected_order(w, ctas, sms, reverse):
+    """The work order by its rule: heavy first (a stable sort) when the
+    heaviest unit's CTA is more than 1/20 of an SM's share of the launch,
+    else index order (descending on the query side)."""
+    if int(w.max()) * sms * 20 > int(w.sum()) * ctas:
+        return np.argsort(-w, kind="stable")
+    idx = np.arange(w.size)
+    return idx[::-1] if reverse else idx
+
+
+@pytest.mark.parametrize("name,b,s,hq,hkv,want", [
+    # one head: every unit is a large share of the launch, heavy first on both sides
+    ("full_swa_64k", None, None, 1, 1, ("sort", "sort")),
+    ("packed_thd", None, None, 1, 1, ("sort", "sort")),
+    ("ragged", 3, 3000, 1, 1, ("sort", "sort")),        # ragged tail, many equal weights
+    # two rows of a million tokens (8192 tiles per row): one causal segment
+    # with window 300000 (16384 units, none over 1.1 % of an SM's share:
+    # index order), and 3/4 padding then a causal segment of 262144 (weights
+    # to 2048, 12288 units of weight 0: heavy first, ties across many chunks)
+    ("long_rows", 2, 1 << 20, 1, 1, ("index", "index")),
+    ("long_tail_segment", 2, 1 << 20, 1, 1, ("sort", "sort")),
+    # the benchmark's workload with its heads: index order on both sides
+    ("full_swa_64k", None, None, 128, 8, ("index", "index")),
+    # short window, few units: heavy first on both sides
+    ("packed_swa", None, None, 32, 8, ("sort", "sort")),
+    # one causal segment: index order for the queries, heavy first for the keys
+    ("ring_cp4", None, None, 64, 8, ("index", "sort")),
 ])
-def test_heavy_first_order_is_stable_argsort(name, b, s):
-    """The work order of the kernels equals a host stable argsort of the plan
-    weights, heaviest first (bit for bit, both sides), at the 64k workload and
-    at two rows of a million tokens (no cap on the weights)."""
+def test_work_order_follows_its_rule(name, b, s, hq, hkv, want):
+    """The kernels' work order equals the rule's order computed on the host
+    from the plan weights (bit for bit, both sides): a stable heaviest-first
+    argsort, or index order, as the tail ratio decides; at the 64k workload
+    with one head and with its 128 / 8 heads, and at two rows of a million
+    tokens in both orders (no cap on the weights)."""
     import long_context_attention_attn_gb300 as ga
     if name in workload.WORKLOADS:
         w = workload.WORKLOADS[name]
@@ -220,19 +244,37 @@ def test_heavy_first_order_is_stable_argsort(name, b, s):
     elif name == "long_rows":
         ids, pos = workload.segments(b, s, None)  # one causal segment per row
         window = 300000
+    elif name == "long_tail_segment":
+        ids = torch.zeros(b, s, dtype=torch.int32)
+        pos = torch.zeros(b, s, dtype=torch.int32)
+        ids[:, 3 * s // 4:] = 1
+        pos[:, 3 * s // 4:] = torch.arange(s // 4, dtype=torch.int32)
+        window = -1
     else:
         ids, pos = workload.random_segments(b, s, seed=3)
         window = 700
     dev_ids, dev_pos = ids.cuda(), pos.cuda()
-    q = torch.empty(b, s, 1, 64, dtype=torch.bfloat16, device="cuda")  # only shapes are read
-    cls, _ = ga.attn_tile_plan(q, q, dev_ids, dev_pos, window_left=window)
-    qo, ko = ga.attn_tile_order(q, q, dev_ids, dev_pos, window_left=window)
+    # only shapes are read
+    q = torch.empty(b, s, hq, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty(b, s, hkv, 64, dtype=torch.bfloat16, device="cuda")
+    cls, _ = ga.attn_tile_plan(q, k, dev_ids, dev_pos, window_left=window)
+    qo, ko = ga.attn_tile_order(q, k, dev_ids, dev_pos, window_left=window)
     torch.cuda.synchronize()
+    del q, k
     c = cls.cpu().numpy() != 0
     q_w = c.sum(axis=2).reshape(-1)
     k_w = c.sum(axis=1).reshape(-1)
-    np.testing.assert_array_equal(qo.cpu().numpy(), np.argsort(-q_w, kind="stable"))
-    np.testing.assert_array_equal(ko.cpu().numpy(), np.argsort(-k_w, kind="stable"))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    q_ctas = hkv * -(-(hq // hkv) // 2)  # forward: one CTA per kv head and pair of query heads
+    k_ctas = hkv                         # fused backward: one CTA per kv head
+    eq = _expected_order(q_w, q_ctas, sms, True)
+    ek = _expected_order(k_w, k_ctas, sms, False)
+    np.testing.assert_array_equal(qo.cpu().numpy(), eq)
+    np.testing.assert_array_equal(ko.cpu().numpy(), ek)
+    # the case covers the branch it is listed for (on one causal segment the
+    # key side's sort is the index order itself: weights fall with the index)
+    rule = lambda w, ctas: "sort" if int(w.max()) * sms * 20 > int(w.sum()) * ctas else "index"
+    assert (rule(q_w, q_ctas), rule(k_w, k_ctas)) == want
 
 
 @pytest.mark.parametrize("det", [False, True])
