@@ -165,9 +165,12 @@ typedef struct attn_fwd_params {
  *  delta            optional output (NULL: none): fp32 [b, h_q, s_q], 4-byte
  *                   aligned, D = rowsum(dO * O) of every query row and head,
  *                   as the backward uses it (its workspace copy otherwise).
- *                   Its sum is vdot(out, dout), the loss whose gradient this
- *                   call computes (TE tutorial section 5 differentiates that
- *                   vdot).  Must not overlap the other buffers.
+ *                   Rows of a 128-row query tile that sees no key at all
+ *                   (padding, where attn_fwd leaves O = 0) get 0 without O and
+ *                   dO being read.  Its sum is vdot(out, dout), the loss whose
+ *                   gradient this call computes (TE tutorial section 5
+ *                   differentiates that vdot).  Must not overlap the other
+ *                   buffers.
  */
 typedef struct attn_bwd_params {
   attn_fwd_params fwd;

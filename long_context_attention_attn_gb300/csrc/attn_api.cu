@@ -303,7 +303,8 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
       e = launch_tile_plan(*f, sl.plan, sl.nq, sl.nk, true, f->h_q,
                            f->h_kv * split_bwd_col_slices(f->d, dv), st);
     if (e == cudaSuccess)
-      e = launch_bwd_preprocess(f->out, p->dout, sl.D, nullptr, f->b, f->s_q, f->h_q, dv, st);
+      e = launch_bwd_preprocess(f->out, p->dout, sl.D, nullptr, sl.plan.q_weight, f->b, f->s_q,
+                                f->h_q, dv, st);
     if (e == cudaSuccess) e = mark(0);
     if (e == cudaSuccess) e = launch_attn_bwd_split(sl, st);
     if (e == cudaSuccess) e = mark(1);
@@ -329,20 +330,20 @@ int attn_bwd(const attn_bwd_params* p, attn_stream_t stream) {
       !encode_qkv_map(&bl.tm_do, p->dout, f->b, f->s_q, f->h_q, f->d, 0) ||
       !encode_acc_map(&bl.tm_dq, bl.dq_acc, f->b, f->s_q, f->h_q, f->d))
     return ATTN_ERR_CUDA;
-  const size_t n_dq = (size_t)(f->b * f->s_q * f->h_q * f->d);
   cudaError_t e = cudaMemsetAsync(bl.plan.status, 0, sizeof(int), st);
   if (e == cudaSuccess)
     e = launch_tile_plan(*f, bl.plan, bl.nq, bl.nk, true, f->h_q, f->h_kv, st);
   // the D pre-pass also zeroes the workspace's fp32 dQ accumulator (not the
   // caller's accumulator in accumulate mode)
   if (e == cudaSuccess)
-    e = launch_bwd_preprocess(f->out, p->dout, bl.D, acc ? nullptr : bl.dq_acc, f->b, f->s_q,
-                              f->h_q, f->d, st);
+    e = launch_bwd_preprocess(f->out, p->dout, bl.D, acc ? nullptr : bl.dq_acc,
+                              bl.plan.q_weight, f->b, f->s_q, f->h_q, f->d, st);
   if (e == cudaSuccess) e = mark(0);
   if (e == cudaSuccess) e = launch_attn_bwd(bl, st);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
-  if (e == cudaSuccess && !acc) e = launch_dq_finalize(bl.dq_acc, p->dq, (int64_t)n_dq, st);
+  if (e == cudaSuccess && !acc)
+    e = launch_dq_finalize(bl.dq_acc, p->dq, bl.plan.q_weight, f->b, f->s_q, f->h_q, f->d, st);
   return cuda_status(e);
 }
 

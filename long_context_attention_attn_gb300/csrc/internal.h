@@ -145,10 +145,15 @@ cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, co
                          int blk_bf16, void* out_final, int64_t b, int64_t s, int64_t h, int64_t d,
                          cudaStream_t st);
 // D = rowsum(dout * out) per row-head; also zeroes zero_acc (fp32, out's
-// layout) when it is not null.
+// layout) when it is not null.  Query tiles of plan weight 0 (q_weight
+// [b, ceil(s/128)]) get D = 0 and keep their accumulator rows untouched.
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, float* zero_acc,
-                                  int64_t b, int64_t s, int64_t h, int64_t d, cudaStream_t st);
-cudaError_t launch_dq_finalize(const float* acc, void* dq, int64_t n, cudaStream_t st);
+                                  const int* q_weight, int64_t b, int64_t s, int64_t h, int64_t d,
+                                  cudaStream_t st);
+// dq (bf16, [b, s, h, d]) from the fp32 accumulator; zeros for query tiles of
+// plan weight 0, whose accumulator rows are not read.
+cudaError_t launch_dq_finalize(const float* acc, void* dq, const int* q_weight, int64_t b,
+                               int64_t s, int64_t h, int64_t d, cudaStream_t st);
 constexpr int kSegMax = 8192;  // segments per row accepted by launch_segments
 cudaError_t launch_segments(const int* seqlens, const int* offsets, int64_t b, int64_t nseg,
                             int64_t s, int* ids, int* pos, cudaStream_t st);

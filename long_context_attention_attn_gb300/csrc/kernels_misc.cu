@@ -633,113 +633,152 @@ cudaError_t launch_merge(float* out_acc, float* lse_acc, const void* out_blk, co
 // The LSE/D layout is [b, h, s] so each row-head writes one float.  With
 // zero_acc the same pass clears the fp32 dQ accumulator (out's layout, 32
 // bytes per thread and row), instead of a separate memset over it.
+// Work items are (query tile, slice of kPreGroups row groups per warp), so the
+// tile's plan weight is read once per item.  Rows of a tile of weight 0 (it
+// sees no key tile: padding) take no step of the backward: their D is 0
+// (their O is 0) and is written without reading O or dO, and their
+// accumulator rows are not cleared (no reduce-add reaches them; the finalise
+// writes their zeros).
+constexpr int kPreThreads = 256;
+constexpr int kPreGroups = 4;  // row groups in flight per warp and item
+
 template <int D>
-__global__ void bwd_preprocess_kernel(const uint4* __restrict__ out, const uint4* __restrict__ dout,
-                                      float* __restrict__ Dv, float4* __restrict__ zero_acc,
-                                      int64_t b, int64_t s, int64_t h) {
-  constexpr int kLanes = D / 8;            // lanes per row-head
+__global__ void __launch_bounds__(kPreThreads)
+    bwd_preprocess_kernel(const uint4* __restrict__ out, const uint4* __restrict__ dout,
+                          float* __restrict__ Dv, float4* __restrict__ zero_acc,
+                          const int* __restrict__ q_weight, int64_t s, int64_t h, int64_t nq,
+                          int64_t nslices, int64_t nitems) {
+  constexpr int kLanes = D / 8;  // lanes per row-head
   constexpr int kRowsPerWarp = 32 / kLanes;
+  constexpr int kWarps = kPreThreads / 32;
+  constexpr int kItemRows = kWarps * kRowsPerWarp * kPreGroups;
   const int lane = threadIdx.x & 31;
   const int sub = lane % kLanes;
-  const int64_t nrows = b * s * h;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
-  const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  for (int64_t r0 = warp0 * kRowsPerWarp; r0 < nrows; r0 += nwarps * kRowsPerWarp * 2) {
-    // two independent row groups per iteration keep more bytes in flight
-    const int64_t ra = r0 + lane / kLanes;
-    const int64_t rb = ra + nwarps * kRowsPerWarp;
-    uint4 oa = make_uint4(0, 0, 0, 0), da = oa, ob = oa, db = oa;
-    if (ra < nrows) {
-      oa = out[ra * kLanes + sub];
-      da = dout[ra * kLanes + sub];
+  const int wrow = (threadIdx.x / 32) * kRowsPerWarp * kPreGroups + lane / kLanes;
+  for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+    const int64_t tile = item / nslices, slice = item % nslices;
+    const int64_t bi = tile / nq, t0 = (tile % nq) * kTile;
+    const int64_t t1 = t0 + kTile < s ? t0 + kTile : s;
+    const int64_t row0 = (bi * s + t0) * h;  // the tile's first row-head
+    const int nrows = (int)((t1 - t0) * h);  // row-heads of the tile (<= 128 h)
+    const int lo = (int)(slice * kItemRows);
+    if (lo >= nrows) continue;
+    const bool live = q_weight[tile] != 0;
+    uint4 o[kPreGroups], g[kPreGroups];
+#pragma unroll
+    for (int k = 0; k < kPreGroups; ++k) {
+      const int lr = lo + wrow + k * kRowsPerWarp;  // row-head within the tile
+      o[k] = make_uint4(0, 0, 0, 0);
+      g[k] = o[k];
+      if (live && lr < nrows) {
+        o[k] = out[(row0 + lr) * kLanes + sub];
+        g[k] = dout[(row0 + lr) * kLanes + sub];
+      }
     }
-    if (rb < nrows) {
-      ob = out[rb * kLanes + sub];
-      db = dout[rb * kLanes + sub];
-    }
-    if (zero_acc) {
+    if (zero_acc && live) {
       // the fp32 dQ accumulator has out's layout: clear this thread's 8 values
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ra < nrows) {
-        zero_acc[(ra * kLanes + sub) * 2] = z;
-        zero_acc[(ra * kLanes + sub) * 2 + 1] = z;
-      }
-      if (rb < nrows) {
-        zero_acc[(rb * kLanes + sub) * 2] = z;
-        zero_acc[(rb * kLanes + sub) * 2 + 1] = z;
+#pragma unroll
+      for (int k = 0; k < kPreGroups; ++k) {
+        const int lr = lo + wrow + k * kRowsPerWarp;
+        if (lr < nrows) {
+          zero_acc[((row0 + lr) * kLanes + sub) * 2] = z;
+          zero_acc[((row0 + lr) * kLanes + sub) * 2 + 1] = z;
+        }
       }
     }
-    auto dot8 = [](const uint4& x, const uint4& y) {
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-      const uint32_t ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int k = 0; k < kPreGroups; ++k) {
+      const uint32_t xs[4] = {o[k].x, o[k].y, o[k].z, o[k].w};
+      const uint32_t ys[4] = {g[k].x, g[k].y, g[k].z, g[k].w};
       float acc = 0.f;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[k]));
-        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[k]));
-        acc += a.x * c.x + a.y * c.y;
+      for (int u = 0; u < 4; ++u) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[u]));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[u]));
+        acc += x.x * y.x + x.y * y.y;
       }
-      return acc;
-    };
-    float sa = dot8(oa, da), sb = dot8(ob, db);
 #pragma unroll
-    for (int off = kLanes / 2; off > 0; off >>= 1) {
-      sa += __shfl_xor_sync(0xffffffffu, sa, off);
-      sb += __shfl_xor_sync(0xffffffffu, sb, off);
-    }
-    if (sub == 0) {
-      if (ra < nrows) {
-        const int64_t hh = ra % h, ti = (ra / h) % s, bi = ra / (h * s);
-        Dv[(bi * h + hh) * s + ti] = sa;
-      }
-      if (rb < nrows) {
-        const int64_t hh = rb % h, ti = (rb / h) % s, bi = rb / (h * s);
-        Dv[(bi * h + hh) * s + ti] = sb;
+      for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const int lr = lo + wrow + k * kRowsPerWarp;
+      if (sub == 0 && lr < nrows) {
+        const int hh = lr % (int)h;
+        const int64_t ti = t0 + lr / (int)h;
+        Dv[(bi * h + hh) * s + ti] = acc;
       }
     }
   }
 }
 
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, float* D, float* zero_acc,
-                                  int64_t b, int64_t s, int64_t h, int64_t d, cudaStream_t st) {
-  const int64_t rows = b * s * h;
-  const int rows_per_cta = 8 * (d == 256 ? 1 : d == 128 ? 2 : 4);
-  const unsigned grid =
-      (unsigned)std::min<int64_t>((rows + rows_per_cta - 1) / rows_per_cta, (int64_t)sm_count() * 16);
+                                  const int* q_weight, int64_t b, int64_t s, int64_t h, int64_t d,
+                                  cudaStream_t st) {
+  const int64_t nq = (s + kTile - 1) / kTile;
+  const int64_t item_rows = (kPreThreads / 32) * (32 / (d / 8)) * kPreGroups;
+  const int64_t nslices = (kTile * h + item_rows - 1) / item_rows;
+  const int64_t nitems = b * nq * nslices;
+  if (nitems == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)std::min<int64_t>(nitems, (int64_t)sm_count() * 16);
+  const uint4* o4 = static_cast<const uint4*>(out);
+  const uint4* d4 = static_cast<const uint4*>(dout);
+  float4* z4 = reinterpret_cast<float4*>(zero_acc);
   if (d == 256)
-    bwd_preprocess_kernel<256><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
-                                                     static_cast<const uint4*>(dout), D,
-                                                     reinterpret_cast<float4*>(zero_acc), b, s, h);
+    bwd_preprocess_kernel<256><<<grid, kPreThreads, 0, st>>>(o4, d4, D, z4, q_weight, s, h, nq,
+                                                             nslices, nitems);
   else if (d == 128)
-    bwd_preprocess_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
-                                                     static_cast<const uint4*>(dout), D,
-                                                     reinterpret_cast<float4*>(zero_acc), b, s, h);
+    bwd_preprocess_kernel<128><<<grid, kPreThreads, 0, st>>>(o4, d4, D, z4, q_weight, s, h, nq,
+                                                             nslices, nitems);
   else
-    bwd_preprocess_kernel<64><<<grid, 256, 0, st>>>(static_cast<const uint4*>(out),
-                                                    static_cast<const uint4*>(dout), D,
-                                                    reinterpret_cast<float4*>(zero_acc), b, s, h);
+    bwd_preprocess_kernel<64><<<grid, kPreThreads, 0, st>>>(o4, d4, D, z4, q_weight, s, h, nq,
+                                                            nslices, nitems);
   return cudaGetLastError();
 }
 
-__global__ void dq_finalize_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
-                                   int64_t n4) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 v = acc[i];
-    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-    const __nv_bfloat162 c = __floats2bfloat162_rn(v.z, v.w);
-    uint2 o;
-    o.x = *reinterpret_cast<const uint32_t*>(&a);
-    o.y = *reinterpret_cast<const uint32_t*>(&c);
-    dq[i] = o;
+// dq (bf16) from the fp32 accumulator, both [b, s, h, d].  Work items are
+// (query tile, slice of kFinSlice float4 groups) so that a tile's plan weight is
+// read once per item; a tile of weight 0 (no key tile reaches it) gets zeros
+// without its accumulator rows being read (the pre-pass did not clear them).
+constexpr int kFinThreads = 256;
+constexpr int64_t kFinSlice = kFinThreads * 8;
+
+__global__ void __launch_bounds__(kFinThreads)
+    dq_finalize_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
+                       const int* __restrict__ q_weight, int64_t s, int64_t nq, int64_t per_tok4,
+                       int64_t nslices, int64_t nitems) {
+  for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+    const int64_t tile = item / nslices, slice = item % nslices;
+    const int64_t bi = tile / nq, t0 = (tile % nq) * kTile;
+    const int64_t t1 = t0 + kTile < s ? t0 + kTile : s;
+    const int64_t lo = (bi * s + t0) * per_tok4 + slice * kFinSlice;
+    const int64_t end = (bi * s + t1) * per_tok4;
+    const int64_t hi = lo + kFinSlice < end ? lo + kFinSlice : end;
+    const bool live = q_weight[tile] != 0;
+#pragma unroll 4
+    for (int64_t i = lo + threadIdx.x; i < hi; i += kFinThreads) {
+      uint2 o = make_uint2(0u, 0u);
+      if (live) {
+        const float4 v = acc[i];
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 c = __floats2bfloat162_rn(v.z, v.w);
+        o.x = *reinterpret_cast<const uint32_t*>(&a);
+        o.y = *reinterpret_cast<const uint32_t*>(&c);
+      }
+      dq[i] = o;
+    }
   }
 }
 
-cudaError_t launch_dq_finalize(const float* acc, void* dq, int64_t n, cudaStream_t st) {
-  const int64_t n4 = n / 4;
-  const unsigned grid = (unsigned)std::min<int64_t>((n4 + 255) / 256, (int64_t)sm_count() * 16);
-  dq_finalize_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(acc),
-                                           static_cast<uint2*>(dq), n4);
+cudaError_t launch_dq_finalize(const float* acc, void* dq, const int* q_weight, int64_t b,
+                               int64_t s, int64_t h, int64_t d, cudaStream_t st) {
+  const int64_t nq = (s + kTile - 1) / kTile;
+  const int64_t per_tok4 = h * d / 4;
+  const int64_t nslices = (kTile * per_tok4 + kFinSlice - 1) / kFinSlice;
+  const int64_t nitems = b * nq * nslices;
+  if (nitems == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)std::min<int64_t>(nitems, (int64_t)sm_count() * 16);
+  dq_finalize_kernel<<<grid, kFinThreads, 0, st>>>(reinterpret_cast<const float4*>(acc),
+                                                   static_cast<uint2*>(dq), q_weight, s, nq,
+                                                   per_tok4, nslices, nitems);
   return cudaGetLastError();
 }
 
