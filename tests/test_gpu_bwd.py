@@ -279,3 +279,47 @@ def test_delta_output_is_rowsum_of_dout_times_out(det):
     assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
     if det:
         assert torch.equal(got[0], ref[0])
+
+
+@pytest.mark.parametrize("det", [False, True])
+def test_stale_workspace_changes_no_result(det):
+    """The workspace is scratch: filled with NaN bytes before the call, it
+    changes no result.  (The fp32 dQ accumulator rows of query tiles that
+    see no key are neither cleared by the pre-pass nor read by the finalise;
+    their dq is written as zeros.)"""
+    import long_context_attention_attn_gb300 as ga
+    w = workload.WORKLOADS["packed_swa"]
+    x = workload.make(w, device=DEV, with_dout=True)
+    q, k, v, ids, pos, dout = x["q"], x["k"], x["v"], x["ids"], x["pos"], x["dout"]
+    kw = dict(window_left=w.window_left, scale=w.scale, deterministic=det)
+    out, lse = ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale)
+    ref = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, **kw)
+    need = ga.workspace_bytes_bwd(q, k, ids, pos, w.window_left, v=v, deterministic=det)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)  # fp32 NaN everywhere
+    got = ga.attn_bwd(q, k, v, out, lse, dout, ids, pos, workspace=ws, check_status=True, **kw)
+    torch.cuda.synchronize()
+    for g in got:
+        assert torch.isfinite(g).all()
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+    if det:
+        assert torch.equal(got[0], ref[0])
+    else:  # dQ sums with unordered fp32 reduce-adds
+        check_grad(got[0].cpu(), ref[0].cpu(), "dq")
+    pad = ids == 0
+    assert torch.all(got[0][pad] == 0)
+
+
+def test_stale_forward_workspace_changes_no_result():
+    """attn_fwd's workspace (tile plan, work order) filled with NaN bytes
+    before the call: out and lse bit-identical to a call on a fresh one."""
+    import long_context_attention_attn_gb300 as ga
+    w = workload.WORKLOADS["packed_swa"]
+    x = workload.make(w, device=DEV, with_dout=False)
+    q, k, v, ids, pos = x["q"], x["k"], x["v"], x["ids"], x["pos"]
+    out, lse = ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale)
+    need = ga.workspace_bytes_fwd(q, k, ids, pos, window_left=w.window_left, v=v)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)
+    out2, lse2 = ga.attn_fwd(q, k, v, ids, pos, window_left=w.window_left, scale=w.scale,
+                             workspace=ws, check_status=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
