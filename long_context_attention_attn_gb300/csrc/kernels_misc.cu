@@ -15,13 +15,10 @@ namespace gb300 {
 // a mask, mask the overlapping ones.  Generalised to segments, padding and a
 // left window through per-tile summaries of the segment descriptors.
 
-__global__ void tile_summary_kernel(const int* __restrict__ ids, const int* __restrict__ pos,
-                                    int64_t b, int64_t s, int64_t ntile,
-                                    TileSummary* __restrict__ out) {
-  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  if (w >= b * ntile) return;
-  const int64_t bi = w / ntile, t = w % ntile;
+// Summary of tile t of batch row bi (one warp; every lane returns it).
+__device__ __forceinline__ TileSummary warp_tile_summary(const int* __restrict__ ids,
+                                                         const int* __restrict__ pos, int64_t s,
+                                                         int64_t bi, int64_t t, int lane) {
   int any_valid = 0, has_pad = 0;
   int id_min = INT_MAX, id_max = INT_MIN, pmin = INT_MAX, pmax = INT_MIN;
 #pragma unroll
@@ -49,17 +46,25 @@ __global__ void tile_summary_kernel(const int* __restrict__ ids, const int* __re
   id_max = __reduce_max_sync(0xffffffffu, id_max);
   pmin = __reduce_min_sync(0xffffffffu, pmin);
   pmax = __reduce_max_sync(0xffffffffu, pmax);
-  if (lane == 0) {
-    TileSummary r;
-    r.any_valid = any_valid;
-    r.has_pad = has_pad;
-    r.id_min = any_valid ? id_min : 0;
-    r.id_max = any_valid ? id_max : 0;
-    r.pos_min = any_valid ? pmin : 0;
-    r.pos_max = any_valid ? pmax : 0;
-    r.reserved0 = r.reserved1 = 0;
-    out[w] = r;
-  }
+  TileSummary r;
+  r.any_valid = any_valid;
+  r.has_pad = has_pad;
+  r.id_min = any_valid ? id_min : 0;
+  r.id_max = any_valid ? id_max : 0;
+  r.pos_min = any_valid ? pmin : 0;
+  r.pos_max = any_valid ? pmax : 0;
+  r.reserved0 = r.reserved1 = 0;
+  return r;
+}
+
+__global__ void tile_summary_kernel(const int* __restrict__ ids, const int* __restrict__ pos,
+                                    int64_t b, int64_t s, int64_t ntile,
+                                    TileSummary* __restrict__ out) {
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= b * ntile) return;
+  const TileSummary r = warp_tile_summary(ids, pos, s, w / ntile, w % ntile, lane);
+  if (lane == 0) out[w] = r;
 }
 
 __device__ __forceinline__ uint8_t classify(const TileSummary& q, const TileSummary& k, int window) {
@@ -394,8 +399,173 @@ static cudaError_t launch_work_order(const int* weight, int64_t n, int64_t ctas_
   return cudaGetLastError();
 }
 
+// ---- the whole plan in one CTA, for small problems (both sides at most
+// kSmallPlanUnits units, at most kSmallPlanPairs class bytes): the same
+// summaries, classes, ranges, weights and work orders as the kernels above,
+// in one launch instead of up to fifteen (the plan is then most of a small
+// call's launches).
+
+constexpr int kSmallPlanUnits = 1024;
+// One CTA's serial walk overtakes the parallel kernels' extra launches near
+// here: on GB300 the fused plan saved ~20 / 40 µs per forward / backward call
+// at 2 x 4096 tokens (2048 class bytes) and cost ~20 µs at 2 x 16384 (32768).
+constexpr int64_t kSmallPlanPairs = 4096;
+
+// The work order of one side (n <= 1024 units), block-wide: the choice rule of
+// order_bucketscan_kernel from a block reduction, and the heavy-first order
+// from one bitonic sort of (heaviest first, index) keys (the single-chunk case
+// of the counting sort: same order).  Every thread of the block calls it.
+__device__ void small_work_order(const int* __restrict__ weight, int n, int64_t ctas_per_unit,
+                                 int sms, bool reverse, int* __restrict__ order, uint64_t* keys) {
+  __shared__ long long r_work[32];
+  __shared__ int r_wmax[32];
+  __shared__ int s_lpt;
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const int w = t < n ? weight[t] : 0;
+  long long wk = w;
+  int wm = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    wk += __shfl_xor_sync(0xffffffffu, wk, o);
+    wm = max(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+  }
+  if (lane == 0) {
+    r_work[wid] = wk;
+    r_wmax[wid] = wm;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    long long tw = r_work[lane];
+    int tm = r_wmax[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tw += __shfl_xor_sync(0xffffffffu, tw, o);
+      tm = max(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+    }
+    if (lane == 0)
+      s_lpt = (long long)tm * sms * kTailShare > tw * (ctas_per_unit > 0 ? ctas_per_unit : 1);
+  }
+  __syncthreads();
+  if (!s_lpt) {  // uniform over the block
+    if (t < n) order[reverse ? n - 1 - t : t] = t;
+    return;
+  }
+  keys[t] = t < n ? ((uint64_t)(uint32_t)(INT_MAX - w) << 32) | (uint32_t)t : ~0ull;
+  __syncthreads();
+  for (int k = 2; k <= kSmallPlanUnits; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int q = t ^ j;
+      if (q > t) {
+        const uint64_t x = keys[t], y = keys[q];
+        if ((x > y) == ((t & k) == 0)) {
+          keys[t] = y;
+          keys[q] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (t < n) order[t] = (int)(uint32_t)keys[t];
+}
+
+struct SmallPlanArgs {
+  const int* q_ids;
+  const int* q_pos;
+  const int* kv_ids;
+  const int* kv_pos;
+  int64_t b, s_q, s_kv, nq, nk, q_ctas, kv_ctas;
+  int window, need_kv, sms;
+};
+
+__global__ void __launch_bounds__(kSmallPlanUnits)
+    small_plan_kernel(const SmallPlanArgs a, const PlanPtrs pp) {
+  __shared__ uint64_t keys[kSmallPlanUnits];
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  constexpr int kWarps = kSmallPlanUnits / 32;
+  const int64_t nqt = a.b * a.nq, nkt = a.b * a.nk;
+  // summaries: one warp per tile, query tiles then key tiles
+  for (int64_t u = wid; u < nqt + nkt; u += kWarps) {
+    const bool qside = u < nqt;
+    const int64_t v = qside ? u : u - nqt, nt = qside ? a.nq : a.nk;
+    const TileSummary r = qside ? warp_tile_summary(a.q_ids, a.q_pos, a.s_q, v / nt, v % nt, lane)
+                                : warp_tile_summary(a.kv_ids, a.kv_pos, a.s_kv, v / nt, v % nt, lane);
+    if (lane == 0) (qside ? pp.q_sum : pp.kv_sum)[v] = r;
+  }
+  __syncthreads();
+  // classes, and each query tile's range and weight: one warp per query tile
+  for (int64_t r = wid; r < nqt; r += kWarps) {
+    const int64_t bi = r / a.nq;
+    const TileSummary qsum = pp.q_sum[r];
+    int first = INT_MAX, last = -1, count = 0;
+    for (int64_t c = lane; c < a.nk; c += 32) {
+      const uint8_t k = classify(qsum, pp.kv_sum[bi * a.nk + c], a.window);
+      pp.classes[r * a.nk + c] = k;
+      if (k != kSkip) {
+        first = min(first, (int)c);
+        last = max(last, (int)c);
+        ++count;
+      }
+    }
+    first = __reduce_min_sync(0xffffffffu, first);
+    last = __reduce_max_sync(0xffffffffu, last);
+    count = __reduce_add_sync(0xffffffffu, count);
+    if (lane == 0) {
+      pp.q_range[r] = last < 0 ? make_int2(0, -1) : make_int2(first, last);
+      pp.q_weight[r] = count;
+    }
+  }
+  __syncthreads();
+  // each key tile's range and weight: one warp per key tile
+  if (a.need_kv) {
+    for (int64_t kc = wid; kc < nkt; kc += kWarps) {
+      const int64_t bi = kc / a.nk, c = kc % a.nk;
+      int first = INT_MAX, last = -1, count = 0;
+      for (int64_t r = lane; r < a.nq; r += 32) {
+        if (pp.classes[(bi * a.nq + r) * a.nk + c] != kSkip) {
+          first = min(first, (int)r);
+          last = max(last, (int)r);
+          ++count;
+        }
+      }
+      first = __reduce_min_sync(0xffffffffu, first);
+      last = __reduce_max_sync(0xffffffffu, last);
+      count = __reduce_add_sync(0xffffffffu, count);
+      if (lane == 0) {
+        pp.kv_range[kc] = last < 0 ? make_int2(0, -1) : make_int2(first, last);
+        pp.kv_weight[kc] = count;
+      }
+    }
+  }
+  __syncthreads();
+  small_work_order(pp.q_weight, (int)nqt, a.q_ctas, a.sms, true, pp.q_order, keys);
+  if (a.need_kv) {
+    __syncthreads();
+    small_work_order(pp.kv_weight, (int)nkt, a.kv_ctas, a.sms, false, pp.kv_order, keys);
+  }
+}
+
 cudaError_t launch_tile_plan(const attn_fwd_params& p, const PlanPtrs& pp, int64_t nq, int64_t nk,
                              bool need_kv_side, int64_t q_ctas, int64_t kv_ctas, cudaStream_t st) {
+  if (p.b * nq <= kSmallPlanUnits && p.b * nk <= kSmallPlanUnits &&
+      p.b * nq * nk <= kSmallPlanPairs) {
+    SmallPlanArgs a;
+    a.q_ids = p.q_segment_ids;
+    a.q_pos = p.q_segment_pos;
+    a.kv_ids = p.kv_segment_ids;
+    a.kv_pos = p.kv_segment_pos;
+    a.b = p.b;
+    a.s_q = p.s_q;
+    a.s_kv = p.s_kv;
+    a.nq = nq;
+    a.nk = nk;
+    a.q_ctas = q_ctas;
+    a.kv_ctas = kv_ctas;
+    a.window = (int)p.window_left;
+    a.need_kv = need_kv_side ? 1 : 0;
+    a.sms = sm_count();
+    small_plan_kernel<<<1, kSmallPlanUnits, 0, st>>>(a, pp);
+    return cudaGetLastError();
+  }
   const int wpb = 8;
   tile_summary_kernel<<<(unsigned)((p.b * nq + wpb - 1) / wpb), wpb * 32, 0, st>>>(
       p.q_segment_ids, p.q_segment_pos, p.b, p.s_q, nq, pp.q_sum);
