@@ -503,6 +503,21 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def plan_launches(w):
+    """Kernels one attn_fwd and one attn_bwd call launch on this workload.
+
+    The tile plan is one kernel when b * ceil(s/128)^2 <= 4096 (and each side
+    has at most 1024 tiles), else two summaries, the classes and four order
+    kernels per side, plus the key ranges on the backward.  Forward: plan +
+    fused kernel; backward: plan + D pre-pass + fused kernel + dQ finalise, or
+    + dK / dV kernel + dQ kernel (same count)."""
+    nq = -(-w.s // 128)
+    small = w.b * nq <= 1024 and w.b * nq * nq <= 4096
+    fwd = (1 if small else 7) + 1
+    bwd = (1 if small else 12) + 3
+    return fwd, bwd
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -732,11 +747,9 @@ def run_ours(args, rank, world, local_rank):
         val, info = oracle_sample(w)
         cpu = {"value": val, "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
                "sample": info["sample"]}
-    # fwd: plan (2 summaries, classes, 4-kernel order sort) + 1 fused kernel;
-    # bwd: plan (+ kv ranges and the kv-side sort) + D pre-pass + fused kernel +
-    # dQ finalise, or + dK / dV kernel + dQ kernel
     split_bwd = args.deterministic or w.d == 256 or w.dv != w.d
-    launches_per_step = 8 + 15
+    fwd_launches, bwd_launches = plan_launches(w)
+    launches_per_step = fwd_launches + bwd_launches
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
@@ -813,7 +826,7 @@ def fwd_only_line(args, w, world, pairs, value, ms_per_step, fwd_avg, fwd_tflops
                      "peak_kind": f"bf16 sustained, {pk['source']}", "traffic": None},
         "cpu_baseline": None,
         "e2e": None,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": plan_launches(w)[0] * args.steps,
         "clocks": clocks.summary(),
     }
 
