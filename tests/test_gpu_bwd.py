@@ -57,6 +57,7 @@ def test_tiny_workload(ga, det):
     (1, 200, 3, 1, 64, -1, 2),    # odd group
     (1, 384, 2, 2, 128, -1, 3),   # g = 1
     (1, 640, 4, 2, 128, 0, 4),    # window 0
+    (2, 6000, 2, 1, 128, 700, 5),  # plan above 4096 class bytes: the parallel plan kernels
 ])
 def test_random_packing(ga, b, s, hq, hkv, d, window, seed, det):
     q, k, v, dout = workload.qkv(b, s, hq, hkv, d, seed=seed, with_dout=True)

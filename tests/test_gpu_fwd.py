@@ -59,6 +59,7 @@ def test_tiny_workload(ga):
     (2, 300, 4, 2, 256, 70, 6),     # d = 256 (one head per CTA), ragged tail
     (1, 520, 3, 1, 256, -1, 7),     # d = 256, odd group size
     (1, 1000, 2, 2, 256, 0, 8),     # d = 256, window 0
+    (2, 6000, 2, 1, 128, 700, 9),   # plan above 4096 class bytes: the parallel plan kernels
 ])
 def test_random_packing(ga, b, s, hq, hkv, d, window, seed):
     q, k, v = workload.qkv(b, s, hq, hkv, d, seed=seed)

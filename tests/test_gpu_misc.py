@@ -80,15 +80,19 @@ def test_plan_bit_exact_on_workloads(ga, name):
     _plan_case(ga, ids, pos, w.window_left)
 
 
-@pytest.mark.parametrize("seed,s,window", [(1, 1000, -1), (2, 777, 40), (3, 1300, 0)])
+# up to 4096 class bytes (b * nq * nk) the plan runs in one CTA, above it as
+# the parallel kernels: random packings and cross descriptors on both paths
+@pytest.mark.parametrize("seed,s,window", [(1, 1000, -1), (2, 777, 40), (3, 1300, 0),
+                                           (4, 9000, -1), (5, 8500, 300), (6, 10000, 0)])
 def test_plan_bit_exact_on_random_packing(ga, seed, s, window):
     ids, pos = workload.random_segments(2, s, seed=seed)
     _plan_case(ga, ids, pos, window)
 
 
-def test_plan_cross_descriptor(ga):
-    ids, pos = workload.segments(1, 1024, None)
-    kv_ids, kv_pos = ids[:, 256:768].contiguous(), pos[:, 256:768].contiguous()
+@pytest.mark.parametrize("s,lo,hi", [(1024, 256, 768), (12000, 3000, 9500)])
+def test_plan_cross_descriptor(ga, s, lo, hi):
+    ids, pos = workload.segments(1, s, None)
+    kv_ids, kv_pos = ids[:, lo:hi].contiguous(), pos[:, lo:hi].contiguous()
     _plan_case(ga, ids, pos, 100, kv_ids, kv_pos)
 
 
